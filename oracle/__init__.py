@@ -1,0 +1,23 @@
+"""CPU oracle of the routed-expert block-quantized MoE FFN (numpy, float64).
+
+TEST INFRASTRUCTURE. Only the test suite, `__graft_entry__.smoke()` and the
+benchmark's `cpu_baseline` / `--impl reference` legs may import or call anything
+here. It shares no code, tables or helpers with the CUDA library under
+`block_quantized_moe_gb300/`, and neither imports the other.
+
+Parity status per function (what pins it is in tests/test_oracle_*.py):
+  formats.encode_e4m3 / decode_e4m3   pinned: OCP table values, torch float8_e4m3fn (exhaustive)
+  formats.encode_e2m1 / decode_e2m1   pinned: OCP E2M1 magnitudes, every midpoint, saturation
+  formats.round_to_bf16               pinned: torch bfloat16 conversion
+  moe.quantize_act_fp8 / weight_fp8   pinned: closed forms (a 448 code in every nonzero group,
+                                      exact power-of-two scales, round trip of representable values)
+  moe.quantize_nvfp4                  pinned: closed forms (exact block/global scales, 6.0 codes)
+  moe.segment_routes                  pinned: brute-force double loop, invariants
+  moe.gather_rows_scales              pinned: identity map, duplicate rows, empty map
+  moe.gemm_rows / moe_forward         pinned: brute-force dense FFN per token, one-hot columns,
+                                      inactive-slot invariants
+  moe.silu_mul                        pinned: scipy.special.expit, closed-form points
+  moe.combine                         pinned: single route of weight 1, all inactive
+  moe.pick_tile                       pinned: the dsfp4 page's table (tests/golden)
+"""
+from . import formats, moe  # noqa: F401
