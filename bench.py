@@ -1,0 +1,453 @@
+"""Benchmark of the routed-expert block-quantized MoE FFN on GB300 (libftmoe).
+
+Default workload: the decode sweep geometry -- hidden 4096, intermediate 1024, 64-expert
+FP8 bank with 128x128 block scales, top-k 8, batch 8 tokens, all 8 routes active --
+replayed from one CUDA graph while the routes and inputs change between steps.
+A step is one ftmoe_moe_forward (quantize -> gate/up -> SiLU-and-mul -> down ->
+combine). Other workloads (--workload) are available for measurement runs.
+
+Timing: W warm-up steps, then K timed steps; before every step the inputs of the
+next route set are copied into the graph's input buffers and L2 is flushed (a 512 MiB
+write), both outside the timed events; each step is bracketed by CUDA events on the
+launching stream; barrier + synchronize on both sides of the timed loop; max over
+ranks. `value` is microseconds per call for the whole job (time / calls of all ranks).
+
+Prints one JSON line. --impl reference times the CPU oracle instead (host cores).
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+# the CPU oracle legs use one BLAS thread so the reported core count is exact
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+WORKLOADS = {
+    # name: (tokens, hidden, inter, experts, topk, active per token, path)
+    "decode-h4096-i1024-e64-t8-a8": (8, 4096, 1024, 64, 8, 8, 1),
+    "decode-h4096-i1024-e64-t1-a8": (1, 4096, 1024, 64, 8, 8, 1),
+    "decode-h4096-i1024-e64-t8-a2": (8, 4096, 1024, 64, 8, 2, 1),
+    "decode-h2048-i768-e8-t1-a2": (1, 2048, 768, 8, 8, 2, 1),
+}
+DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (replicas: each rank runs its own copy of the workload)
+# ------------------------------------------------------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# workload construction (inputs resident in HBM before timing starts)
+# ------------------------------------------------------------------------------------
+
+class DecodeWorkload:
+    NSETS = 8  # route/input sets rotated between steps
+
+    def __init__(self, name, device, seed=0xF7E00002):
+        import block_quantized_moe_gb300 as ft
+        self.ft = ft
+        T, H, I, E, k, active, path = WORKLOADS[name]
+        self.name, self.T, self.H, self.I, self.E, self.k, self.active, self.path = name, T, H, I, E, k, active, path
+        self.dev = device
+        gq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
+        gs = torch.empty(E, -(-2 * I // 128), -(-H // 128), dtype=torch.float32, device=device)
+        dq = torch.empty(E, H, I, dtype=torch.uint8, device=device)
+        ds = torch.empty(E, -(-H // 128), -(-I // 128), dtype=torch.float32, device=device)
+        for e in range(E):
+            ft.ftmoe_quantize_weights(synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", device)[None],
+                                      gq[e:e + 1], gs[e:e + 1])
+            ft.ftmoe_quantize_weights(synth.expert_weight_fp32(H, I, seed, e, "down", device)[None],
+                                      dq[e:e + 1], ds[e:e + 1])
+        self.gq, self.gs, self.dq, self.ds = gq, gs, dq, ds
+        self.bank_gu, self.bank_dn = ft.make_bank(gq, gs), ft.make_bank(dq, ds)
+        self.sets = []
+        for i in range(self.NSETS):
+            s = seed + 17 * (i + 1)
+            self.sets.append((synth.activations_bf16(T, H, s, device),
+                              synth.routes(T, k, E, s, active_per_token=active, device=device),
+                              synth.routing_weights(T, k, s, device)))
+        self.shape = ft.moe_shape(T, H, I, k, E, path=path)
+        self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
+        self.x_in = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
+        self.w_in = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.launches_per_step = 5
+
+    # algorithmic bytes/flops of one forward on route set i
+    def work(self, i):
+        _, ids, _ = self.sets[i]
+        ids = ids.cpu().numpy()
+        T, H, I, k = self.T, self.H, self.I, self.k
+        uniq = len(set(int(e) for e in ids.reshape(-1) if e >= 0))
+        act_routes = int((ids >= 0).sum())
+        R = T * k
+        w_gu = 2 * I * H + 4 * (-(-2 * I // 128)) * (-(-H // 128))
+        w_dn = H * I + 4 * (-(-H // 128)) * (-(-I // 128))
+        gateup_bytes = uniq * w_gu + T * (H + 4 * (-(-H // 128))) + R * 2 * I * 4
+        total = (T * H * 2 + T * (H + 4 * (-(-H // 128))) + T * k * 8  # x in, x_q out, routes
+                 + gateup_bytes                                      # gate/up kernel
+                 + R * 2 * I * 4 + R * (I + 4 * (-(-I // 128)))      # silu_mul in/out
+                 + uniq * w_dn + R * (I + 4 * (-(-I // 128))) + R * H * 4  # down kernel
+                 + act_routes * H * 4 + T * H * 2)                   # combine
+        flops = 2 * act_routes * (2 * I * H + H * I)
+        return dict(bytes=total, gateup_bytes=gateup_bytes, flops=flops, uniq=uniq, active=act_routes)
+
+    def load_set(self, i):
+        x, ids, w = self.sets[i]
+        self.x_in.copy_(x)
+        self.ids_in.copy_(ids)
+        self.w_in.copy_(w)
+
+    def forward(self, stream=None):
+        self.ft.ftmoe_moe_forward(self.shape, self.x_in, self.ids_in, self.w_in, self.bank_gu, self.bank_dn,
+                                  self.out, self.ws, stream=stream)
+
+    def dominant_kernel(self):
+        """The gate/up streaming GEMM alone, on the quantized rows the forward left in the workspace."""
+        ft = self.ft
+        lay = ft.ftmoe_forward_workspace_layout(self.shape)
+        xq = self.ws[lay["x_q"]:lay["x_q"] + self.T * self.H].view(self.T, self.H)
+        xs = self.ws[lay["x_scales"]:lay["x_scales"] + self.T * (-(-self.H // 128)) * 4].view(torch.float32).view(self.T, -1)
+        gu = self.ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(self.T * self.k, -1)
+        act = ft.make_act(xq, xs)
+        routes = ft.slot_routes(self.ids_in)
+        return lambda: ft.ftmoe_grouped_gemm_gateup(act, routes, self.bank_gu, gu, variant=1)
+
+
+def time_events(fn, prep, steps, stream):
+    """Sum of per-call CUDA-event durations (ms) over `steps` calls; prep() runs outside."""
+    total = 0.0
+    evs = []
+    for i in range(steps):
+        prep(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        total += e0.elapsed_time(e1)
+    return total
+
+
+def run_gpu(args, rank, world, local):
+    import block_quantized_moe_gb300 as ft
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = DecodeWorkload(args.workload, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def prep(i):
+        wl.load_set(i % wl.NSETS)
+        flush.zero_()
+
+    # eager warm-up, then capture one graph of the whole forward
+    wl.load_set(0)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        wl.forward(stream=side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        wl.forward()
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        prep(i)
+        graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    ms = time_events(graph.replay, prep, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world, dev)
+    us_per_call_rank = ms_max * 1e3 / args.steps
+    value = ms_max * 1e3 / (args.steps * world)
+
+    # algorithmic work averaged over the sets the timed steps used
+    works = [wl.work(i % wl.NSETS) for i in range(args.steps)]
+    bytes_avg = float(np.mean([w["bytes"] for w in works]))
+    flops_avg = float(np.mean([w["flops"] for w in works]))
+    gu_bytes_avg = float(np.mean([w["gateup_bytes"] for w in works]))
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+    fp8_peak = 2.0 * bf16_peak  # dense FP8 = 2x bf16 (nominal ratio 4.5 / 2.25)
+
+    # dominant kernel alone: gate/up streaming GEMM, events on its launching stream
+    kern = wl.dominant_kernel()
+    for i in range(3):
+        prep(i)
+        kern()
+    kms = time_events(kern, prep, args.steps, stream)
+    k_us = kms * 1e3 / args.steps
+    k_gbs = gu_bytes_avg / (k_us * 1e-6) / 1e9
+
+    # end to end through the public API: pinned host inputs -> device, forward, output -> host
+    hx = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16, pin_memory=True) for _ in range(wl.NSETS)]
+    hids = [torch.empty(wl.T, wl.k, dtype=torch.int32, pin_memory=True) for _ in range(wl.NSETS)]
+    hw = [torch.empty(wl.T, wl.k, dtype=torch.float32, pin_memory=True) for _ in range(wl.NSETS)]
+    for i, (x, ids, w) in enumerate(wl.sets):
+        hx[i].copy_(x)
+        hids[i].copy_(ids)
+        hw[i].copy_(w)
+    hout = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e_step(i):
+        j = i % wl.NSETS
+        wl.x_in.copy_(hx[j], non_blocking=True)
+        wl.ids_in.copy_(hids[j], non_blocking=True)
+        wl.w_in.copy_(hw[j], non_blocking=True)
+        graph.replay()
+        hout.copy_(wl.out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_total = 0.0
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step(i)
+        torch.cuda.synchronize()
+        e2e_total += time.perf_counter() - t0
+    e2e_us = max_over_ranks(e2e_total, world, dev) * 1e6 / (args.steps * world)
+    h2d = wl.T * wl.H * 2 + wl.T * wl.k * 4 * 2
+    d2h = wl.T * wl.H * 2
+
+    result = {
+        "metric": "MoE FFN us/call",
+        "value": round(value, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8-e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
+        "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
+                   "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
+                   "l2": "flushed before every timed step (512 MiB write)", "parallelism": f"replicas x{world}",
+                   "graph": "one CUDA graph replayed; inputs copied in place between steps"},
+        "us_per_call_per_gpu": round(us_per_call_rank, 3),
+        "hbm_gbs": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9, 1),
+        "hbm_frac_of_peak": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9 / hbm_peak, 4),
+        "fp8_tflops": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12, 3),
+        "fp8_frac_of_dense_peak": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12 / fp8_peak, 5),
+        "algorithmic_bytes_per_call": int(bytes_avg),
+        "roofline": {"kernel": "stream_gemm_kernel (gate/up, route slots)", "bound": "hbm",
+                     "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(k_gbs / hbm_peak, 4), "traffic": None,
+                     "launch_us": round(k_us, 3), "algorithmic_bytes_per_launch": int(gu_bytes_avg),
+                     "peak_source": peak_src},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl.name, budget_s=args.cpu_budget)
+    return result
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------
+
+def _oracle_problem(name, seed=0xF7E00002):
+    from oracle import moe as M
+    T, H, I, E, k, active, _ = WORKLOADS[name]
+    x = synth.activations_bf16(T, H, seed + 17, "cpu")
+    ids = synth.routes(T, k, E, seed + 17, active_per_token=active, device="cpu")
+    w = synth.routing_weights(T, k, seed + 17, "cpu")
+    used = sorted(set(int(e) for e in ids.view(-1).tolist() if e >= 0))
+    bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I)
+    bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H)
+    for e in used:  # the quantized bank is an input; build it before timing
+        bg.parts(e)
+        bd.parts(e)
+    return M, x.float().numpy(), ids.numpy(), w.numpy(), bg, bd, T
+
+
+def cpu_baseline(name, budget_s=20.0, repeats=None):
+    """Time the oracle's forward on a bounded sample of tokens; scale to one full call."""
+    M, x, ids, w, bg, bd, T = _oracle_problem(name)
+    t0 = time.perf_counter()
+    done = 0
+    toks = []
+    while done < T and (time.perf_counter() - t0) < budget_s:
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[done])
+        toks.append(done)
+        done += 1
+    el = time.perf_counter() - t0
+    per_call = el / len(toks) * T
+    return {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+            "sample": f"{len(toks)} of {T} tokens of one call (numpy float64, single thread), "
+                      f"{el:.1f} s of CPU work, scaled to the full call"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    M, x, ids, w, bg, bd, T = _oracle_problem(args.workload)
+    for i in range(args.warmup):
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % T])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % T])
+    el = time.perf_counter() - t0
+    us = el / args.steps * T * 1e6
+    return {"impl": "reference", "metric": "MoE FFN us/call", "value": round(us, 1), "unit": "us/call",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: 1 of {T} tokens of one call, scaled to the full call"},
+            "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ftmoe", choices=["ftmoe", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_gpu(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

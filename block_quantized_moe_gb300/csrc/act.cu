@@ -1,0 +1,240 @@
+// SiLU-and-mul with re-quantization, and the routing-weighted top-k combine.
+//
+// The FreeToken decode page ("perf(moe): skip inactive block-fp8 decode routes") has the
+// activation and the reduction read the whole gate/up and down buffers, including the
+// zero tiles of inactive routes; zero rows here give scale 0 and zero codes, and the
+// combine skips inactive slots without reading their routing weight.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ftmoe {
+
+__device__ __forceinline__ float silu_mul_1(float g, float u) {
+  return g / (1.0f + expf(-g)) * u;
+}
+
+// One warp per (row, 128 outputs); lane owns 4 consecutive outputs.
+template <bool kVec>
+__global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
+    const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
+    const int32_t* __restrict__ rows_dev, uint8_t* __restrict__ q, float* __restrict__ s,
+    int64_t ng) {
+  int64_t limit = rows;
+  if (rows_dev != nullptr) {
+    const int64_t d = *rows_dev;
+    limit = d < limit ? d : limit;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < limit * ng;
+       w += nwarps) {
+    const int64_t row = w / ng, g = w - row * ng;
+    const int64_t c0 = g * kGroup + lane * 4;
+    const float* gr = gu + row * ld;
+    float a[4];
+    const bool full = c0 + 4 <= inter;
+    if (kVec && full) {
+      const float4 gv = *reinterpret_cast<const float4*>(gr + c0);
+      const float4 uv = *reinterpret_cast<const float4*>(gr + inter + c0);
+      a[0] = silu_mul_1(gv.x, uv.x);
+      a[1] = silu_mul_1(gv.y, uv.y);
+      a[2] = silu_mul_1(gv.z, uv.z);
+      a[3] = silu_mul_1(gv.w, uv.w);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = (c0 + i < inter) ? silu_mul_1(gr[c0 + i], gr[inter + c0 + i]) : 0.0f;
+    }
+    float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
+    amax = warp_max(amax);
+    const float sc = div_rn(amax, kE4M3Max);
+    uint32_t codes = 0;
+    if (amax > 0.0f) {
+      codes = (uint32_t)f2_to_e4m3x2(div_rn(a[0], sc), div_rn(a[1], sc)) |
+              ((uint32_t)f2_to_e4m3x2(div_rn(a[2], sc), div_rn(a[3], sc)) << 16);
+    }
+    uint8_t* qr = q + row * inter;
+    if (kVec && full) {
+      *reinterpret_cast<uint32_t*>(qr + c0) = codes;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c0 + i < inter) qr[c0 + i] = (uint8_t)(codes >> (8 * i));
+    }
+    if (lane == 0) s[row * ng + g] = sc;
+  }
+}
+
+static int grid_cap(int64_t blocks) {
+  const int64_t cap = 152 * 32;
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                                const int32_t* rows_dev, uint8_t* q, float* scales,
+                                cudaStream_t st) {
+  const int64_t ng = cdiv(inter, kGroup);
+  const bool vec = (ld_gu % 4 == 0) && (inter % 4 == 0) && ((uintptr_t)gu % 16 == 0) &&
+                   ((uintptr_t)q % 4 == 0);
+  const int grid = grid_cap(cdiv(rows * ng, 8));
+  if (vec)
+    silu_mul_fp8_kernel<true><<<grid, 256, 0, st>>>(gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
+  else
+    silu_mul_fp8_kernel<false><<<grid, 256, 0, st>>>(gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
+  return cudaGetLastError();
+}
+
+// ---- NVFP4: pass 1 amax of a over the valid rows, pass 2 quantize, pass 3 amax -> g ----
+__global__ void __launch_bounds__(256) silu_amax_kernel(const float* __restrict__ gu, int64_t rows,
+                                                        int64_t inter, int64_t ld,
+                                                        const int32_t* __restrict__ rows_dev,
+                                                        float* __restrict__ amax_out) {
+  int64_t limit = rows;
+  if (rows_dev != nullptr) {
+    const int64_t d = *rows_dev;
+    limit = d < limit ? d : limit;
+  }
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < limit * inter;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / inter, c = i - r * inter;
+    m = fmaxf(m, fabsf(silu_mul_1(gu[r * ld + c], gu[r * ld + inter + c])));
+  }
+  m = warp_max(m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < 8 ? red[threadIdx.x] : 0.0f;
+    m = warp_max(m);
+    if (threadIdx.x == 0 && m > 0.0f) atomic_max_pos(amax_out, m);
+  }
+}
+
+__global__ void __launch_bounds__(256) silu_quant_nvfp4_kernel(
+    const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
+    const int32_t* __restrict__ rows_dev, const float* __restrict__ amax_in,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sb) {
+  int64_t limit = rows;
+  if (rows_dev != nullptr) {
+    const int64_t d = *rows_dev;
+    limit = d < limit ? d : limit;
+  }
+  const int64_t nblk = inter / kNvfp4Block;
+  const float g = div_rn(amax_in[0], kE4M3Max * kE2M1Max);
+  const float six_g = kE2M1Max * g;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < limit * nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = b / nblk, c0 = (b - r * nblk) * kNvfp4Block;
+    float v[16];
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[i] = silu_mul_1(gu[r * ld + c0 + i], gu[r * ld + inter + c0 + i]);
+      am = fmaxf(am, fabsf(v[i]));
+    }
+    uint8_t code_s = 0;
+    float eff = 0.0f;
+    if (g > 0.0f) {
+      code_s = f_to_e4m3(div_rn(am, six_g));
+      eff = e4m3_to_f(code_s) * g;
+    }
+    uint32_t lo = 0, hi = 0;
+    if (eff != 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        lo |= (uint32_t)f2_to_e2m1x2(div_rn(v[2 * i], eff), div_rn(v[2 * i + 1], eff)) << (8 * i);
+        hi |= (uint32_t)f2_to_e2m1x2(div_rn(v[8 + 2 * i], eff), div_rn(v[8 + 2 * i + 1], eff)) << (8 * i);
+      }
+    }
+    *reinterpret_cast<uint2*>(q + r * (inter / 2) + c0 / 2) = make_uint2(lo, hi);
+    sb[r * nblk + c0 / kNvfp4Block] = code_s;
+  }
+}
+
+__global__ void amax_to_gscale_1(float* g) { g[0] = div_rn(g[0], kE4M3Max * kE2M1Max); }
+
+cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                                  const int32_t* rows_dev, uint8_t* q, uint8_t* scales,
+                                  float* gscale, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(gscale, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  silu_amax_kernel<<<grid_cap(cdiv(rows * inter, 256 * 8)), 256, 0, st>>>(gu, rows, inter, ld_gu,
+                                                                           rows_dev, gscale);
+  silu_quant_nvfp4_kernel<<<grid_cap(cdiv(rows * inter / kNvfp4Block, 256)), 256, 0, st>>>(
+      gu, rows, inter, ld_gu, rows_dev, gscale, q, scales);
+  amax_to_gscale_1<<<1, 1, 0, st>>>(gscale);
+  return cudaGetLastError();
+}
+
+// ---- combine: out[t, h] = bf16( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
+template <bool kVec>
+__global__ void __launch_bounds__(128) combine_kernel(
+    const float* __restrict__ y, int64_t ld_y, const int32_t* __restrict__ route2dst,
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t tokens, int32_t topk,
+    int64_t hidden, uint16_t* __restrict__ out, int64_t ld_out) {
+  const int64_t t = blockIdx.y;
+  const int64_t h0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (h0 >= hidden) return;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int j = 0; j < topk; ++j) {
+    const int64_t r = t * topk + j;
+    if (ids[r] < 0) continue;  // inactive: neither the weight nor the row is read
+    const float wt = w[r];
+    const int64_t row = route2dst != nullptr ? (int64_t)route2dst[r] : r;
+    if (row < 0) continue;
+    const float* yr = y + row * ld_y + h0;
+    if (kVec && h0 + 4 <= hidden) {
+      const float4 v = *reinterpret_cast<const float4*>(yr);
+      acc[0] = fmaf(wt, v.x, acc[0]);
+      acc[1] = fmaf(wt, v.y, acc[1]);
+      acc[2] = fmaf(wt, v.z, acc[2]);
+      acc[3] = fmaf(wt, v.w, acc[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (h0 + i < hidden) acc[i] = fmaf(wt, yr[i], acc[i]);
+    }
+  }
+  uint16_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
+  uint16_t* o = out + t * ld_out + h0;
+  if (kVec && h0 + 4 <= hidden) {
+    *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16),
+                                              (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (h0 + i < hidden) o[i] = b[i];
+  }
+}
+
+cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
+                           const int32_t* ids, const float* w, int64_t tokens, int32_t topk,
+                           int64_t hidden, uint16_t* out, int64_t ld_out, cudaStream_t st) {
+  if (tokens > 65535) {
+    // one launch per 65535-token slab keeps grid.y in range
+    for (int64_t t0 = 0; t0 < tokens; t0 += 65535) {
+      const int64_t tn = tokens - t0 < 65535 ? tokens - t0 : 65535;
+      cudaError_t e = launch_combine(y, ld_y, route2dst ? route2dst + t0 * topk : nullptr,
+                                     ids + t0 * topk, w + t0 * topk, tn, topk, hidden,
+                                     out + t0 * ld_out, ld_out, st);
+      if (e != cudaSuccess) return e;
+      if (route2dst == nullptr) y += tn * topk * ld_y;
+    }
+    return cudaSuccess;
+  }
+  const bool vec = (hidden % 4 == 0) && (ld_y % 4 == 0) && ((uintptr_t)y % 16 == 0) &&
+                   (ld_out % 4 == 0) && ((uintptr_t)out % 8 == 0);
+  dim3 grid((unsigned)cdiv(hidden, 4 * 128), (unsigned)tokens);
+  if (vec)
+    combine_kernel<true><<<grid, 128, 0, st>>>(y, ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
+  else
+    combine_kernel<false><<<grid, 128, 0, st>>>(y, ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
+  return cudaGetLastError();
+}
+
+FTMOE_DEFINE_ERR_READER(read_err_act)
+
+}  // namespace ftmoe

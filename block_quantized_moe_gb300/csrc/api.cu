@@ -1,0 +1,397 @@
+// C ABI of libftmoe: argument validation on the host, then kernel launches on the
+// caller's stream. Nothing here allocates, frees or synchronises (except
+// ftmoe_read_error_flags), so every entry point can be captured in a CUDA graph.
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace ftmoe;
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline ftmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FTMOE_OK : FTMOE_CUDA_ERROR; }
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool valid_format(int32_t f) { return f == FTMOE_FMT_FP8 || f == FTMOE_FMT_NVFP4; }
+
+// bytes of one quantized row of k elements and of its scale row
+size_t code_row_bytes(int32_t fmt, int64_t k) { return fmt == FTMOE_FMT_FP8 ? (size_t)k : (size_t)(k / 2); }
+size_t scale_row_bytes(int32_t fmt, int64_t k) {
+  return fmt == FTMOE_FMT_FP8 ? (size_t)cdiv(k, kGroup) * 4 : (size_t)(k / kNvfp4Block);
+}
+
+int pick_tile_value(int64_t routes, int32_t E) {
+  const int64_t per = cdiv(routes, E);
+  const int cand[4] = {16, 32, 64, 128};
+  for (int m : cand)
+    if (m >= per) return m;
+  return 128;
+}
+
+ftmoe_status check_bank(const ftmoe_expert_bank* w) {
+  if (!w || !w->q || !w->scales) return FTMOE_INVALID_ARG;
+  if (w->num_experts <= 0 || w->n <= 0 || w->k <= 0 || !valid_format(w->format)) return FTMOE_INVALID_ARG;
+  if (w->format == FTMOE_FMT_NVFP4 && (!w->global_scale || w->k % 32 != 0)) return FTMOE_INVALID_ARG;
+  return FTMOE_OK;
+}
+
+ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const ftmoe_expert_bank* w,
+                          float* out, int64_t ld_out, const ftmoe_tile* tile, void* stream,
+                          bool is_down) {
+  if (!a || !routes || !out) return FTMOE_INVALID_ARG;
+  ftmoe_status st = check_bank(w);
+  if (st != FTMOE_OK) return st;
+  if (a->format != w->format || a->k != w->k || a->rows < 0 || ld_out < w->n) return FTMOE_INVALID_ARG;
+  if (a->rows > 0 && (!a->q || !a->scales)) return FTMOE_INVALID_ARG;
+  if (tile && tile->tok_tile != 0 && tile->tok_tile != 16 && tile->tok_tile != 32 &&
+      tile->tok_tile != 64 && tile->tok_tile != 128)
+    return FTMOE_INVALID_ARG;
+  if (tile && (tile->variant < 0 || tile->variant > 2)) return FTMOE_INVALID_ARG;
+  const int variant = tile ? tile->variant : 0;
+  if (w->format != FTMOE_FMT_FP8) return FTMOE_UNSUPPORTED;  // NVFP4 GEMMs: grouped path only (below)
+
+  if (routes->kind == FTMOE_ROUTES_SLOTS) {
+    if (!routes->slots || routes->tokens < 0 || routes->topk <= 0) return FTMOE_INVALID_ARG;
+    const int64_t R = routes->tokens * routes->topk;
+    if (R == 0) return FTMOE_OK;
+    const int64_t need_rows = is_down ? R : routes->tokens;
+    if (a->rows < need_rows) return FTMOE_INVALID_ARG;
+    if (variant == 2) return FTMOE_UNSUPPORTED;
+    StreamGemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.a_q = a->q;
+    g.a_s = static_cast<const float*>(a->scales);
+    g.w_q = w->q;
+    g.w_s = static_cast<const float*>(w->scales);
+    g.out = out;
+    g.ld_out = ld_out;
+    g.n = w->n;
+    g.k = w->k;
+    g.E = w->num_experts;
+    g.grouped = 0;
+    g.slots = routes->slots;
+    g.routes = R;
+    g.act_div = is_down ? 1 : routes->topk;
+    return from_cuda(launch_stream_gemm(g, as_stream(stream)));
+  }
+  if (routes->kind != FTMOE_ROUTES_GROUPED || !routes->offsets) return FTMOE_INVALID_ARG;
+  if (a->rows == 0) return FTMOE_OK;
+  if (variant != 1) {
+    TcGemmArgs t;
+    memset(&t, 0, sizeof(t));
+    t.a_q = a->q;
+    t.a_s = static_cast<const float*>(a->scales);
+    t.a_rows = a->rows;
+    t.w_q = w->q;
+    t.w_s = static_cast<const float*>(w->scales);
+    t.out = out;
+    t.ld_out = ld_out;
+    t.n = w->n;
+    t.k = w->k;
+    t.E = w->num_experts;
+    t.offsets = routes->offsets;
+    t.tok_tile = (tile && tile->tok_tile) ? tile->tok_tile : pick_tile_value(a->rows, w->num_experts);
+    int unsupported = 0;
+    cudaError_t e = launch_tc_gemm(t, as_stream(stream), &unsupported);
+    if (!unsupported) return from_cuda(e);
+    if (variant == 2) return FTMOE_UNSUPPORTED;
+  }
+  StreamGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a_q = a->q;
+  g.a_s = static_cast<const float*>(a->scales);
+  g.w_q = w->q;
+  g.w_s = static_cast<const float*>(w->scales);
+  g.out = out;
+  g.ld_out = ld_out;
+  g.n = w->n;
+  g.k = w->k;
+  g.E = w->num_experts;
+  g.grouped = 1;
+  g.offsets = routes->offsets;
+  g.a_rows = a->rows;
+  return from_cuda(launch_stream_gemm(g, as_stream(stream)));
+}
+
+struct Layout {
+  ftmoe_workspace_layout l;
+  bool grouped;
+};
+
+ftmoe_status check_shape(const ftmoe_moe_shape* s) {
+  if (!s) return FTMOE_INVALID_ARG;
+  if (s->tokens < 0 || s->hidden <= 0 || s->inter <= 0 || s->topk <= 0 || s->num_experts <= 0)
+    return FTMOE_INVALID_ARG;
+  if (!valid_format(s->format) || s->path < 0 || s->path > 2) return FTMOE_INVALID_ARG;
+  if (s->tok_tile != 0 && s->tok_tile != 16 && s->tok_tile != 32 && s->tok_tile != 64 && s->tok_tile != 128)
+    return FTMOE_INVALID_ARG;
+  if (s->format == FTMOE_FMT_NVFP4 && (s->hidden % 32 != 0 || s->inter % 32 != 0)) return FTMOE_INVALID_ARG;
+  return FTMOE_OK;
+}
+
+bool use_grouped(const ftmoe_moe_shape* s) {
+  if (s->path == 1) return false;
+  if (s->path == 2) return true;
+  return s->tokens > 8;
+}
+
+Layout make_layout(const ftmoe_moe_shape* s) {
+  Layout L;
+  memset(&L, 0, sizeof(L));
+  L.grouped = use_grouped(s);
+  const int64_t T = s->tokens, H = s->hidden, I = s->inter, R = T * s->topk, E = s->num_experts;
+  const int32_t f = s->format;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.l.x_q = take(T * code_row_bytes(f, H));
+  L.l.x_scales = take(T * scale_row_bytes(f, H));
+  L.l.x_gscale = take(16);
+  if (L.grouped) {
+    L.l.counts = take(E * 4);
+    L.l.offsets = take((E + 1) * 4);
+    L.l.dst2src = take(R * 4);
+    L.l.route2dst = take(R * 4);
+    L.l.rows_q = take(R * code_row_bytes(f, H));
+    L.l.rows_scales = take(R * scale_row_bytes(f, H));
+  }
+  L.l.gateup_bytes = (size_t)R * 2 * I * 4;
+  L.l.gateup = take(L.l.gateup_bytes);
+  L.l.act_q_bytes = R * code_row_bytes(f, I);
+  L.l.act_q = take(L.l.act_q_bytes);
+  L.l.act_scales_bytes = R * scale_row_bytes(f, I);
+  L.l.act_scales = take(L.l.act_scales_bytes);
+  L.l.act_gscale = take(16);
+  L.l.down_bytes = (size_t)R * H * 4;
+  L.l.down = take(L.l.down_bytes);
+  L.l.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ftmoe_status_string(int status) {
+  switch (status) {
+    case FTMOE_OK: return "ok";
+    case FTMOE_INVALID_ARG: return "invalid argument";
+    case FTMOE_UNSUPPORTED: return "unsupported by this build";
+    case FTMOE_CUDA_ERROR: return "CUDA error";
+    case FTMOE_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FTMOE_CHECK_FAILED: return "check failed";
+    default: return "unknown status";
+  }
+}
+
+ftmoe_status ftmoe_pick_tile(int64_t routes, int32_t num_experts, ftmoe_tile* out) {
+  if (!out || routes < 0 || num_experts <= 0) return FTMOE_INVALID_ARG;
+  memset(out, 0, sizeof(*out));
+  out->tok_tile = pick_tile_value(routes, num_experts);
+  return FTMOE_OK;
+}
+
+ftmoe_status ftmoe_quantize_act(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
+                                int32_t format, uint8_t* q, void* scales, float* global_scale,
+                                void* stream) {
+  if (rows < 0 || k <= 0 || ld_x < k || !valid_format(format)) return FTMOE_INVALID_ARG;
+  if (rows == 0) return FTMOE_OK;
+  if (!x || !q || !scales) return FTMOE_INVALID_ARG;
+  if (format == FTMOE_FMT_FP8)
+    return from_cuda(launch_quantize_act_fp8(x, rows, k, ld_x, q, static_cast<float*>(scales),
+                                             as_stream(stream)));
+  if (!global_scale || k % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_quantize_act_nvfp4(x, rows, k, ld_x, q, static_cast<uint8_t*>(scales),
+                                             global_scale, as_stream(stream)));
+}
+
+ftmoe_status ftmoe_quantize_weights(const float* w, int32_t num_experts, int64_t n, int64_t k,
+                                    int32_t format, uint8_t* q, void* scales, float* global_scale,
+                                    void* stream) {
+  if (num_experts < 0 || n <= 0 || k <= 0 || !valid_format(format)) return FTMOE_INVALID_ARG;
+  if (num_experts == 0) return FTMOE_OK;
+  if (!w || !q || !scales) return FTMOE_INVALID_ARG;
+  if (format == FTMOE_FMT_FP8)
+    return from_cuda(launch_quantize_weights_fp8(w, num_experts, n, k, q, static_cast<float*>(scales),
+                                                 as_stream(stream)));
+  if (!global_scale || k % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_quantize_weights_nvfp4(w, num_experts, n, k, q, static_cast<uint8_t*>(scales),
+                                                 global_scale, as_stream(stream)));
+}
+
+ftmoe_status ftmoe_segment_routes(const int32_t* expert_ids, int64_t tokens, int32_t topk,
+                                  int32_t num_experts, int32_t* counts, int32_t* offsets,
+                                  int32_t* dst2src, int32_t* route2dst, void* stream) {
+  if (tokens < 0 || topk <= 0 || num_experts <= 0) return FTMOE_INVALID_ARG;
+  if (!counts || !offsets) return FTMOE_INVALID_ARG;
+  if (tokens > 0 && (!expert_ids || !dst2src || !route2dst)) return FTMOE_INVALID_ARG;
+  if (tokens * (int64_t)topk > 0x7fffffff) return FTMOE_UNSUPPORTED;
+  return from_cuda(launch_segment(expert_ids, tokens * topk, topk, num_experts, counts, offsets,
+                                  dst2src, route2dst, as_stream(stream)));
+}
+
+ftmoe_status ftmoe_gather_rows_scales(const uint8_t* src, const void* src_scales, int64_t n_src,
+                                      int64_t row_bytes, int64_t scale_bytes,
+                                      const int32_t* dst2src, int64_t n_dst,
+                                      const int32_t* n_dst_dev, uint8_t* dst, void* dst_scales,
+                                      void* stream) {
+  if (n_dst < 0 || n_src < 0 || row_bytes <= 0 || scale_bytes < 0) return FTMOE_INVALID_ARG;
+  if (n_dst == 0) return FTMOE_OK;  // zero-row short circuit: nothing is launched
+  if (!src || !dst2src || !dst) return FTMOE_INVALID_ARG;
+  if (scale_bytes > 0 && (!src_scales || !dst_scales)) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_gather(src, static_cast<const uint8_t*>(src_scales), n_src, row_bytes,
+                                 scale_bytes, dst2src, n_dst, n_dst_dev, dst,
+                                 static_cast<uint8_t*>(dst_scales), as_stream(stream)));
+}
+
+ftmoe_status ftmoe_grouped_gemm_gateup(const ftmoe_act* a, const ftmoe_routes* routes,
+                                       const ftmoe_expert_bank* w, float* out, int64_t ld_out,
+                                       const ftmoe_tile* tile, void* stream) {
+  return grouped_gemm(a, routes, w, out, ld_out, tile, stream, false);
+}
+
+ftmoe_status ftmoe_grouped_gemm_down(const ftmoe_act* a, const ftmoe_routes* routes,
+                                     const ftmoe_expert_bank* w, float* out, int64_t ld_out,
+                                     const ftmoe_tile* tile, void* stream) {
+  return grouped_gemm(a, routes, w, out, ld_out, tile, stream, true);
+}
+
+ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                            const int32_t* rows_dev, int32_t format, uint8_t* q, void* scales,
+                            float* global_scale, void* stream) {
+  if (rows < 0 || inter <= 0 || ld_gu < 2 * inter || !valid_format(format)) return FTMOE_INVALID_ARG;
+  if (rows == 0) return FTMOE_OK;
+  if (!gu || !q || !scales) return FTMOE_INVALID_ARG;
+  if (format == FTMOE_FMT_FP8)
+    return from_cuda(launch_silu_mul_fp8(gu, rows, inter, ld_gu, rows_dev, q,
+                                         static_cast<float*>(scales), as_stream(stream)));
+  if (!global_scale || inter % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_silu_mul_nvfp4(gu, rows, inter, ld_gu, rows_dev, q,
+                                         static_cast<uint8_t*>(scales), global_scale,
+                                         as_stream(stream)));
+}
+
+ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
+                           const int32_t* expert_ids, const float* weights, int64_t tokens,
+                           int32_t topk, int64_t hidden, uint16_t* out, int64_t ld_out,
+                           void* stream) {
+  if (tokens < 0 || topk <= 0 || hidden <= 0 || ld_y < hidden || ld_out < hidden) return FTMOE_INVALID_ARG;
+  if (tokens == 0) return FTMOE_OK;
+  if (!y || !expert_ids || !weights || !out) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_combine(y, ld_y, route2dst, expert_ids, weights, tokens, topk, hidden, out,
+                                  ld_out, as_stream(stream)));
+}
+
+size_t ftmoe_forward_workspace_bytes(const ftmoe_moe_shape* shape) {
+  if (check_shape(shape) != FTMOE_OK) return 0;
+  return make_layout(shape).l.total;
+}
+
+ftmoe_status ftmoe_forward_workspace_layout(const ftmoe_moe_shape* shape, ftmoe_workspace_layout* out) {
+  if (!out) return FTMOE_INVALID_ARG;
+  ftmoe_status st = check_shape(shape);
+  if (st != FTMOE_OK) return st;
+  *out = make_layout(shape).l;
+  return FTMOE_OK;
+}
+
+ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!args) return FTMOE_INVALID_ARG;
+  const ftmoe_moe_shape* s = &args->shape;
+  ftmoe_status st = check_shape(s);
+  if (st != FTMOE_OK) return st;
+  st = check_bank(&args->w_gateup);
+  if (st != FTMOE_OK) return st;
+  st = check_bank(&args->w_down);
+  if (st != FTMOE_OK) return st;
+  const int64_t T = s->tokens, H = s->hidden, I = s->inter, E = s->num_experts;
+  const int32_t f = s->format;
+  const ftmoe_expert_bank& wg = args->w_gateup;
+  const ftmoe_expert_bank& wd = args->w_down;
+  if (wg.format != f || wd.format != f || wg.num_experts != E || wd.num_experts != E ||
+      wg.n != 2 * I || wg.k != H || wd.n != H || wd.k != I)
+    return FTMOE_INVALID_ARG;
+  if (args->ld_x < H || args->ld_out < H) return FTMOE_INVALID_ARG;
+  if (T == 0) return FTMOE_OK;
+  if (!args->x || !args->expert_ids || !args->route_weights || !args->out) return FTMOE_INVALID_ARG;
+  const Layout L = make_layout(s);
+  if (!workspace) return FTMOE_INVALID_ARG;
+  if (workspace_bytes < L.l.total) return FTMOE_WORKSPACE_TOO_SMALL;
+  if (f != FTMOE_FMT_FP8) return FTMOE_UNSUPPORTED;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t R = T * s->topk;
+  cudaStream_t strm = as_stream(stream);
+  uint8_t* xq = ws + L.l.x_q;
+  float* xs = reinterpret_cast<float*>(ws + L.l.x_scales);
+  float* gu = reinterpret_cast<float*>(ws + L.l.gateup);
+  uint8_t* aq = ws + L.l.act_q;
+  float* as = reinterpret_cast<float*>(ws + L.l.act_scales);
+  float* y = reinterpret_cast<float*>(ws + L.l.down);
+  ftmoe_tile tile;
+  memset(&tile, 0, sizeof(tile));
+  tile.tok_tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, (int32_t)E);
+
+  st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, nullptr, stream);
+  if (st != FTMOE_OK) return st;
+  if (!L.grouped) {
+    ftmoe_routes rt;
+    memset(&rt, 0, sizeof(rt));
+    rt.kind = FTMOE_ROUTES_SLOTS;
+    rt.topk = s->topk;
+    rt.tokens = T;
+    rt.slots = args->expert_ids;
+    ftmoe_act a1 = {f, 0, T, H, xq, xs, nullptr};
+    st = ftmoe_grouped_gemm_gateup(&a1, &rt, &wg, gu, 2 * I, &tile, stream);
+    if (st != FTMOE_OK) return st;
+    st = ftmoe_silu_mul(gu, R, I, 2 * I, nullptr, f, aq, as, nullptr, stream);
+    if (st != FTMOE_OK) return st;
+    ftmoe_act a2 = {f, 0, R, I, aq, as, nullptr};
+    st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
+    if (st != FTMOE_OK) return st;
+    return ftmoe_combine(y, H, nullptr, args->expert_ids, args->route_weights, T, s->topk, H,
+                         args->out, args->ld_out, stream);
+  }
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.l.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.l.offsets);
+  int32_t* dst2src = reinterpret_cast<int32_t*>(ws + L.l.dst2src);
+  int32_t* route2dst = reinterpret_cast<int32_t*>(ws + L.l.route2dst);
+  uint8_t* rq = ws + L.l.rows_q;
+  float* rs = reinterpret_cast<float*>(ws + L.l.rows_scales);
+  st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src,
+                            route2dst, stream);
+  if (st != FTMOE_OK) return st;
+  st = ftmoe_gather_rows_scales(xq, xs, T, H, (int64_t)scale_row_bytes(f, H), dst2src, R,
+                                offsets + E, rq, rs, stream);
+  if (st != FTMOE_OK) return st;
+  ftmoe_routes rt;
+  memset(&rt, 0, sizeof(rt));
+  rt.kind = FTMOE_ROUTES_GROUPED;
+  rt.offsets = offsets;
+  ftmoe_act a1 = {f, 0, R, H, rq, rs, nullptr};
+  st = ftmoe_grouped_gemm_gateup(&a1, &rt, &wg, gu, 2 * I, &tile, stream);
+  if (st != FTMOE_OK) return st;
+  st = ftmoe_silu_mul(gu, R, I, 2 * I, offsets + E, f, aq, as, nullptr, stream);
+  if (st != FTMOE_OK) return st;
+  ftmoe_act a2 = {f, 0, R, I, aq, as, nullptr};
+  st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
+  if (st != FTMOE_OK) return st;
+  return ftmoe_combine(y, H, route2dst, args->expert_ids, args->route_weights, T, s->topk, H,
+                       args->out, args->ld_out, stream);
+}
+
+ftmoe_status ftmoe_read_error_flags(uint32_t* flags) {
+  if (!flags) return FTMOE_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FTMOE_CUDA_ERROR;
+  *flags = read_err_quant() | read_err_segment() | read_err_gather() | read_err_stream_gemm() |
+           read_err_tc_gemm() | read_err_act();
+  return FTMOE_OK;
+}
+
+}  // extern "C"

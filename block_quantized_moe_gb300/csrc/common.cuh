@@ -1,0 +1,91 @@
+// Device helpers shared by the libftmoe kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp4.h>
+#include <stdint.h>
+
+#include "../../include/ftmoe.h"
+
+namespace ftmoe {
+
+constexpr int kGroup = 128;        // activation group width = weight block edge
+constexpr float kE4M3Max = 448.0f;
+constexpr float kE2M1Max = 6.0f;
+constexpr int kNvfp4Block = 16;
+
+// Each translation unit keeps its own device error word; the host reads all of them.
+// An index read on the device that is out of range is skipped and reported here.
+static __device__ unsigned int g_err_word;
+
+__device__ __forceinline__ void raise_error(unsigned int bit) { atomicOr(&g_err_word, bit); }
+
+#define FTMOE_DEFINE_ERR_READER(fname)                                                \
+  uint32_t fname() {                                                                  \
+    unsigned int v = 0, zero = 0;                                                     \
+    if (cudaMemcpyFromSymbol(&v, ftmoe::g_err_word, sizeof(v)) != cudaSuccess) return 0; \
+    cudaMemcpyToSymbol(ftmoe::g_err_word, &zero, sizeof(zero));                       \
+    return v;                                                                         \
+  }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturate to +-448), packed with
+// the first value in the low byte. Uses the cuda_fp8.h conversion.
+__device__ __forceinline__ uint16_t f2_to_e4m3x2(float a, float b) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint8_t f_to_e4m3(float a) {
+  return (uint8_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_to_f(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Two e4m3 codes (low byte first) -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c2) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+
+// Two floats -> two e2m1 codes in one byte (first value in the low nibble), round to
+// nearest even with saturation to +-6 (cuda_fp4.h conversion).
+__device__ __forceinline__ uint8_t f2_to_e2m1x2(float a, float b) {
+  return (uint8_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+}
+
+__device__ __forceinline__ float2 e2m1x2_to_f2(uint8_t c2) {
+  __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)c2, __NV_E2M1);
+  return __half22float2(__half2(h));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// IEEE single-precision quotient, round to nearest (the build never uses fast math; the
+// explicit intrinsic documents that the quantization decision depends on it).
+__device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
+
+// Positive floats order like their bit patterns, so a max over |x| can use atomicMax on
+// the bits of a zero-initialised word.
+__device__ __forceinline__ void atomic_max_pos(float* addr, float v) {
+  atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
+}  // namespace ftmoe

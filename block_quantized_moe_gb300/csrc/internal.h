@@ -1,0 +1,87 @@
+// Host-side launchers shared between the libftmoe translation units (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ftmoe.h"
+
+namespace ftmoe {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// quant.cu
+cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
+                                    uint8_t* q, float* scales, cudaStream_t s);
+cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
+                                      uint8_t* q, uint8_t* scales, float* gscale, cudaStream_t s);
+cudaError_t launch_quantize_weights_fp8(const float* w, int32_t E, int64_t n, int64_t k,
+                                        uint8_t* q, float* scales, cudaStream_t s);
+cudaError_t launch_quantize_weights_nvfp4(const float* w, int32_t E, int64_t n, int64_t k,
+                                          uint8_t* q, uint8_t* scales, float* gscale,
+                                          cudaStream_t s);
+uint32_t read_err_quant();
+
+// segment.cu
+cudaError_t launch_segment(const int32_t* ids, int64_t routes, int32_t topk, int32_t E,
+                           int32_t* counts, int32_t* offsets, int32_t* dst2src,
+                           int32_t* route2dst, cudaStream_t s);
+uint32_t read_err_segment();
+
+// gather.cu
+cudaError_t launch_gather(const uint8_t* src, const uint8_t* src_scales, int64_t n_src,
+                          int64_t row_bytes, int64_t scale_bytes, const int32_t* dst2src,
+                          int64_t n_dst, const int32_t* n_dst_dev, uint8_t* dst,
+                          uint8_t* dst_scales, cudaStream_t s);
+uint32_t read_err_gather();
+
+// stream_gemm.cu: HBM-streaming CUDA-core GEMM (route slots or grouped rows)
+struct StreamGemmArgs {
+  const uint8_t* a_q;      // activation codes [rows][k]
+  const float* a_s;        // [rows][ceil(k/128)]
+  const uint8_t* w_q;      // [E][n][k]
+  const float* w_s;        // [E][ceil(n/128)][ceil(k/128)]
+  float* out;              // [*][ld_out]
+  int64_t ld_out;
+  int64_t n, k;
+  int32_t E;
+  int32_t grouped;         // 1: GROUPED layout via offsets, 0: SLOTS
+  const int32_t* offsets;  // GROUPED
+  int64_t a_rows;          // GROUPED: rows of the activation and output buffers
+  const int32_t* slots;    // SLOTS
+  int64_t routes;          // SLOTS: tokens * topk
+  int32_t act_div;         // SLOTS: activation row of route r is r / act_div
+};
+cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t s);
+uint32_t read_err_stream_gemm();
+
+// tc_gemm.cu: tcgen05 grouped GEMM
+struct TcGemmArgs {
+  const uint8_t* a_q;
+  const float* a_s;
+  int64_t a_rows;          // allocated rows of the activation buffer
+  const uint8_t* w_q;
+  const float* w_s;
+  float* out;
+  int64_t ld_out;
+  int64_t n, k;
+  int32_t E;
+  const int32_t* offsets;
+  int32_t tok_tile;
+};
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s, int* unsupported);
+uint32_t read_err_tc_gemm();
+
+// act.cu: silu_mul and combine
+cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                                const int32_t* rows_dev, uint8_t* q, float* scales,
+                                cudaStream_t s);
+cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                                  const int32_t* rows_dev, uint8_t* q, uint8_t* scales,
+                                  float* gscale, cudaStream_t s);
+cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
+                           const int32_t* ids, const float* w, int64_t tokens, int32_t topk,
+                           int64_t hidden, uint16_t* out, int64_t ld_out, cudaStream_t s);
+uint32_t read_err_act();
+
+}  // namespace ftmoe

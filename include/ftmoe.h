@@ -1,0 +1,273 @@
+/*
+ * libftmoe -- routed-expert block-quantized MoE FFN for NVIDIA GB300 (sm_103a).
+ *
+ * The path, per token row x of a top-k routed MoE layer:
+ *   1. quantize x once per 1x128 group to FP8-e4m3 with an fp32 scale per group
+ *      (SGLang "Gather the cutlass MoE activation and its scales in one launch",
+ *      Motivation: the activation is quantized once, k//128 fp32 scales beside k fp8);
+ *   2. group the active routes by expert (counts, offsets, dst2src);
+ *   3. gather the FP8 rows and their scale rows in one walk of dst2src
+ *      (same page, Modifications);
+ *   4. grouped gate/up GEMM against FP8 expert weights with 128x128 fp32 block scales
+ *      (FreeToken "perf(moe): skip inactive block-fp8 decode routes", first section);
+ *   5. SiLU-and-mul, re-quantized per 1x128 for the down GEMM;
+ *   6. grouped down GEMM;
+ *   7. routing-weighted top-k combine into bf16.
+ * A negative expert slot is an inactive route: its gate/up and down output tiles are
+ * written as exact zeros and nothing else of it is read (FreeToken page, first section).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in the argument lists are DEVICE pointers unless stated; the caller
+ *     allocates and owns all memory. No entry point allocates, frees or synchronises,
+ *     so every call may be captured into a CUDA graph (ftmoe_read_error_flags excepted).
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     Errors of the asynchronous work surface at the caller's next synchronisation.
+ *   - Argument checks run on the host before anything is enqueued and touch no device
+ *     memory: a NULL pointer that is needed, a negative or inconsistent size or stride
+ *     returns FTMOE_INVALID_ARG; a valid request this build cannot run returns
+ *     FTMOE_UNSUPPORTED; a failed launch returns FTMOE_CUDA_ERROR.
+ *   - A call with zero rows returns FTMOE_OK without launching anything.
+ *   - Sizes and strides are in elements unless named *_bytes. Row bases are computed in
+ *     64-bit. Index arrays are int32.
+ *   - Index values that the kernels read on the device (expert ids, dst2src entries) and
+ *     that fall outside their range are skipped and raise a bit in the device error word
+ *     (ftmoe_read_error_flags); they never cause an out-of-bounds access.
+ */
+#ifndef FTMOE_H
+#define FTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ftmoe_status {
+  FTMOE_OK = 0,
+  FTMOE_INVALID_ARG = 1,
+  FTMOE_UNSUPPORTED = 2,
+  FTMOE_CUDA_ERROR = 3,
+  FTMOE_WORKSPACE_TOO_SMALL = 4,
+  FTMOE_CHECK_FAILED = 5
+} ftmoe_status;
+
+/* Storage formats of weights and activations. */
+typedef enum ftmoe_format {
+  /* FP8-e4m3 codes; activations carry one fp32 scale per 1x128 row group, weights one
+   * fp32 scale per 128x128 block on the padded (ceil-div) grid. value = code * scale. */
+  FTMOE_FMT_FP8 = 0,
+  /* NVFP4: e2m1 codes packed two per byte (even column in the low nibble), one e4m3
+   * scale per 16 consecutive elements of a row, one fp32 scale per tensor.
+   * value = code * block_scale * global_scale. */
+  FTMOE_FMT_NVFP4 = 1
+} ftmoe_format;
+
+/* Device error word bits (see ftmoe_read_error_flags). */
+#define FTMOE_ERR_EXPERT_ID_RANGE 0x1u  /* an expert id >= num_experts was skipped */
+#define FTMOE_ERR_MAP_RANGE 0x2u        /* a dst2src entry outside [0, n_src) was skipped */
+#define FTMOE_ERR_WAIT_TIMEOUT 0x4u     /* a bounded pipeline wait gave up */
+
+/* E expert matrices of shape [n, k] (row = output feature, K-major).
+ * FP8:   q      uint8 [E][n][k]
+ *        scales float [E][ceil(n/128)][ceil(k/128)]
+ * NVFP4: q      uint8 [E][n][k/2]
+ *        scales uint8 (e4m3) [E][n][k/16]
+ *        global_scale float [E]
+ * Gate/up banks hold the gate rows [0, I) then the up rows [I, 2I) of each expert. */
+typedef struct ftmoe_expert_bank {
+  int32_t format;      /* ftmoe_format */
+  int32_t num_experts; /* E */
+  int64_t n;
+  int64_t k;
+  const uint8_t* q;
+  const void* scales;
+  const float* global_scale; /* NVFP4 only; NULL for FP8 */
+} ftmoe_expert_bank;
+
+/* Quantized activation rows [rows, k] in the same formats (FP8: scales float
+ * [rows][ceil(k/128)]; NVFP4: q [rows][k/2], scales e4m3 [rows][k/16], global_scale
+ * float[1]). Rows are dense (row stride k, resp. k/2 bytes). */
+typedef struct ftmoe_act {
+  int32_t format;
+  int32_t reserved;
+  int64_t rows;
+  int64_t k;
+  const uint8_t* q;
+  const void* scales;
+  const float* global_scale;
+} ftmoe_act;
+
+/* How activation rows and output rows relate to experts.
+ * FTMOE_ROUTES_GROUPED: rows are sorted by expert; the rows of expert e are
+ *   [offsets[e], offsets[e+1]) (device int32 [E+1], e.g. from ftmoe_segment_routes).
+ *   Output row i belongs to activation row i. Rows >= offsets[E] are not touched.
+ * FTMOE_ROUTES_SLOTS: one output row per route r in [0, tokens*topk); the route's
+ *   expert is slots[r] (device int32; < 0 = inactive, the output row is written as
+ *   zeros). The activation row of route r is r / topk for the gate/up GEMM (token
+ *   rows) and r for the down GEMM (one intermediate row per route). */
+enum { FTMOE_ROUTES_GROUPED = 0, FTMOE_ROUTES_SLOTS = 1 };
+typedef struct ftmoe_routes {
+  int32_t kind;
+  int32_t topk;           /* SLOTS */
+  int64_t tokens;         /* SLOTS */
+  const int32_t* offsets; /* GROUPED */
+  const int32_t* slots;   /* SLOTS */
+} ftmoe_routes;
+
+/* GEMM kernel choice. variant: 0 = automatic (SLOTS -> the HBM-streaming CUDA-core
+ * kernel, GROUPED -> the tcgen05 tensor-core kernel), 1 = the streaming kernel,
+ * 2 = the tcgen05 kernel. tok_tile: token columns per tensor-core tile, one of
+ * 16/32/64/128; 0 = ftmoe_pick_tile's choice. */
+typedef struct ftmoe_tile {
+  int32_t tok_tile;
+  int32_t variant;
+  int32_t reserved[2];
+} ftmoe_tile;
+
+const char* ftmoe_status_string(int status);
+
+/* Token tile from route density (FreeToken "perf(dsfp4): pick the grouped-prefill tile
+ * from route density on sm_89", Measurements: the best M tile tracks rows per expert,
+ * 16 -> 32 -> 128 at about 6 -> 24 -> 96 rows): the smallest of 16/32/64/128 that holds
+ * ceil(routes / num_experts) rows, else 128. Pure host function; out is a host pointer. */
+ftmoe_status ftmoe_pick_tile(int64_t routes, int32_t num_experts, ftmoe_tile* out);
+
+/* Per-token activation quantization of bf16 x [rows, k] (row stride ld_x elements).
+ * FP8 (SGLang gather page, Motivation): per 1x128 group amax = max|x|,
+ *   s = amax / 448 (IEEE fp32), q = e4m3_rne_satfinite(x / s); amax = 0 gives s = 0 and
+ *   all-zero codes. q uint8 [rows][k]; scales float [rows][ceil(k/128)];
+ *   global_scale must be NULL.
+ * NVFP4 (requires k % 32 == 0): g = amax_tensor / 2688 is written to global_scale[0];
+ *   per 16 elements sb = e4m3(amax_block / (6 g)), q = e2m1_rne(x / (sb g)).
+ *   q uint8 [rows][k/2]; scales uint8 [rows][k/16]. */
+ftmoe_status ftmoe_quantize_act(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
+                                int32_t format, uint8_t* q, void* scales, float* global_scale,
+                                void* stream);
+
+/* Weight-bank quantization of float32 w [E][n][k] (dense) into the layout of
+ * ftmoe_expert_bank: FP8 with one scale per 128x128 block (amax / 448, padded grid),
+ * or NVFP4 with one global scale per expert matrix (requires k % 32 == 0). */
+ftmoe_status ftmoe_quantize_weights(const float* w, int32_t num_experts, int64_t n, int64_t k,
+                                    int32_t format, uint8_t* q, void* scales, float* global_scale,
+                                    void* stream);
+
+/* Expert segmenter: stable grouping of the active routes by expert.
+ * expert_ids int32 [tokens*topk] (route r = t*topk + j; < 0 inactive).
+ * Outputs: counts int32 [E]; offsets int32 [E+1] (exclusive prefix, offsets[E] = active
+ * routes); dst2src int32 [tokens*topk] capacity, entry d < offsets[E] is the token of
+ * grouped row d; route2dst int32 [tokens*topk], the grouped row of route r or -1.
+ * Within an expert rows keep route order. All outputs are deterministic. */
+ftmoe_status ftmoe_segment_routes(const int32_t* expert_ids, int64_t tokens, int32_t topk,
+                                  int32_t num_experts, int32_t* counts, int32_t* offsets,
+                                  int32_t* dst2src, int32_t* route2dst, void* stream);
+
+/* Fused row + scale gather (SGLang gather page, Modifications): one walk of dst2src
+ * copies, for every destination row i, the row_bytes bytes of src row dst2src[i] and
+ * the scale_bytes bytes of its scale row. Bytes are copied, never decoded, so any
+ * 1-byte code format works (FP8: row_bytes = k, scale_bytes = 4*ceil(k/128)).
+ * src [n_src][row_bytes], src_scales [n_src][scale_bytes], dst [n_dst][row_bytes],
+ * dst_scales [n_dst][scale_bytes], all dense. n_dst_dev: optional device int32 holding
+ * the number of valid destination rows (<= n_dst); rows at or beyond it are left
+ * untouched (lets a fixed-size launch follow a device-side count). */
+ftmoe_status ftmoe_gather_rows_scales(const uint8_t* src, const void* src_scales, int64_t n_src,
+                                      int64_t row_bytes, int64_t scale_bytes,
+                                      const int32_t* dst2src, int64_t n_dst,
+                                      const int32_t* n_dst_dev, uint8_t* dst, void* dst_scales,
+                                      void* stream);
+
+/* Grouped gate/up GEMM: out[row, c] = sum over 128-wide K blocks kb of
+ *   act_scale[row, kb] * w_scale[e, c/128, kb] * sum_{k in kb} a[row, k] * w[e, c, k]
+ * for c in [0, w->n) (= 2I), with e the expert of the row (see ftmoe_routes).
+ * a->k must equal w->k (= hidden). out float32, row stride ld_out >= w->n.
+ * FTMOE_ROUTES_SLOTS: an inactive route's row is written as zeros before anything of
+ * that route is read (FreeToken page, first section). tile may be NULL. */
+ftmoe_status ftmoe_grouped_gemm_gateup(const ftmoe_act* a, const ftmoe_routes* routes,
+                                       const ftmoe_expert_bank* w, float* out, int64_t ld_out,
+                                       const ftmoe_tile* tile, void* stream);
+
+/* SiLU-and-mul with re-quantization: for each row, a[i] = silu(g[i]) * u[i] with
+ * g = gu[row, 0:inter], u = gu[row, inter:2*inter], silu(g) = g / (1 + exp(-g)) in fp32;
+ * then a is quantized like ftmoe_quantize_act (FP8: q [rows][inter], scales float
+ * [rows][ceil(inter/128)]; NVFP4: q [rows][inter/2], scales [rows][inter/16],
+ * global_scale float[1] taken over all valid rows). rows_dev: optional device int32
+ * count of valid rows (<= rows); rows beyond it are not touched. An all-zero input
+ * row gives scale 0 and zero codes. */
+ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
+                            const int32_t* rows_dev, int32_t format, uint8_t* q, void* scales,
+                            float* global_scale, void* stream);
+
+/* Grouped down GEMM: the same contraction as ftmoe_grouped_gemm_gateup with
+ * w->n = hidden and w->k = a->k = inter. In FTMOE_ROUTES_SLOTS mode activation row r
+ * belongs to route r. */
+ftmoe_status ftmoe_grouped_gemm_down(const ftmoe_act* a, const ftmoe_routes* routes,
+                                     const ftmoe_expert_bank* w, float* out, int64_t ld_out,
+                                     const ftmoe_tile* tile, void* stream);
+
+/* Routing-weighted top-k combine:
+ *   out[t, h] = bf16_rne( sum_{j ascending, expert_ids[t*topk+j] >= 0}
+ *                         weights[t*topk+j] * y[row(t*topk+j), h] )   (fp32 accumulate)
+ * row(r) = route2dst[r] if route2dst != NULL, else r (route-major y). Inactive slots
+ * are skipped without reading their weight or y row. y float [*, hidden] with row
+ * stride ld_y; out bf16 [tokens, hidden] with row stride ld_out. */
+ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
+                           const int32_t* expert_ids, const float* weights, int64_t tokens,
+                           int32_t topk, int64_t hidden, uint16_t* out, int64_t ld_out,
+                           void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Fused forward. Launch shapes depend only on the shape below, never on route content,
+ * so one captured CUDA graph can be replayed while routes and inputs change in place.
+ * path: 0 = automatic (tokens <= 8 -> route-slot streaming path, else grouped
+ * tensor-core path), 1 = route-slot path, 2 = grouped path.
+ * ------------------------------------------------------------------------------------ */
+typedef struct ftmoe_moe_shape {
+  int64_t tokens;     /* T */
+  int64_t hidden;     /* H */
+  int64_t inter;      /* I (per expert) */
+  int32_t topk;
+  int32_t num_experts;
+  int32_t format;     /* ftmoe_format of weights and activations */
+  int32_t tok_tile;   /* 0 = ftmoe_pick_tile(T*topk, E) */
+  int32_t path;
+  int32_t reserved;
+} ftmoe_moe_shape;
+
+typedef struct ftmoe_moe_args {
+  ftmoe_moe_shape shape;
+  const uint16_t* x;          /* bf16 [T][ld_x] */
+  int64_t ld_x;
+  const int32_t* expert_ids;  /* int32 [T*topk], < 0 inactive */
+  const float* route_weights; /* float [T*topk]; entries of inactive routes are never read */
+  ftmoe_expert_bank w_gateup; /* n = 2I, k = H */
+  ftmoe_expert_bank w_down;   /* n = H, k = I */
+  uint16_t* out;              /* bf16 [T][ld_out] */
+  int64_t ld_out;
+} ftmoe_moe_args;
+
+/* Byte offsets of the intermediate buffers inside the forward workspace (each 256-byte
+ * aligned). Offsets of buffers a path does not use are 0 with size 0. */
+typedef struct ftmoe_workspace_layout {
+  size_t x_q, x_scales, x_gscale;            /* quantized token rows */
+  size_t counts, offsets, dst2src, route2dst; /* segmenter (grouped path) */
+  size_t rows_q, rows_scales;                /* gathered rows (grouped path) */
+  size_t gateup, gateup_bytes;               /* float gate/up output [R][2I] */
+  size_t act_q, act_q_bytes, act_scales, act_scales_bytes, act_gscale;
+  size_t down, down_bytes;                   /* float down output [R][H] */
+  size_t total;
+} ftmoe_workspace_layout;
+
+size_t ftmoe_forward_workspace_bytes(const ftmoe_moe_shape* shape);
+ftmoe_status ftmoe_forward_workspace_layout(const ftmoe_moe_shape* shape,
+                                            ftmoe_workspace_layout* out);
+ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Reads and clears the device error word of the current device (FTMOE_ERR_* bits) into
+ * *flags (host pointer). Synchronises the device; not for use inside graph capture. */
+ftmoe_status ftmoe_read_error_flags(uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FTMOE_H */

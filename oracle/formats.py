@@ -66,19 +66,19 @@ assert np.all(np.diff(_E4M3_POS) > 0) and np.all(np.diff(_E2M1_POS) > 0)
 def _nearest_code(mag: np.ndarray, table: np.ndarray) -> np.ndarray:
     """Index of the nearest entry of `table` to each magnitude, ties to the even index.
 
-    Magnitudes beyond the last entry saturate to it. `mag` must be >= 0 and finite.
-    All differences below are exact in float64 (inputs have <= 24 significant bits).
+    The decision boundaries of round-to-nearest are the midpoints between adjacent
+    entries: a magnitude above the midpoint of entries i and i+1 rounds to i+1, one
+    below it to i, and one exactly on it to whichever of i, i+1 is even. Counting the
+    midpoints strictly below `mag` gives the index for all non-tie inputs; a tie adds
+    one when i+1 is even. Magnitudes beyond the last entry saturate to it (no midpoint
+    lies above the last entry). `mag` must be >= 0 and finite; midpoints of these
+    formats are exact in float32 and float64.
     """
-    hi = np.searchsorted(table, mag, side="left")  # first entry >= mag
-    hi = np.minimum(hi, len(table) - 1)
-    lo = np.maximum(hi - 1, 0)
-    d_lo = mag - table[lo]
-    d_hi = table[hi] - mag
-    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
-    idx = np.where(pick_hi, hi, lo)
-    # at or above the largest finite value: saturate
-    idx = np.where(mag >= table[-1], len(table) - 1, idx)
-    return idx.astype(np.int64)
+    mids = (table[:-1] + table[1:]) / 2
+    below = np.searchsorted(mids, mag, side="left")  # midpoints strictly below mag
+    at = np.minimum(below, len(mids) - 1)
+    tie_up = (mids[at] == mag) & ((at + 1) % 2 == 0)
+    return below + tie_up
 
 
 def encode_e4m3(v) -> np.ndarray:

@@ -123,6 +123,23 @@ def quantize_weight_fp8(w):
     return q, s
 
 
+def quantize_weight_fp8_fast(w):
+    """Same result as quantize_weight_fp8, vectorised over blocks (for large matrices)."""
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    nb, kb = ceil_div(n, GROUP), ceil_div(k, GROUP)
+    pad = np.zeros((nb * GROUP, kb * GROUP), np.float32)
+    pad[:n, :k] = w
+    blocks = pad.reshape(nb, GROUP, kb, GROUP)
+    amax = np.max(np.abs(blocks), axis=(1, 3)).astype(np.float32)  # padding zeros never win
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(amax == 0, np.float32(1), s).astype(np.float32)
+    v = (blocks / safe[:, None, :, None]).astype(np.float32)
+    q = encode_e4m3(v)
+    q[np.broadcast_to((amax == 0)[:, None, :, None], q.shape)] = 0
+    return q.reshape(nb * GROUP, kb * GROUP)[:n, :k].copy(), s
+
+
 def dequant_act_fp8(q, s):
     """[rows, k] codes + [rows, ceil(k/128)] scales -> float64 [rows, k]."""
     q = np.asarray(q)
@@ -310,11 +327,39 @@ class Bank:
 
     def __init__(self, fmt, q, s, g=None):
         self.fmt, self.q, self.s, self.g = fmt, q, s, g
+        self.n = q.shape[1]
 
     def dequant(self, e):
         if self.fmt == "fp8":
             return dequant_weight_fp8(self.q[e], self.s[e])
         return dequant_nvfp4(self.q[e], self.s[e], self.g[e])
+
+
+class LazyBank:
+    """A bank whose experts are quantized on first use from raw(e) -> float32 [n, k].
+
+    Large workloads touch one expert at a time; the result per expert is the same as
+    quantize_bank's.
+    """
+
+    def __init__(self, raw, n, fmt="fp8"):
+        self.raw, self.n, self.fmt = raw, n, fmt
+        self._cache = {}
+
+    def parts(self, e):
+        if e not in self._cache:
+            w = np.asarray(self.raw(e), np.float32)
+            if self.fmt == "fp8":
+                self._cache[e] = quantize_weight_fp8_fast(w)
+            else:
+                self._cache[e] = quantize_nvfp4(w)
+        return self._cache[e]
+
+    def dequant(self, e):
+        p = self.parts(e)
+        if self.fmt == "fp8":
+            return dequant_weight_fp8(*p)
+        return dequant_nvfp4(*p)
 
 
 def quantize_bank(weights_fp32, fmt="fp8"):
@@ -358,7 +403,7 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
     H = x.shape[1]
     toks = range(T) if tokens_subset is None else list(tokens_subset)
     xdeq, _ = quantize_acts(x, fmt)
-    inter = bank_gateup.q.shape[1] // 2
+    inter = bank_gateup.n // 2
     # all active routes' intermediates (needed for the NVFP4 tensor-wide amax)
     routes = [(t, j) for t in toks for j in range(topk) if ids[t, j] >= 0]
     if fmt == "nvfp4" and tokens_subset is not None:

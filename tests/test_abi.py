@@ -1,0 +1,109 @@
+"""The C ABI library builds, loads and exports every symbol include/ftmoe.h declares;
+host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ftmoe.h")
+
+
+@pytest.fixture(scope="module")
+def ft():
+    from block_quantized_moe_gb300 import build_lib
+    build_lib.build()
+    import block_quantized_moe_gb300 as ft
+    ft.lib()
+    return ft
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ftmoe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["ftmoe_quantize_act", "ftmoe_gather_rows_scales", "ftmoe_grouped_gemm_gateup",
+                 "ftmoe_silu_mul", "ftmoe_grouped_gemm_down", "ftmoe_combine", "ftmoe_moe_forward",
+                 "ftmoe_segment_routes", "ftmoe_pick_tile"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(ft):
+    lib = ctypes.CDLL(ft.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    bound = {n for n, _, _ in ft._SIGNATURES}
+    assert set(declared_functions()) <= bound
+
+
+def test_pick_tile_host_function(ft):
+    assert ft.ftmoe_pick_tile(1536, 256) == 16
+    assert ft.ftmoe_pick_tile(6144, 256) == 32
+    assert ft.ftmoe_pick_tile(24576, 256) == 128
+    assert ft.ftmoe_pick_tile(64, 64) == 16
+    with pytest.raises(ft.FtmoeError):
+        ft.ftmoe_pick_tile(10, 0)
+
+
+def test_status_strings(ft):
+    assert ft.lib().ftmoe_status_string(0) == b"ok"
+    assert ft.lib().ftmoe_status_string(1) == b"invalid argument"
+
+
+def test_invalid_arguments_rejected_on_host(ft):
+    L = ft.lib()
+    # NULL input with rows > 0
+    assert L.ftmoe_quantize_act(None, 4, 128, 128, 0, None, None, None, None) == ft.FTMOE_INVALID_ARG
+    # ld < k
+    assert L.ftmoe_quantize_act(ctypes.c_void_p(16), 4, 128, 64, 0, ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), None, None) == ft.FTMOE_INVALID_ARG
+    # unknown format
+    assert L.ftmoe_quantize_act(ctypes.c_void_p(16), 4, 128, 128, 7, ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), None, None) == ft.FTMOE_INVALID_ARG
+    # NVFP4 needs k % 32 == 0 and a global scale
+    assert L.ftmoe_quantize_act(ctypes.c_void_p(16), 4, 48, 48, 1, ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), ctypes.c_void_p(16), None) == ft.FTMOE_INVALID_ARG
+    # zero rows: OK without any launch
+    assert L.ftmoe_quantize_act(None, 0, 128, 128, 0, None, None, None, None) == ft.FTMOE_OK
+    assert L.ftmoe_gather_rows_scales(None, None, 5, 896, 28, None, 0, None, None, None, None) == ft.FTMOE_OK
+    assert L.ftmoe_gather_rows_scales(None, None, 5, 896, 28, None, 3, None, None, None, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_segment_routes(None, 4, 2, 0, None, None, None, None, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, None, 16, None) == ft.FTMOE_OK
+    assert L.ftmoe_combine(None, 8, None, None, None, 2, 2, 16, None, 16, None) == ft.FTMOE_INVALID_ARG
+
+
+def test_forward_workspace_layout(ft):
+    s = ft.moe_shape(8, 4096, 1024, 8, 64)
+    n = ft.ftmoe_forward_workspace_bytes(s)
+    lay = ft.ftmoe_forward_workspace_layout(s)
+    assert lay["total"] == n
+    R = 64
+    assert lay["gateup_bytes"] == R * 2 * 1024 * 4 and lay["down_bytes"] == R * 4096 * 4
+    for key in ("x_q", "x_scales", "gateup", "act_q", "act_scales", "down"):
+        assert lay[key] % 256 == 0
+    assert lay["rows_q"] == 0  # decode-size shapes take the route-slot path: no gather buffers
+    g = ft.ftmoe_forward_workspace_layout(ft.moe_shape(256, 7168, 2048, 6, 256))
+    assert g["rows_q"] > 0 and g["dst2src"] > 0
+    bad = ft.moe_shape(8, 4096, 1024, 8, 64, tok_tile=48)
+    assert ft.ftmoe_forward_workspace_bytes(bad) == 0
+
+
+def test_forward_rejects_inconsistent_banks(ft):
+    # Every call here must be refused by the host checks: the pointers are fake, so a call
+    # that got as far as a launch would fault on a GPU.
+    s = ft.moe_shape(2, 256, 128, 2, 4)
+    bank_gu = ft.ExpertBank(0, 4, 300, 256, ctypes.c_void_p(256), ctypes.c_void_p(256), None)  # n != 2I
+    bank_dn = ft.ExpertBank(0, 4, 256, 128, ctypes.c_void_p(256), ctypes.c_void_p(256), None)
+    args = ft.MoeArgs(s, ctypes.c_void_p(256), 256, ctypes.c_void_p(256), ctypes.c_void_p(256),
+                      bank_gu, bank_dn, ctypes.c_void_p(256), 256)
+    assert ft.lib().ftmoe_moe_forward(ctypes.byref(args), ctypes.c_void_p(256), 1 << 30, None) == ft.FTMOE_INVALID_ARG
+    args.w_gateup.n = 2 * 128
+    args.w_down.num_experts = 5  # bank E != shape E
+    assert ft.lib().ftmoe_moe_forward(ctypes.byref(args), ctypes.c_void_p(256), 1 << 30, None) == ft.FTMOE_INVALID_ARG
+    args.w_down.num_experts = 4
+    assert ft.lib().ftmoe_moe_forward(ctypes.byref(args), ctypes.c_void_p(256), 16, None) == ft.FTMOE_WORKSPACE_TOO_SMALL

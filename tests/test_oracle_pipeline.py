@@ -126,6 +126,17 @@ def test_quantize_weight_blocks_closed_forms():
     assert np.all(np.abs(deq / srep - v) <= _e4m3_spacing(np.abs(v)) / 2 + np.abs(v) * 2.0 ** -23)
 
 
+def test_quantize_weight_fast_equals_plain():
+    rng = np.random.default_rng(16)
+    w = (rng.standard_normal((300, 260)) * 0.02).astype(np.float32)
+    w[:128, 128:256] = 0  # an all-zero block
+    a = M.quantize_weight_fp8(w)
+    b = M.quantize_weight_fp8_fast(w)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    lazy = M.LazyBank(lambda e: w, 300)
+    assert np.array_equal(lazy.dequant(0), M.dequant_weight_fp8(*a))
+
+
 # -- NVFP4 ---------------------------------------------------------------------
 
 def test_nvfp4_exact_when_scales_are_exact():
