@@ -1,13 +1,531 @@
-// tcgen05 grouped GEMM (placeholder until the tensor-core kernel lands: reports
-// unsupported so the grouped path runs on the streaming kernel).
+// Grouped block-FP8 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// out[row, n] = sum_kb  s_a[row, kb] * s_w[e, n/128, kb] * sum_{k in kb} a[row, k] * w[e, n, k]
+// for the rows of each expert's segment (rows sorted by expert, offsets[e]..offsets[e+1]).
+// The 128x128 fp32 weight block scales and 1x128 activation scales are arbitrary fp32
+// numbers, which the block-scaled MMA kinds (power-of-two or e4m3 scales per 16/32
+// elements) cannot express; so, as the FreeToken block-FP8 page and the SGLang CUTLASS
+// path do with their block scales, each 128-wide K block is accumulated separately and
+// then rescaled on CUDA cores.
+//
+// Layout of the work ("swap AB"): the MMA's M = 128 rows are 128 weight rows (one
+// weight-scale block row), the MMA's N is the token tile (16/32/64/128 rows of one
+// expert, picked from rows per expert because padding is not free -- FreeToken
+// "perf(dsfp4): pick the grouped-prefill tile from route density on sm_89").
+// Per 128-wide K block: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM
+// accumulator; the epilogue warps tcgen05.ld it, multiply by s_w * s_a[column] and add
+// into fp32 registers. Two TMEM accumulators alternate so the MMA of block kb+1 runs
+// while block kb is promoted.
+//
+// One persistent CTA per SM walks units (expert, 128-row weight block, token tile) in an
+// order where the token tiles of one weight block are adjacent, so CTAs that run at the
+// same time share weight tiles through L2. Roles: warp 0 = TMA producer, warp 1 = MMA
+// issuer (and TMEM owner), warps 2..9 = epilogue (two groups of four warps, one per half
+// of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is
+// bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all roles, waits
+// for its own TMA loads still in flight, frees its TMEM and returns.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace ftmoe {
 
-cudaError_t launch_tc_gemm(const TcGemmArgs&, cudaStream_t, int* unsupported) {
-  *unsupported = 1;
-  return cudaSuccess;
+namespace tc {
+
+constexpr int kThreads = 320;          // 10 warps
+constexpr int kEpiWarp0 = 2;
+constexpr int kBM = 128;               // weight rows per tile (MMA M)
+constexpr int kBK = 128;               // K bytes per stage = one scale block
+constexpr int kMaxExperts = 1024;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete. Returns false (and raises the
+// abort flag) on timeout, or if another role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      raise_error(FTMOE_ERR_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes, written by
+// TMA with the 128-byte swizzle: 8-row swizzle atoms of 1024 bytes stacked along M/N
+// (stride byte offset 1024); the leading byte offset is unused because the tile's K
+// extent is exactly one swizzle atom wide.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                         // leading byte offset (unused), 16 B
+  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
+  d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D fp32, A = B = e4m3, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f8(int n) {
+  return (1u << 4)                      // D format f32
+         | (0u << 7) | (0u << 10)       // A, B format e4m3
+         | ((uint32_t)(n >> 3) << 17)   // N >> 3
+         | ((uint32_t)(kBM >> 4) << 24);  // M >> 4
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 16 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Named barrier that also ORs a flag over the participating threads (uniform result).
+__device__ __forceinline__ int named_bar_or(int id, int n, int v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.s32 pi, %3, 0;\n bar.red.or.pred po, %1, %2, pi;\n selp.s32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"(v)
+      : "memory");
+  return r;
+}
+
+struct Params {
+  const int32_t* offsets;
+  const float* a_s;   // [a_rows][kb_count]
+  const float* w_s;   // [E][nb_count][kb_count]
+  float* out;
+  int64_t ld_out;
+  int64_t a_rows;
+  int n, k, E, kb_count, nb_count, stages;
+};
+
+template <int TT>
+struct Smem {
+  static constexpr int kTileW = kBM * kBK;    // 16 KiB
+  static constexpr int kTileA = TT * kBK;     // TT * 128 B
+  static constexpr int kStage = kTileW + kTileA;
+};
+
+// Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the promoted
+// scale table comb[2][kb_count][TT/2], the unit prefix table and the barriers.
+template <int TT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a, Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int S = p.stages;
+  uint8_t* tiles = smem;
+  float* comb = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT>::kStage);
+  int* cum = reinterpret_cast<int*>(comb + 2 * p.kb_count * (TT / 2));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(cum + kMaxExperts + 2)) + 7) & ~(uintptr_t)7);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, NB = p.nb_count, KB = p.kb_count;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), 8);  // one arrival per epilogue warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // unit prefix: cum[e] = number of units of experts < e (units = token tiles x weight blocks)
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int u = 0;
+      if (e < E) {
+        int lo = p.offsets[e], hi = p.offsets[e + 1];
+        if (lo < 0) lo = 0;
+        if (hi > p.a_rows) hi = (int)p.a_rows;
+        const int m = hi > lo ? hi - lo : 0;
+        u = ((m + TT - 1) / TT) * NB;
+      }
+      int inc = u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (e < E) cum[e] = run + inc - u;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) cum[E] = run;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(2 * TT < 32 ? 32 : 2 * TT));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int total_units = cum[E];
+
+  // unit -> (expert, weight block, first row, rows in tile)
+  auto decode = [&](int u, int& e, int& nb, int& row0, int& rows) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {  // last e with cum[e] <= u
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    int s0 = p.offsets[e], s1 = p.offsets[e + 1];
+    if (s0 < 0) s0 = 0;
+    if (s1 > p.a_rows) s1 = (int)p.a_rows;
+    const int m = s1 - s0;
+    const int ntt = (m + TT - 1) / TT;
+    const int local = u - cum[e];
+    nb = local / ntt;
+    const int tt = local - nb * ntt;
+    row0 = s0 + tt * TT;
+    rows = min(TT, s1 - row0);
+  };
+
+  if (warp == 0) {
+    // ------------------------------- TMA producer -------------------------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < total_units && !s_abort; u += gridDim.x) {
+        int e, nb, row0, rows;
+        decode(u, e, nb, row0, rows);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int st = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
+          uint8_t* tw = tiles + (size_t)st * Smem<TT>::kStage;
+          uint8_t* ta = tw + Smem<TT>::kTileW;
+          const uint32_t fb = smem_u32(&full[st]);
+          mbar_expect_tx(fb, Smem<TT>::kStage);
+          tma_load_3d(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e);
+          tma_load_2d(smem_u32(ta), &map_a, fb, kb * kBK, row0);
+        }
+      }
+      // loads still in flight complete on their full barrier: wait for the last phase
+      // issued on each stage (a bounded wait; the phase completes once its bytes land)
+      const uint32_t issued = it;
+      for (int st = 0; st < S && (uint32_t)st < issued; ++st) {
+        const uint32_t last = issued - 1 - ((issued - 1 - st) % S);
+        const uint32_t ph = (last / S) & 1;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&full[st]), ph) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------- MMA issuer --------------------------------
+    if (lane == 0) {
+      uint32_t it = 0, kc = 0;
+      constexpr uint32_t idesc = idesc_f8(TT);
+      for (int u = blockIdx.x; u < total_units && !s_abort; u += gridDim.x) {
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          const int st = it % S;
+          const uint32_t acc = kc & 1;
+          if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&tempty[acc]), ((kc >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
+          fence_after();
+          const uint32_t tw = smem_u32(tiles + (size_t)st * Smem<TT>::kStage);
+          const uint32_t ta = tw + Smem<TT>::kTileW;
+          const uint32_t d = tmem_base + acc * TT;
+#pragma unroll
+          for (int j = 0; j < kBK / 32; ++j)
+            mma_f8(d, smem_desc_sw128(tw + 32 * j), smem_desc_sw128(ta + 32 * j), idesc, j > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&empty[st]));
+          mma_commit(smem_u32(&tfull[acc]));
+        }
+        if (!ok) break;
+      }
+      // MMAs still running write TMEM: wait (bounded) for the last commit of each
+      // accumulator before the CTA may free it
+      for (uint32_t b = 0; b < 2 && b < kc; ++b) {
+        const uint32_t last = kc - 1 - ((kc - 1 - b) & 1);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&tfull[b]), (last >> 1) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else {
+    // --------------------------------- epilogue ---------------------------------
+    const int ew = warp - kEpiWarp0;          // 0..7
+    const int half = ew >> 2;                 // token-column half
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    constexpr int HC = TT / 2;                // columns per half
+    const int tid_h = (ew & 3) * 32 + lane;   // 0..127 within the half's warps
+    float* my_comb = comb + (size_t)half * KB * HC;
+    uint32_t kc = 0;
+    float acc[HC];
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      int e, nb, row0, rows;
+      decode(u, e, nb, row0, rows);
+      // all four warps of this half leave together on an abort; the barrier also orders
+      // the previous unit's reads of the scale table before it is rewritten
+      if (named_bar_or(1 + half, 128, s_abort)) break;
+      // combined scales of this unit: comb[kb][c] = s_w[e][nb][kb] * s_a[row0 + c][kb]
+      const float* wsr = p.w_s + ((int64_t)e * NB + nb) * KB;
+      for (int i = tid_h; i < KB * HC; i += 128) {
+        const int c = i / KB, kb = i - c * KB;
+        const int r = half * HC + c;
+        float v = 0.0f;
+        if (r < rows) v = wsr[kb] * p.a_s[(int64_t)(row0 + r) * KB + kb];
+        my_comb[kb * HC + c] = v;
+      }
+      named_bar(1 + half, 128);
+#pragma unroll
+      for (int c = 0; c < HC; ++c) acc[c] = 0.0f;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb, ++kc) {
+        const uint32_t b = kc & 1;
+        const int got = mbar_wait(smem_u32(&tfull[b]), (kc >> 1) & 1, &s_abort) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + b * TT + half * HC;
+        float d[HC];
+        if constexpr (HC == 8) {
+          tmem_ld8(taddr, d);
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < HC; c0 += 16) tmem_ld16(taddr + c0, d + c0);
+        }
+        tmem_ld_wait();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
+        const float4* cs = reinterpret_cast<const float4*>(my_comb + kb * HC);
+#pragma unroll
+        for (int c4 = 0; c4 < HC / 4; ++c4) {
+          const float4 s4 = cs[c4];
+          acc[4 * c4 + 0] = fmaf(d[4 * c4 + 0], s4.x, acc[4 * c4 + 0]);
+          acc[4 * c4 + 1] = fmaf(d[4 * c4 + 1], s4.y, acc[4 * c4 + 1]);
+          acc[4 * c4 + 2] = fmaf(d[4 * c4 + 2], s4.z, acc[4 * c4 + 2]);
+          acc[4 * c4 + 3] = fmaf(d[4 * c4 + 3], s4.w, acc[4 * c4 + 3]);
+        }
+      }
+      const int n = nb * kBM + 32 * quarter + lane;
+      if (ok && n < p.n) {
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          const int r = half * HC + c;
+          if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[c];
+        }
+      }
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(2 * TT < 32 ? 32 : 2 * TT));
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int TT>
+static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  const int KB = (int)cdiv(a.k, 128), NB = (int)cdiv(a.n, 128);
+  const size_t comb_bytes = (size_t)2 * KB * (TT / 2) * 4;
+  const size_t fixed = 1024 /*align*/ + comb_bytes + (tc::kMaxExperts + 2) * 4 + 8;
+  const size_t max_smem = 227 * 1024;
+  int stages = 8;
+  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 4) * 8 > max_smem) --stages;
+  const size_t smem = fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 4) * 8;
+  if (smem > max_smem) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  CUtensorMap mw, ma;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)a.k, (cuuint64_t)a.n, (cuuint64_t)a.E};
+    cuuint64_t strides[2] = {(cuuint64_t)a.k, (cuuint64_t)a.k * (cuuint64_t)a.n};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w_q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.k, (cuuint64_t)a.a_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)a.k};
+    cuuint32_t box[2] = {128, (cuuint32_t)TT};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.a_q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  tc::Params p;
+  p.offsets = a.offsets;
+  p.a_s = a.a_s;
+  p.w_s = a.w_s;
+  p.out = a.out;
+  p.ld_out = a.ld_out;
+  p.a_rows = a.a_rows;
+  p.n = (int)a.n;
+  p.k = (int)a.k;
+  p.E = a.E;
+  p.kb_count = KB;
+  p.nb_count = NB;
+  p.stages = stages;
+  cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  tc::tc_gemm_kernel<TT><<<sm_count(), tc::kThreads, smem, st>>>(mw, ma, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
+  *unsupported = 0;
+  // TMA needs 16-byte aligned bases and row strides; the kernel indexes rows and
+  // columns in 32-bit; the unit prefix table holds up to kMaxExperts experts.
+  if (a.k % 16 != 0 || (uintptr_t)a.w_q % 16 != 0 || (uintptr_t)a.a_q % 16 != 0 || a.E > tc::kMaxExperts ||
+      a.n > (1 << 30) || a.k > (1 << 30) || a.a_rows > (1 << 30) || a.E > 65535) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  switch (a.tok_tile) {
+    case 16: return launch_tt<16>(a, st, unsupported);
+    case 32: return launch_tt<32>(a, st, unsupported);
+    case 64: return launch_tt<64>(a, st, unsupported);
+    case 128: return launch_tt<128>(a, st, unsupported);
+    default: *unsupported = 1; return cudaSuccess;
+  }
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_tc_gemm)
