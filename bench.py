@@ -37,11 +37,19 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 WORKLOADS = {
-    # name: (tokens, hidden, inter, experts, topk, active per token, path)
+    # name: (tokens, hidden, inter, experts, topk, active per token, path: 1 route slots, 2 grouped)
     "decode-h4096-i1024-e64-t8-a8": (8, 4096, 1024, 64, 8, 8, 1),
     "decode-h4096-i1024-e64-t1-a8": (1, 4096, 1024, 64, 8, 8, 1),
     "decode-h4096-i1024-e64-t8-a2": (8, 4096, 1024, 64, 8, 2, 1),
+    "decode-h4096-i1024-e64-t1-a2": (1, 4096, 1024, 64, 8, 2, 1),
+    "decode-h4096-i1024-e64-t1-a0": (1, 4096, 1024, 64, 8, 0, 1),
     "decode-h2048-i768-e8-t1-a2": (1, 2048, 768, 8, 8, 2, 1),
+    "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
+    # a 32-expert bank with the same rows per expert (96) as the 24,576-route case: small
+    # enough (1.4 GB of weights) for multi-pass profiler captures
+    "prefill-fp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
 }
 DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
 
@@ -105,7 +113,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -143,8 +151,8 @@ class ClockSampler:
 # workload construction (inputs resident in HBM before timing starts)
 # ------------------------------------------------------------------------------------
 
-class DecodeWorkload:
-    NSETS = 8  # route/input sets rotated between steps
+class MoeWorkload:
+    NSETS = 8  # route/input sets rotated between steps (2 for the prefill sizes)
 
     def __init__(self, name, device, seed=0xF7E00002):
         import block_quantized_moe_gb300 as ft
@@ -152,6 +160,8 @@ class DecodeWorkload:
         T, H, I, E, k, active, path = WORKLOADS[name]
         self.name, self.T, self.H, self.I, self.E, self.k, self.active, self.path = name, T, H, I, E, k, active, path
         self.dev = device
+        if path == 2:
+            self.NSETS = 2
         gq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
         gs = torch.empty(E, -(-2 * I // 128), -(-H // 128), dtype=torch.float32, device=device)
         dq = torch.empty(E, H, I, dtype=torch.uint8, device=device)
@@ -166,8 +176,9 @@ class DecodeWorkload:
         self.sets = []
         for i in range(self.NSETS):
             s = seed + 17 * (i + 1)
-            self.sets.append((synth.activations_bf16(T, H, s, device),
-                              synth.routes(T, k, E, s, active_per_token=active, device=device),
+            ids = (synth.routes_fast(T, k, E, s, device) if active == k and T * k > 256 else
+                   synth.routes(T, k, E, s, active_per_token=active, device=device))
+            self.sets.append((synth.activations_bf16(T, H, s, device), ids,
                               synth.routing_weights(T, k, s, device)))
         self.shape = ft.moe_shape(T, H, I, k, E, path=path)
         self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
@@ -175,7 +186,7 @@ class DecodeWorkload:
         self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
         self.w_in = torch.empty(T, k, dtype=torch.float32, device=device)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
-        self.launches_per_step = 5
+        self.launches_per_step = 5 if path == 1 else 7
 
     # algorithmic bytes/flops of one forward on route set i
     def work(self, i):
@@ -183,18 +194,24 @@ class DecodeWorkload:
         ids = ids.cpu().numpy()
         T, H, I, k = self.T, self.H, self.I, self.k
         uniq = len(set(int(e) for e in ids.reshape(-1) if e >= 0))
-        act_routes = int((ids >= 0).sum())
+        ra = int((ids >= 0).sum())
         R = T * k
+        sc = lambda n: 4 * (-(-n // 128))  # noqa: E731 - fp32 scale bytes of an n-wide row
         w_gu = 2 * I * H + 4 * (-(-2 * I // 128)) * (-(-H // 128))
         w_dn = H * I + 4 * (-(-H // 128)) * (-(-I // 128))
-        gateup_bytes = uniq * w_gu + T * (H + 4 * (-(-H // 128))) + R * 2 * I * 4
-        total = (T * H * 2 + T * (H + 4 * (-(-H // 128))) + T * k * 8  # x in, x_q out, routes
-                 + gateup_bytes                                      # gate/up kernel
-                 + R * 2 * I * 4 + R * (I + 4 * (-(-I // 128)))      # silu_mul in/out
-                 + uniq * w_dn + R * (I + 4 * (-(-I // 128))) + R * H * 4  # down kernel
-                 + act_routes * H * 4 + T * H * 2)                   # combine
-        flops = 2 * act_routes * (2 * I * H + H * I)
-        return dict(bytes=total, gateup_bytes=gateup_bytes, flops=flops, uniq=uniq, active=act_routes)
+        out_rows = R if self.path == 1 else ra   # the route-slot path also writes zero rows
+        gateup = uniq * w_gu + (T if self.path == 1 else ra) * (H + sc(H)) + out_rows * 2 * I * 4
+        down = uniq * w_dn + out_rows * (I + sc(I)) + out_rows * H * 4
+        total = (T * H * 2 + T * (H + sc(H))                       # quantize
+                 + gateup
+                 + out_rows * 2 * I * 4 + out_rows * (I + sc(I))     # silu_mul
+                 + down
+                 + ra * H * 4 + T * k * 8 + T * H * 2)               # combine
+        if self.path == 2:
+            total += T * k * 4 * 3 + ra * (H + sc(H)) * 2           # segment + gather
+        flops = 2 * ra * (2 * I * H + H * I)
+        return dict(bytes=total, gateup_bytes=gateup, flops=flops, gateup_flops=2 * ra * 2 * I * H,
+                    uniq=uniq, active=ra)
 
     def load_set(self, i):
         x, ids, w = self.sets[i]
@@ -207,15 +224,25 @@ class DecodeWorkload:
                                   self.out, self.ws, stream=stream)
 
     def dominant_kernel(self):
-        """The gate/up streaming GEMM alone, on the quantized rows the forward left in the workspace."""
+        """The gate/up GEMM alone, on the rows the forward left in the workspace."""
         ft = self.ft
         lay = ft.ftmoe_forward_workspace_layout(self.shape)
-        xq = self.ws[lay["x_q"]:lay["x_q"] + self.T * self.H].view(self.T, self.H)
-        xs = self.ws[lay["x_scales"]:lay["x_scales"] + self.T * (-(-self.H // 128)) * 4].view(torch.float32).view(self.T, -1)
-        gu = self.ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(self.T * self.k, -1)
-        act = ft.make_act(xq, xs)
-        routes = ft.slot_routes(self.ids_in)
-        return lambda: ft.ftmoe_grouped_gemm_gateup(act, routes, self.bank_gu, gu, variant=1)
+        T, H, k = self.T, self.H, self.k
+        gu = self.ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(T * k, -1)
+        if self.path == 1:
+            xq = self.ws[lay["x_q"]:lay["x_q"] + T * H].view(T, H)
+            xs = self.ws[lay["x_scales"]:lay["x_scales"] + T * (-(-H // 128)) * 4].view(torch.float32).view(T, -1)
+            act, routes = ft.make_act(xq, xs), ft.slot_routes(self.ids_in)
+            return "stream_gemm_kernel (gate/up, route slots)", lambda: ft.ftmoe_grouped_gemm_gateup(
+                act, routes, self.bank_gu, gu, variant=1)
+        R = T * k
+        rq = self.ws[lay["rows_q"]:lay["rows_q"] + R * H].view(R, H)
+        rs = self.ws[lay["rows_scales"]:lay["rows_scales"] + R * (-(-H // 128)) * 4].view(torch.float32).view(R, -1)
+        off = self.ws[lay["offsets"]:lay["offsets"] + (self.E + 1) * 4].view(torch.int32)
+        act, routes = ft.make_act(rq, rs), ft.grouped_routes(off)
+        tile = ft.ftmoe_pick_tile(R, self.E)
+        return f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)", lambda: ft.ftmoe_grouped_gemm_gateup(
+            act, routes, self.bank_gu, gu, tok_tile=tile, variant=2)
 
 
 def time_events(fn, prep, steps, stream):
@@ -240,7 +267,7 @@ def run_gpu(args, rank, world, local):
     import block_quantized_moe_gb300 as ft
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = DecodeWorkload(args.workload, dev)
+    wl = MoeWorkload(args.workload, dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
@@ -248,7 +275,8 @@ def run_gpu(args, rank, world, local):
         wl.load_set(i % wl.NSETS)
         flush.zero_()
 
-    # eager warm-up, then capture one graph of the whole forward
+    # eager warm-up, then capture one graph of the whole forward (--eager: direct launches,
+    # e.g. for profilers that replay kernels one by one)
     wl.load_set(0)
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -256,14 +284,18 @@ def run_gpu(args, rank, world, local):
         wl.forward(stream=side)
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        wl.forward()
-    torch.cuda.synchronize()
+    if args.eager:
+        run_step = wl.forward
+    else:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wl.forward()
+        torch.cuda.synchronize()
+        run_step = graph.replay
 
     for i in range(args.warmup):
         prep(i)
-        graph.replay()
+        run_step()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -271,7 +303,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     clocks.start()
     t_wall = time.perf_counter()
-    ms = time_events(graph.replay, prep, args.steps, stream)
+    ms = time_events(run_step, prep, args.steps, stream)
     torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall
@@ -285,17 +317,19 @@ def run_gpu(args, rank, world, local):
     bytes_avg = float(np.mean([w["bytes"] for w in works]))
     flops_avg = float(np.mean([w["flops"] for w in works]))
     gu_bytes_avg = float(np.mean([w["gateup_bytes"] for w in works]))
+    gu_flops_avg = float(np.mean([w["gateup_flops"] for w in works]))
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
     fp8_peak = 2.0 * bf16_peak  # dense FP8 = 2x bf16 (nominal ratio 4.5 / 2.25)
 
     # dominant kernel alone: gate/up streaming GEMM, events on its launching stream
-    kern = wl.dominant_kernel()
+    kname, kern = wl.dominant_kernel()
     for i in range(3):
         prep(i)
         kern()
     kms = time_events(kern, prep, args.steps, stream)
     k_us = kms * 1e3 / args.steps
     k_gbs = gu_bytes_avg / (k_us * 1e-6) / 1e9
+    k_tflops = gu_flops_avg / (k_us * 1e-6) / 1e12
 
     # end to end through the public API: pinned host inputs -> device, forward, output -> host
     hx = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16, pin_memory=True) for _ in range(wl.NSETS)]
@@ -312,7 +346,7 @@ def run_gpu(args, rank, world, local):
         wl.x_in.copy_(hx[j], non_blocking=True)
         wl.ids_in.copy_(hids[j], non_blocking=True)
         wl.w_in.copy_(hw[j], non_blocking=True)
-        graph.replay()
+        run_step()
         hout.copy_(wl.out, non_blocking=True)
 
     for i in range(3):
@@ -346,17 +380,19 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
                    "l2": "flushed before every timed step (512 MiB write)", "parallelism": f"replicas x{world}",
-                   "graph": "one CUDA graph replayed; inputs copied in place between steps"},
+                   "graph": ("direct launches (--eager)" if args.eager else
+                             "one CUDA graph replayed; inputs copied in place between steps")},
         "us_per_call_per_gpu": round(us_per_call_rank, 3),
         "hbm_gbs": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9, 1),
         "hbm_frac_of_peak": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9 / hbm_peak, 4),
         "fp8_tflops": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12, 3),
         "fp8_frac_of_dense_peak": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12 / fp8_peak, 5),
         "algorithmic_bytes_per_call": int(bytes_avg),
-        "roofline": {"kernel": "stream_gemm_kernel (gate/up, route slots)", "bound": "hbm",
+        "roofline": {"kernel": kname, "bound": "hbm",
                      "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(k_gbs / hbm_peak, 4), "traffic": None,
                      "launch_us": round(k_us, 3), "algorithmic_bytes_per_launch": int(gu_bytes_avg),
+                     "fp8_tflops": round(k_tflops, 2), "fp8_frac_of_dense_peak": round(k_tflops / fp8_peak, 4),
                      "peak_source": peak_src},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -373,13 +409,16 @@ def run_gpu(args, rank, world, local):
 # CPU oracle (baseline leg and the reference arm)
 # ------------------------------------------------------------------------------------
 
-def _oracle_problem(name, seed=0xF7E00002):
+def _oracle_problem(name, seed=0xF7E00002, max_tokens=None):
     from oracle import moe as M
     T, H, I, E, k, active, _ = WORKLOADS[name]
     x = synth.activations_bf16(T, H, seed + 17, "cpu")
-    ids = synth.routes(T, k, E, seed + 17, active_per_token=active, device="cpu")
+    ids = (synth.routes_fast(T, k, E, seed + 17, "cpu") if active == k and T * k > 256 else
+           synth.routes(T, k, E, seed + 17, active_per_token=active, device="cpu"))
     w = synth.routing_weights(T, k, seed + 17, "cpu")
-    used = sorted(set(int(e) for e in ids.view(-1).tolist() if e >= 0))
+    if max_tokens is not None:  # per-token FP8 quantization: a token subset is exact
+        ids, x, w = ids[:max_tokens], x[:max_tokens], w[:max_tokens]
+    used = sorted(set(int(e) for e in ids.reshape(-1).tolist() if e >= 0))
     bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I)
     bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H)
     for e in used:  # the quantized bank is an input; build it before timing
@@ -390,11 +429,13 @@ def _oracle_problem(name, seed=0xF7E00002):
 
 def cpu_baseline(name, budget_s=20.0, repeats=None):
     """Time the oracle's forward on a bounded sample of tokens; scale to one full call."""
-    M, x, ids, w, bg, bd, T = _oracle_problem(name)
+    T_full = WORKLOADS[name][0]
+    M, x, ids, w, bg, bd, T = _oracle_problem(name, max_tokens=min(T_full, 4))
+    T = T_full
     t0 = time.perf_counter()
     done = 0
     toks = []
-    while done < T and (time.perf_counter() - t0) < budget_s:
+    while done < ids.shape[0] and (time.perf_counter() - t0) < budget_s:
         M.moe_forward(x, ids, w, bg, bd, tokens_subset=[done])
         toks.append(done)
         done += 1
@@ -408,12 +449,15 @@ def cpu_baseline(name, budget_s=20.0, repeats=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    M, x, ids, w, bg, bd, T = _oracle_problem(args.workload)
+    T_full = WORKLOADS[args.workload][0]
+    M, x, ids, w, bg, bd, T = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
+    T = T_full
+    ns = ids.shape[0]
     for i in range(args.warmup):
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % T])
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % ns])
     t0 = time.perf_counter()
     for i in range(args.steps):
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % T])
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % ns])
     el = time.perf_counter() - t0
     us = el / args.steps * T * 1e6
     return {"impl": "reference", "metric": "MoE FFN us/call", "value": round(us, 1), "unit": "us/call",
@@ -433,6 +477,7 @@ def main():
     ap.add_argument("--impl", default="ftmoe", choices=["ftmoe", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the forward directly instead of a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     if args.warmup < 3:

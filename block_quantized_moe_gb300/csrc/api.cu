@@ -51,6 +51,9 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
   if (tile && (tile->variant < 0 || tile->variant > 2)) return FTMOE_INVALID_ARG;
   const int variant = tile ? tile->variant : 0;
   if (w->format != FTMOE_FMT_FP8) return FTMOE_UNSUPPORTED;  // NVFP4 GEMMs: grouped path only (below)
+  // both GEMM kernels read K-contiguous rows through TMA: 16-byte aligned rows
+  if (w->k % 16 != 0 || (uintptr_t)w->q % 16 != 0 || (a->rows > 0 && (uintptr_t)a->q % 16 != 0))
+    return FTMOE_UNSUPPORTED;
 
   if (routes->kind == FTMOE_ROUTES_SLOTS) {
     if (!routes->slots || routes->tokens < 0 || routes->topk <= 0) return FTMOE_INVALID_ARG;
@@ -58,7 +61,7 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
     if (R == 0) return FTMOE_OK;
     const int64_t need_rows = is_down ? R : routes->tokens;
     if (a->rows < need_rows) return FTMOE_INVALID_ARG;
-    if (variant == 2) return FTMOE_UNSUPPORTED;
+    if (variant == 2 || w->k > kStreamMaxK) return FTMOE_UNSUPPORTED;
     StreamGemmArgs g;
     memset(&g, 0, sizeof(g));
     g.a_q = a->q;
@@ -74,6 +77,8 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
     g.slots = routes->slots;
     g.routes = R;
     g.act_div = is_down ? 1 : routes->topk;
+    g.topk = routes->topk;
+    g.a_rows = a->rows;
     return from_cuda(launch_stream_gemm(g, as_stream(stream)));
   }
   if (routes->kind != FTMOE_ROUTES_GROUPED || !routes->offsets) return FTMOE_INVALID_ARG;
@@ -98,6 +103,7 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
     if (!unsupported) return from_cuda(e);
     if (variant == 2) return FTMOE_UNSUPPORTED;
   }
+  if (w->k > kStreamMaxK) return FTMOE_UNSUPPORTED;
   StreamGemmArgs g;
   memset(&g, 0, sizeof(g));
   g.a_q = a->q;

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the libftmoe translation units (not exported).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -9,6 +10,17 @@
 namespace ftmoe {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// tc_gemm.cu: host helpers shared by the TMA-fed kernels
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();  // cuTensorMapEncodeTiled from the driver, or NULL
+int sm_count();
+// 128B-swizzled uint8 tensor map of rank 2 or 3 (dims innermost first, byte strides of the
+// outer dims); false if the driver entry point is missing or the encoding is rejected
+bool encode_u8_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box);
 
 // quant.cu
 cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
@@ -51,7 +63,10 @@ struct StreamGemmArgs {
   const int32_t* slots;    // SLOTS
   int64_t routes;          // SLOTS: tokens * topk
   int32_t act_div;         // SLOTS: activation row of route r is r / act_div
+  int32_t topk;            // SLOTS
 };
+// largest K the streaming kernel stages (64 K blocks of fp16 activation codes)
+constexpr int64_t kStreamMaxK = 8192;
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t s);
 uint32_t read_err_stream_gemm();
 

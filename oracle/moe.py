@@ -395,7 +395,8 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
     tokens_subset: optional list of token indices to evaluate (others left zero);
     NVFP4 global amaxes are still taken over the whole tensors.
     Returns dict(out=float64 [T, H], out_bf16=float64 values of the bf16 rounding,
-    and per-route intermediates keyed by route id).
+    and per-route intermediates keyed by (token, slot): gu (gate/up output), a (SiLU-and-mul
+    output, before its re-quantization) and y (down output); xdeq the dequantized tokens).
     """
     x = np.asarray(x, np.float32)
     ids = np.asarray(expert_ids)
@@ -413,7 +414,7 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
     by_expert = {}
     for (t, j) in routes_all:
         by_expert.setdefault(int(ids[t, j]), []).append((t, j))
-    a_rows = {}
+    a_rows, gu_rows = {}, {}
     for e, lst in by_expert.items():
         wg = bank_gateup.dequant(e)
         rows = np.stack([xdeq[t] for (t, _) in lst])
@@ -421,6 +422,7 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
         act = silu_mul(gu)
         for i, (t, j) in enumerate(lst):
             a_rows[(t, j)] = act[i]
+            gu_rows[(t, j)] = gu[i]
     keys = sorted(a_rows.keys())
     y_rows = {}
     if keys:
@@ -443,4 +445,4 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
             if ids[t, j] < 0:
                 continue
             out[t] += np.float64(weights[t, j]) * y_rows[(t, j)]
-    return dict(out=out, out_bf16=round_to_bf16(out), a=a_rows, y=y_rows)
+    return dict(out=out, out_bf16=round_to_bf16(out), a=a_rows, gu=gu_rows, y=y_rows, xdeq=xdeq)

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import synth
-from tests.common import Problem, assert_within_tolerance
+from tests.common import Problem
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -26,9 +26,7 @@ def ft():
 
 
 def _check(prob, out, ids=None, weights=None, x=None):
-    ref = prob.oracle(ids=ids, weights=weights, x=x)["out"]
-    assert_within_tolerance(out.float().cpu().numpy(), ref)
-    return ref
+    return prob.check(out, ids=ids, weights=weights, x=x)
 
 
 def test_decode_2048_768_two_of_eight_active(ft):

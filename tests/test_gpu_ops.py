@@ -214,8 +214,22 @@ def test_combine_single_route_weight_one_is_the_row(ft):
 
 # -- the streaming GEMM on its own ------------------------------------------------------
 
+def test_gemm_rejects_unaligned_k(ft):
+    # the GEMM kernels read K-contiguous rows through TMA: K must be a multiple of 16
+    x = synth.activations_bf16(2, 520, 1, DEV)
+    xq, xs, _ = ft.quantize_act(x)
+    w = torch.zeros(2, 64, 520, device=DEV)
+    wq, wsc, _ = ft.quantize_weights(w)
+    ids = torch.zeros(2, 1, dtype=torch.int32, device=DEV)
+    out = torch.empty(2, 64, device=DEV)
+    with pytest.raises(ft.FtmoeError) as ei:
+        ft.ftmoe_grouped_gemm_gateup(ft.make_act(xq, xs), ft.slot_routes(ids), ft.make_bank(wq, wsc), out)
+    assert ei.value.status == ft.FTMOE_UNSUPPORTED
+
+
 @pytest.mark.parametrize("T,H,N,E,k,active", [(1, 2048, 1536, 8, 8, 2), (8, 4096, 2048, 64, 8, 4),
-                                              (3, 384, 300, 4, 2, 1), (8, 520, 256, 6, 4, 4)])
+                                              (3, 384, 300, 4, 2, 1), (8, 528, 256, 6, 4, 4),
+                                              (8, 1024, 4096, 3, 3, 3)])
 def test_stream_gemm_slots_vs_oracle(ft, T, H, N, E, k, active):
     seed = H + N + T
     x = synth.activations_bf16(T, H, seed, DEV)
