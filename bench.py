@@ -44,6 +44,9 @@ WORKLOADS = {
     "decode-h4096-i1024-e64-t1-a2": (1, 4096, 1024, 64, 8, 2, 1),
     "decode-h4096-i1024-e64-t1-a0": (1, 4096, 1024, 64, 8, 0, 1),
     "decode-h2048-i768-e8-t1-a2": (1, 2048, 768, 8, 8, 2, 1),
+    # the same decode batches through the grouped tensor-core path (segment, gather, tcgen05)
+    "decode-h4096-i1024-e64-t8-a8-grouped": (8, 4096, 1024, 64, 8, 8, 2),
+    "decode-h4096-i1024-e64-t1-a8-grouped": (1, 4096, 1024, 64, 8, 8, 2),
     "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),

@@ -35,8 +35,9 @@ namespace st {
 constexpr int kRows = 64;          // weight rows per item
 constexpr int kConsumers = 256;    // 32 row groups x 8 K lanes
 constexpr int kThreads = kConsumers + 32;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 16;
 constexpr int kTile = kRows * kGroup;  // 8 KiB per stage
+constexpr size_t kCtaSmem = 110 * 1024;  // per-CTA budget that keeps two CTAs on an SM
 constexpr int kMaxList = 1024;     // leaders (slot mode) or experts (grouped mode) per launch
 constexpr int kMaxMembers = 8;     // activation rows staged per pass (upper bound)
 constexpr size_t kStageBudget = 64 * 1024;  // bytes of staged activation codes (fp16) per CTA
@@ -50,7 +51,7 @@ struct Params {
   int64_t ld_out;
   int64_t a_rows;
   int64_t kp;           // K rounded up to 128: pitch of a staged activation row (fp16 codes)
-  int n, k, E, KB, NB, n_tiles, mb;
+  int n, k, E, KB, NB, n_tiles, mb, stages;
   int grouped;
   const int32_t* offsets;  // grouped: offsets of experts e0 .. e0+E (E+1 entries)
   int e0;                  // grouped: first expert of this launch
@@ -132,6 +133,7 @@ __device__ __forceinline__ int member_count(const Params& p, const Item& it) {
 __global__ void __launch_bounds__(kThreads) stream_gemm_kernel(const __grid_constant__ CUtensorMap map_w, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int kStages = p.stages;
   __half* xs = reinterpret_cast<__half*>(ring + kStages * kTile);  // [mb][kp] activation codes
   int* list = reinterpret_cast<int*>(xs + (size_t)p.mb * p.kp);    // [kMaxList]
   float* wsc = reinterpret_cast<float*>(list + kMaxList);           // [kMaxKB] weight scales of the tile
@@ -373,11 +375,18 @@ static cudaError_t launch_part(const StreamGemmArgs& a, const CUtensorMap& map, 
   p.slots = slots;
   p.routes = routes;
   p.act_div = a.act_div;
+  // members staged per pass: no more than one route per token can pick an expert in slot
+  // mode, so small batches stage fewer rows and leave the shared memory to the ring
   int mb = st::kMaxMembers;
+  if (!a.grouped && a.topk > 0 && routes / a.topk < mb) mb = (int)(routes / a.topk) > 0 ? (int)(routes / a.topk) : 1;
   while (mb > 1 && (size_t)mb * p.kp * 2 > st::kStageBudget) mb >>= 1;
   p.mb = mb;
-  const size_t smem = 1024 + (size_t)st::kStages * st::kTile + (size_t)mb * p.kp * 2 + st::kMaxList * 4 +
-                      st::kMaxKB * 4 + st::kMaxMembers * st::kMaxKB * 4 + 2 * st::kStages * 8;
+  const size_t fixed = 1024 + (size_t)mb * p.kp * 2 + st::kMaxList * 4 + st::kMaxKB * 4 +
+                       st::kMaxMembers * st::kMaxKB * 4;
+  int stages = st::kMaxStages;
+  while (stages > 2 && fixed + (size_t)stages * (st::kTile + 16) > st::kCtaSmem) --stages;
+  p.stages = stages;
+  const size_t smem = fixed + (size_t)stages * st::kTile + 2 * stages * 8;
   const int64_t max_items = (int64_t)(a.grouped ? E : (routes < a.E ? routes : a.E)) * p.n_tiles;
   int64_t grid = 2 * (int64_t)sm_count();
   if (grid > max_items) grid = max_items;

@@ -14,14 +14,15 @@
 // "perf(dsfp4): pick the grouped-prefill tile from route density on sm_89").
 // Per 128-wide K block: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM
 // accumulator; the epilogue warps tcgen05.ld it, multiply by s_w * s_a[column] and add
-// into fp32 registers. Two TMEM accumulators alternate so the MMA of block kb+1 runs
-// while block kb is promoted.
+// into fp32 registers. Up to sixteen TMEM accumulators rotate (512 columns / token tile)
+// so the MMA runs ahead of the promotion.
 //
-// One persistent CTA per SM walks units (expert, 128-row weight block, token tile) in an
-// order where the token tiles of one weight block are adjacent, so CTAs that run at the
-// same time share weight tiles through L2. Roles: warp 0 = TMA producer, warp 1 = MMA
-// issuer (and TMEM owner), warps 2..9 = epilogue (two groups of four warps, one per half
-// of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is
+// One persistent CTA per SM takes a contiguous range of units (expert, token tile,
+// 128-row weight block), weight block innermost: every weight tile is read once, and a
+// CTA's token tile and its activation scales stay in place across its units; the weight
+// block scale row of the next unit is prefetched while the current one runs. Roles: warp 0 = TMA producer, warp 1 = MMA
+// issuer (and TMEM owner), warps 2..17 = epilogue (four groups of four warps, one group
+// per quarter of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is
 // bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all roles, waits
 // for its own TMA loads still in flight, frees its TMEM and returns.
 #include <cuda.h>
@@ -36,11 +37,12 @@ namespace ftmoe {
 
 namespace tc {
 
-constexpr int kThreads = 320;          // 10 warps
-constexpr int kEpiWarp0 = 2;
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 128;               // K bytes per stage = one scale block
 constexpr int kMaxExperts = 1024;
+// TMEM accumulators in rotation: as many TT-column accumulators as 512 columns hold, at
+// most 16, so the MMA can run that many K blocks ahead of the promotion
+__host__ __device__ constexpr int acc_count(int tt) { return 512 / tt > 16 ? 16 : 512 / tt; }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -112,6 +114,10 @@ struct Params {
   int n, k, E, kb_count, nb_count, stages;
 };
 
+constexpr int kEpiWarps = 16;                    // 4 column groups x 4 TMEM lane quarters
+constexpr int kGroups = kEpiWarps / 4;
+constexpr int kMaxKB = 128;                      // K <= 16384
+
 template <int TT>
 struct Smem {
   static constexpr int kTileW = kBM * kBK;    // 16 KiB
@@ -119,22 +125,42 @@ struct Smem {
   static constexpr int kStage = kTileW + kTileA;
 };
 
-// Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the promoted
-// scale table comb[2][kb_count][TT/2], the unit prefix table and the barriers.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+  if constexpr (N == 4) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+  } else if constexpr (N == 8) {
+    tmem_ld8(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N; c += 16) tmem_ld16(taddr + c, v + c);
+  }
+}
+
+// Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the activation
+// scales of the current token tile sa[kb][TT], the weight-block scales of the current unit
+// per column group sw[kGroups][kMaxKB], the unit prefix table and the barriers.
 template <int TT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
   uint8_t* tiles = smem;
-  float* comb = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT>::kStage);
-  int* cum = reinterpret_cast<int*>(comb + 2 * p.kb_count * (TT / 2));
+  float* sa = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT>::kStage);  // [KB][TT]
+  float* swt = sa + (size_t)p.kb_count * TT;                                  // [kGroups][kMaxKB]
+  int* cum = reinterpret_cast<int*>(swt + kGroups * kMaxKB);
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(cum + kMaxExperts + 2)) + 7) & ~(uintptr_t)7);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
+  constexpr int kAcc = acc_count(TT);
   uint64_t* tfull = bars + 2 * S;
-  uint64_t* tempty = bars + 2 * S + 2;
+  uint64_t* tempty = bars + 2 * S + kAcc;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -147,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 8);  // one arrival per epilogue warp
+      mbar_init(smem_u32(&tempty[i]), kEpiWarps);  // one arrival per epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -179,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(2 * TT < 32 ? 32 : 2 * TT));
+                 "r"(kAcc * TT < 32 ? 32 : kAcc * TT));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   fence_before();
@@ -187,9 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
+  // a contiguous range of units per CTA; units run (expert, token tile, weight block) with
+  // the weight block innermost, so the token tile and its scales stay put across units
+  const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
+  const int u_end = (int)(((int64_t)(blockIdx.x + 1) * total_units) / gridDim.x);
 
-  // unit -> (expert, weight block, first row, rows in tile)
-  auto decode = [&](int u, int& e, int& nb, int& row0, int& rows) {
+  // unit -> (expert, weight block, token tile, first row, rows in tile)
+  auto decode = [&](int u, int& e, int& nb, int& tt, int& row0, int& rows) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {  // last e with cum[e] <= u
       const int mid = (lo + hi + 1) >> 1;
@@ -199,11 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s0 = p.offsets[e], s1 = p.offsets[e + 1];
     if (s0 < 0) s0 = 0;
     if (s1 > p.a_rows) s1 = (int)p.a_rows;
-    const int m = s1 - s0;
-    const int ntt = (m + TT - 1) / TT;
     const int local = u - cum[e];
-    nb = local / ntt;
-    const int tt = local - nb * ntt;
+    tt = local / NB;
+    nb = local - tt * NB;
     row0 = s0 + tt * TT;
     rows = min(TT, s1 - row0);
   };
@@ -212,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
       uint32_t it = 0;
-      for (int u = blockIdx.x; u < total_units && !s_abort; u += gridDim.x) {
-        int e, nb, row0, rows;
-        decode(u, e, nb, row0, rows);
+      for (int u = u_begin; u < u_end && !s_abort; ++u) {
+        int e, nb, tt, row0, rows;
+        decode(u, e, nb, tt, row0, rows);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int st = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -243,13 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, kc = 0;
       constexpr uint32_t idesc = idesc_f8(TT);
-      for (int u = blockIdx.x; u < total_units && !s_abort; u += gridDim.x) {
+      for (int u = u_begin; u < u_end && !s_abort; ++u) {
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
           const int st = it % S;
-          const uint32_t acc = kc & 1;
+          const uint32_t acc = kc % kAcc;
           if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&tempty[acc]), ((kc >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&tempty[acc]), ((kc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
           fence_after();
           const uint32_t tw = smem_u32(tiles + (size_t)st * Smem<TT>::kStage);
           const uint32_t ta = tw + Smem<TT>::kTileW;
@@ -264,74 +292,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // MMAs still running write TMEM: wait (bounded) for the last commit of each
       // accumulator before the CTA may free it
-      for (uint32_t b = 0; b < 2 && b < kc; ++b) {
-        const uint32_t last = kc - 1 - ((kc - 1 - b) & 1);
+      for (uint32_t b = 0; b < (uint32_t)kAcc && b < kc; ++b) {
+        const uint32_t last = kc - 1 - ((kc - 1 - b) % kAcc);
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(smem_u32(&tfull[b]), (last >> 1) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        while (!mbar_try_wait(smem_u32(&tfull[b]), (last / kAcc) & 1) && globaltimer() - t0 < kTimeoutNs) {
         }
       }
     }
   } else {
     // --------------------------------- epilogue ---------------------------------
-    const int ew = warp - kEpiWarp0;          // 0..7
-    const int half = ew >> 2;                 // token-column half
+    constexpr int HC = TT / kGroups;          // token columns of this warp's group
+    const int ew = warp - 2;                  // 0 .. kEpiWarps-1
+    const int grp = ew >> 2;                  // column group
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    constexpr int HC = TT / 2;                // columns per half
-    const int tid_h = (ew & 3) * 32 + lane;   // 0..127 within the half's warps
-    float* my_comb = comb + (size_t)half * KB * HC;
+    const int tid_g = (ew & 3) * 32 + lane;   // 0..127 within the group
+    float* my_sw = swt + grp * kMaxKB;
     uint32_t kc = 0;
+    int staged_e = -1, staged_tt = -1;
+    float sw_next = 0.0f;
+    bool have_next = false;
     float acc[HC];
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      int e, nb, row0, rows;
-      decode(u, e, nb, row0, rows);
-      // all four warps of this half leave together on an abort; the barrier also orders
-      // the previous unit's reads of the scale table before it is rewritten
-      if (named_bar_or(1 + half, 128, s_abort)) break;
-      // combined scales of this unit: comb[kb][c] = s_w[e][nb][kb] * s_a[row0 + c][kb]
-      const float* wsr = p.w_s + ((int64_t)e * NB + nb) * KB;
-      for (int i = tid_h; i < KB * HC; i += 128) {
-        const int c = i / KB, kb = i - c * KB;
-        const int r = half * HC + c;
-        float v = 0.0f;
-        if (r < rows) v = wsr[kb] * p.a_s[(int64_t)(row0 + r) * KB + kb];
-        my_comb[kb * HC + c] = v;
+    for (int u = u_begin; u < u_end; ++u) {
+      int e, nb, tt, row0, rows;
+      decode(u, e, nb, tt, row0, rows);
+      // all warps of the group leave together on an abort; the barrier also orders the
+      // previous unit's reads of the scale tables before they are rewritten
+      if (named_bar_or(1 + grp, 128, s_abort)) break;
+      // weight-block scales of this unit (prefetched during the previous unit)
+      if (tid_g < KB) my_sw[tid_g] = have_next ? sw_next : __ldg(p.w_s + ((int64_t)e * NB + nb) * KB + tid_g);
+      have_next = false;
+      if (u + 1 < u_end && tid_g < KB) {
+        int e2, nb2, tt2, r02, rows2;
+        decode(u + 1, e2, nb2, tt2, r02, rows2);
+        sw_next = __ldg(p.w_s + ((int64_t)e2 * NB + nb2) * KB + tid_g);
+        have_next = true;
       }
-      named_bar(1 + half, 128);
+      // activation scales of the token tile, staged when the token tile changes
+      if (e != staged_e || tt != staged_tt) {
+        for (int i0 = tid_g; i0 < KB * HC; i0 += 128 * 8) {
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * 128;
+            v[q] = 0.0f;
+            if (i < KB * HC) {
+              const int c = i / KB, kb = i - c * KB;
+              const int r = grp * HC + c;
+              if (r < rows) v[q] = __ldg(p.a_s + (int64_t)(row0 + r) * KB + kb);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * 128;
+            if (i < KB * HC) {
+              const int c = i / KB, kb = i - c * KB;
+              sa[kb * TT + grp * HC + c] = v[q];
+            }
+          }
+        }
+        staged_e = e;
+        staged_tt = tt;
+      }
+      named_bar(1 + grp, 128);
 #pragma unroll
       for (int c = 0; c < HC; ++c) acc[c] = 0.0f;
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
-        const uint32_t b = kc & 1;
-        const int got = mbar_wait(smem_u32(&tfull[b]), (kc >> 1) & 1, &s_abort) ? 1 : 0;
+        const uint32_t b = kc % kAcc;
+        const int got = mbar_wait(smem_u32(&tfull[b]), (kc / kAcc) & 1, &s_abort) ? 1 : 0;
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + b * TT + half * HC;
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + b * TT + grp * HC;
         float d[HC];
-        if constexpr (HC == 8) {
-          tmem_ld8(taddr, d);
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < HC; c0 += 16) tmem_ld16(taddr + c0, d + c0);
-        }
+        tmem_ld<HC>(taddr, d);
         tmem_ld_wait();
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
-        const float4* cs = reinterpret_cast<const float4*>(my_comb + kb * HC);
+        const float sw = my_sw[kb];
+        const float4* s4p = reinterpret_cast<const float4*>(sa + kb * TT + grp * HC);
 #pragma unroll
         for (int c4 = 0; c4 < HC / 4; ++c4) {
-          const float4 s4 = cs[c4];
-          acc[4 * c4 + 0] = fmaf(d[4 * c4 + 0], s4.x, acc[4 * c4 + 0]);
-          acc[4 * c4 + 1] = fmaf(d[4 * c4 + 1], s4.y, acc[4 * c4 + 1]);
-          acc[4 * c4 + 2] = fmaf(d[4 * c4 + 2], s4.z, acc[4 * c4 + 2]);
-          acc[4 * c4 + 3] = fmaf(d[4 * c4 + 3], s4.w, acc[4 * c4 + 3]);
+          const float4 s4 = s4p[c4];
+          acc[4 * c4 + 0] = fmaf(d[4 * c4 + 0], s4.x * sw, acc[4 * c4 + 0]);
+          acc[4 * c4 + 1] = fmaf(d[4 * c4 + 1], s4.y * sw, acc[4 * c4 + 1]);
+          acc[4 * c4 + 2] = fmaf(d[4 * c4 + 2], s4.z * sw, acc[4 * c4 + 2]);
+          acc[4 * c4 + 3] = fmaf(d[4 * c4 + 3], s4.w * sw, acc[4 * c4 + 3]);
         }
       }
       const int n = nb * kBM + 32 * quarter + lane;
       if (ok && n < p.n) {
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
-          const int r = half * HC + c;
+          const int r = grp * HC + c;
           if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[c];
         }
       }
@@ -344,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(2 * TT < 32 ? 32 : 2 * TT));
+                 "r"(kAcc * TT < 32 ? 32 : kAcc * TT));
   }
 }
 
@@ -398,12 +451,25 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     return cudaSuccess;
   }
   const int KB = (int)cdiv(a.k, 128), NB = (int)cdiv(a.n, 128);
-  const size_t comb_bytes = (size_t)2 * KB * (TT / 2) * 4;
-  const size_t fixed = 1024 /*align*/ + comb_bytes + (tc::kMaxExperts + 2) * 4 + 8;
-  const size_t max_smem = 227 * 1024;
-  int stages = 8;
-  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 4) * 8 > max_smem) --stages;
-  const size_t smem = fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 4) * 8;
+  if (KB > tc::kMaxKB) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  const size_t scale_bytes = (size_t)KB * TT * 4 + (size_t)tc::kGroups * tc::kMaxKB * 4;
+  const size_t fixed = 1024 /*align*/ + scale_bytes + (tc::kMaxExperts + 2) * 4 + 8;
+  // dynamic shared memory budget: the device's opt-in maximum per block minus the
+  // kernel's static shared memory
+  cudaFuncAttributes fattr;
+  if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const size_t max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
+  constexpr int kAcc = tc::acc_count(TT);
+  int stages = 12;
+  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
+    --stages;
+  const size_t smem = fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8;
   if (smem > max_smem) {
     *unsupported = 1;
     return cudaSuccess;
@@ -444,7 +510,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   p.stages = stages;
   cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc::tc_gemm_kernel<TT><<<sm_count(), tc::kThreads, smem, st>>>(mw, ma, p);
+  tc::tc_gemm_kernel<TT><<<sm_count(), 64 + 32 * tc::kEpiWarps, smem, st>>>(mw, ma, p);
   return cudaGetLastError();
 }
 
