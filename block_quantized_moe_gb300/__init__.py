@@ -87,6 +87,7 @@ _SIGNATURES = [
     ("ftmoe_forward_workspace_bytes", c_size, [ctypes.POINTER(MoeShape)]),
     ("ftmoe_forward_workspace_layout", c_i32, [ctypes.POINTER(MoeShape), ctypes.POINTER(WorkspaceLayout)]),
     ("ftmoe_moe_forward", c_i32, [ctypes.POINTER(MoeArgs), c_ptr, c_size, c_ptr]),
+    ("ftmoe_moe_forward_noalloc", c_i32, [ctypes.POINTER(MoeArgs), c_ptr]),
     ("ftmoe_read_error_flags", c_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 ]
 
@@ -253,6 +254,13 @@ def ftmoe_moe_forward(shape, x, expert_ids, route_weights, bank_gateup, bank_dow
     _check("ftmoe_moe_forward", lib().ftmoe_moe_forward(
         ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def ftmoe_moe_forward_noalloc(shape, x, expert_ids, route_weights, bank_gateup, bank_down, out, stream=None):
+    """The fused forward with its intermediates in the library's own device array (no workspace)."""
+    args = MoeArgs(shape, _p(x), x.stride(0), _p(expert_ids), _p(route_weights), bank_gateup,
+                   bank_down, _p(out), out.stride(0))
+    _check("ftmoe_moe_forward_noalloc", lib().ftmoe_moe_forward_noalloc(ctypes.byref(args), _stream(stream)))
 
 
 def ftmoe_read_error_flags():

@@ -263,6 +263,24 @@ ftmoe_status ftmoe_forward_workspace_layout(const ftmoe_moe_shape* shape,
 ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Allocation-free variant of ftmoe_moe_forward (no counterpart in the pages; a service of
+ * this library). For callers that cannot allocate device memory themselves: a plugin
+ * hosted by a runtime that owns all device memory and exposes no allocator, code that
+ * records a CUDA graph in a capture mode where cudaMalloc is not allowed, or a latency
+ * path that cannot afford an allocation's implicit synchronisation. The intermediates
+ * live in a file-scope device array of 8 MiB that every GPU loading the library keeps
+ * until the process exits; shapes whose workspace (ftmoe_forward_workspace_bytes)
+ * exceeds it return FTMOE_WORKSPACE_TOO_SMALL. Decode-size shapes fit (8 tokens, top-8,
+ * hidden 4096, intermediate 1024 need about 1.7 MiB).
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. Every call
+ * on a device shares the one array: calls whose GPU work overlaps (other streams, other
+ * threads) race on it and must be serialised by the caller. The forward writes every
+ * region of the array before reading it, so a previous call's contents are never used.
+ * No cudaMalloc, cudaFree or allocating library routine is called. Inputs, outputs and
+ * their ownership are as for ftmoe_moe_forward. */
+ftmoe_status ftmoe_moe_forward_noalloc(const ftmoe_moe_args* args, void* stream);
+
 /* Reads and clears the device error word of the current device (FTMOE_ERR_* bits) into
  * *flags (host pointer). Synchronises the device; not for use inside graph capture. */
 ftmoe_status ftmoe_read_error_flags(uint32_t* flags);
