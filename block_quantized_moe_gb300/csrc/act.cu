@@ -168,6 +168,8 @@ cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, 
 }
 
 // ---- combine: out[t, h] = bf16( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
+// The slot ids, weights and rows of a token are loaded eight slots at a time with
+// independent loads, then accumulated in ascending slot order.
 template <bool kVec>
 __global__ void __launch_bounds__(128) combine_kernel(
     const float* __restrict__ y, int64_t ld_y, const int32_t* __restrict__ route2dst,
@@ -176,31 +178,55 @@ __global__ void __launch_bounds__(128) combine_kernel(
   const int64_t t = blockIdx.y;
   const int64_t h0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (h0 >= hidden) return;
+  const bool full = kVec && h0 + 4 <= hidden;
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int j = 0; j < topk; ++j) {
-    const int64_t r = t * topk + j;
-    if (ids[r] < 0) continue;  // inactive: neither the weight nor the row is read
-    const float wt = w[r];
-    const int64_t row = route2dst != nullptr ? (int64_t)route2dst[r] : r;
-    if (row < 0) continue;
-    const float* yr = y + row * ld_y + h0;
-    if (kVec && h0 + 4 <= hidden) {
-      const float4 v = *reinterpret_cast<const float4*>(yr);
-      acc[0] = fmaf(wt, v.x, acc[0]);
-      acc[1] = fmaf(wt, v.y, acc[1]);
-      acc[2] = fmaf(wt, v.z, acc[2]);
-      acc[3] = fmaf(wt, v.w, acc[3]);
-    } else {
+  for (int j0 = 0; j0 < topk; j0 += 8) {
+    int64_t row[8];
+    float wt[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (h0 + i < hidden) acc[i] = fmaf(wt, yr[i], acc[i]);
+    for (int u = 0; u < 8; ++u) {
+      row[u] = -1;
+      wt[u] = 0.0f;
+      const int j = j0 + u;
+      if (j < topk) {
+        const int64_t r = t * topk + j;
+        if (ids[r] >= 0) {  // inactive: neither the weight nor the row is read
+          wt[u] = w[r];
+          row[u] = route2dst != nullptr ? (int64_t)route2dst[r] : r;
+        }
+      }
+    }
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (row[u] >= 0) {
+        const float* yr = y + row[u] * ld_y + h0;
+        if (full) {
+          v[u] = *reinterpret_cast<const float4*>(yr);
+        } else {
+          v[u].x = yr[0];
+          if (h0 + 1 < hidden) v[u].y = yr[1];
+          if (h0 + 2 < hidden) v[u].z = yr[2];
+          if (h0 + 3 < hidden) v[u].w = yr[3];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (row[u] >= 0) {
+        acc[0] = fmaf(wt[u], v[u].x, acc[0]);
+        acc[1] = fmaf(wt[u], v[u].y, acc[1]);
+        acc[2] = fmaf(wt[u], v[u].z, acc[2]);
+        acc[3] = fmaf(wt[u], v[u].w, acc[3]);
+      }
     }
   }
   uint16_t b[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
   uint16_t* o = out + t * ld_out + h0;
-  if (kVec && h0 + 4 <= hidden) {
+  if (full) {
     *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16),
                                               (uint32_t)b[2] | ((uint32_t)b[3] << 16));
   } else {

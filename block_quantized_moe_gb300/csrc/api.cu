@@ -137,10 +137,15 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
   return FTMOE_OK;
 }
 
+// Automatic path: the route-slot streaming kernel for one or two tokens, the grouped
+// tensor-core path from three tokens on (measured crossover on GB300: at one token the
+// streaming path is faster, at eight the grouped one takes about half the time).
+constexpr int64_t kSlotPathMaxTokens = 2;
+
 bool use_grouped(const ftmoe_moe_shape* s) {
   if (s->path == 1) return false;
   if (s->path == 2) return true;
-  return s->tokens > 8;
+  return s->tokens > kSlotPathMaxTokens;
 }
 
 Layout make_layout(const ftmoe_moe_shape* s) {

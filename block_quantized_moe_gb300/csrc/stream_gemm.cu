@@ -377,8 +377,15 @@ static cudaError_t launch_part(const StreamGemmArgs& a, const CUtensorMap& map, 
   p.act_div = a.act_div;
   // members staged per pass: no more than one route per token can pick an expert in slot
   // mode, so small batches stage fewer rows and leave the shared memory to the ring
+  // members staged per pass. In slot mode an expert has at most one route per token (with
+  // distinct ids per token), and with top-k routing over many experts more than four
+  // tokens rarely share one; those rare experts take a second pass over L2-resident
+  // weights, and the shared memory goes to the weight ring instead.
   int mb = st::kMaxMembers;
-  if (!a.grouped && a.topk > 0 && routes / a.topk < mb) mb = (int)(routes / a.topk) > 0 ? (int)(routes / a.topk) : 1;
+  if (!a.grouped) {
+    const int64_t toks = a.topk > 0 ? routes / a.topk : routes;
+    mb = (int)(toks < 4 ? (toks > 0 ? toks : 1) : 4);
+  }
   while (mb > 1 && (size_t)mb * p.kp * 2 > st::kStageBudget) mb >>= 1;
   p.mb = mb;
   const size_t fixed = 1024 + (size_t)mb * p.kp * 2 + st::kMaxList * 4 + st::kMaxKB * 4 +
@@ -392,8 +399,14 @@ static cudaError_t launch_part(const StreamGemmArgs& a, const CUtensorMap& map, 
   if (grid > max_items) grid = max_items;
   if (!a.grouped && grid < 8) grid = 8;  // the zero rows of inactive routes
   if (grid < 1) grid = 1;
-  cudaError_t e = cudaFuncSetAttribute(st::stream_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static size_t granted[64] = {};  // per device: the largest limit set so far
+  if (dev < 0 || dev >= 64 || smem > granted[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(st::stream_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) granted[dev] = smem;
+  }
   st::stream_gemm_kernel<<<(unsigned)grid, st::kThreads, smem, stream>>>(map, p);
   return cudaGetLastError();
 }

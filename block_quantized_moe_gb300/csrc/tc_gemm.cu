@@ -459,12 +459,18 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   const size_t fixed = 1024 /*align*/ + scale_bytes + (tc::kMaxExperts + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
-  cudaFuncAttributes fattr;
-  if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
-  int dev = 0, optin = 0;
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const size_t max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
+  static size_t budget[64] = {};  // per device: opt-in maximum minus static shared memory
+  size_t max_smem = (dev >= 0 && dev < 64) ? budget[dev] : 0;
+  if (max_smem == 0) {
+    cudaFuncAttributes fattr;
+    if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
+    if (dev >= 0 && dev < 64) budget[dev] = max_smem;
+  }
   constexpr int kAcc = tc::acc_count(TT);
   int stages = 12;
   while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
@@ -508,8 +514,17 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   p.kb_count = KB;
   p.nb_count = NB;
   p.stages = stages;
-  cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // raise the kernel's dynamic shared memory limit only when a launch needs more than
+  // any earlier one on this device (the attribute is per function and device)
+  static size_t granted[64] = {};
+  if (dev >= 0 && dev < 64 && smem > granted[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    granted[dev] = smem;
+  } else if (dev < 0 || dev >= 64) {
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   tc::tc_gemm_kernel<TT><<<sm_count(), 64 + 32 * tc::kEpiWarps, smem, st>>>(mw, ma, p);
   return cudaGetLastError();
 }

@@ -38,11 +38,13 @@ def test_decode_2048_768_two_of_eight_active(ft):
     _check(p, out)
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("T", [1, 8])
 @pytest.mark.parametrize("active", [8, 4, 2, 0])
-def test_decode_4096_1024_sweep(ft, T, active):
+def test_decode_4096_1024_sweep(ft, T, active, path):
+    # path 1: route-slot streaming kernel; path 2: segment + gather + tcgen05 grouped GEMMs
     p = Problem(T, 4096, 1024, 64, 8, seed=0xF7E00002, active=active)
-    out, ws, shape = p.forward()
+    out, ws, shape = p.forward(path=path)
     torch.cuda.synchronize()
     ref = _check(p, out)
     if active == 0:
@@ -62,11 +64,11 @@ def _poison(ws, lay):
             region.fill_(0xFF)
 
 
-@pytest.mark.parametrize("T", [1, 8])
-def test_graph_replay_with_poisoned_intermediates(ft, T):
+@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (8, 2)])
+def test_graph_replay_with_poisoned_intermediates(ft, T, path):
     H, I, E, k = 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=8)
-    shape = ft.moe_shape(T, H, I, k, E)
+    shape = ft.moe_shape(T, H, I, k, E, path=path)
     lay = ft.ftmoe_forward_workspace_layout(shape)
     ws = torch.empty(lay["total"], dtype=torch.uint8, device=DEV)
     x_in = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
@@ -98,7 +100,10 @@ def test_graph_replay_with_poisoned_intermediates(ft, T):
         g.replay()
         torch.cuda.synchronize()
         _check(p, out, ids=ids, weights=w, x=x)
-        # inactive routes: exact zeros in the gate/up, activation and down buffers
+        assert not torch.any(torch.isnan(out.float()))
+        if path == 2:
+            continue  # grouped path: inactive routes have no rows at all
+        # route-slot path: exact zeros in the gate/up, activation and down rows of inactive routes
         R = T * k
         gu = ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(R, 2 * I)
         dn = ws[lay["down"]:lay["down"] + lay["down_bytes"]].view(torch.float32).view(R, H)
@@ -113,24 +118,26 @@ def test_graph_replay_with_poisoned_intermediates(ft, T):
         assert not torch.any(torch.isnan(out.float()))
 
 
-def test_negative_slots_equal_clamped_zero_weight_path(ft):
+@pytest.mark.parametrize("path", [1, 2])
+def test_negative_slots_equal_clamped_zero_weight_path(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=2)
     ids_new = p.ids.clone()
     w_new = torch.where(ids_new >= 0, p.w, torch.full_like(p.w, float("nan")))
     ids_old = torch.where(ids_new >= 0, ids_new, torch.zeros_like(ids_new))  # slot 0 ...
     w_old = torch.where(ids_new >= 0, p.w, torch.zeros_like(p.w))             # ... weight 0
-    out_new, _, _ = p.forward(ids=ids_new, weights=w_new)
-    out_old, _, _ = p.forward(ids=ids_old, weights=w_old)
+    out_new, _, _ = p.forward(path=path, ids=ids_new, weights=w_new)
+    out_old, _, _ = p.forward(path=path, ids=ids_old, weights=w_old)
     torch.cuda.synchronize()
     assert torch.equal(out_new.view(torch.int16), out_old.view(torch.int16))
 
 
-def test_all_inactive_and_empty_bank_use(ft):
+@pytest.mark.parametrize("path", [1, 2])
+def test_all_inactive_and_empty_bank_use(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=0)
     w = torch.full_like(p.w, float("nan"))
-    out, ws, shape = p.forward(weights=w)
+    out, ws, shape = p.forward(path=path, weights=w)
     torch.cuda.synchronize()
     assert torch.all(out.view(torch.int16) == 0)
 
@@ -142,7 +149,7 @@ def test_out_of_range_expert_id_is_flagged_not_read(ft):
     ids = p.ids.clone()
     ids[0, (ids[0] < 0).nonzero()[0, 0]] = E + 3  # one bad id in place of an inactive slot
     w = p.w.clone()
-    out, _, _ = p.forward(ids=ids, weights=w)
+    out, _, _ = p.forward(path=1, ids=ids, weights=w)
     flags = ft.ftmoe_read_error_flags()
     assert flags & ft.ERR_EXPERT_ID_RANGE
     ref_ids = torch.where(ids >= E, torch.full_like(ids, -1), ids)
