@@ -61,6 +61,25 @@ WORKLOADS = {
 DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
 
 
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from profiles/traffic.txt, or None when
+    no capture is recorded or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for ln in open(path):
+        parts = ln.split()
+        if len(parts) != 4 or ln.startswith("#") or parts[0] != workload:
+            continue
+        src = os.path.join(ROOT, "block_quantized_moe_gb300", parts[1])
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        return int(parts[3]) if sha == parts[2] else None
+    return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -407,7 +426,7 @@ def run_gpu(args, rank, world, local):
         "algorithmic_bytes_per_call": int(bytes_avg),
         "roofline": {"kernel": kname, "bound": "hbm",
                      "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(k_gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(k_gbs / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
                      "launch_us": round(k_us, 3), "algorithmic_bytes_per_launch": int(gu_bytes_avg),
                      "fp8_tflops": round(k_tflops, 2), "fp8_frac_of_dense_peak": round(k_tflops / fp8_peak, 4),
                      "peak_source": peak_src},
