@@ -44,23 +44,6 @@ constexpr int kMaxExperts = 1024;
 // most 16, so the MMA can run that many K blocks ahead of the promotion
 __host__ __device__ constexpr int acc_count(int tt) { return 512 / tt > 16 ? 16 : 512 / tt; }
 
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes, written by
-// TMA with the 128-byte swizzle: 8-row swizzle atoms of 1024 bytes stacked along M/N
-// (stride byte offset 1024); the leading byte offset is unused because the tile's K
-// extent is exactly one swizzle atom wide.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFF) >> 4);        // start address
-  d |= (uint64_t)1 << 16;                         // leading byte offset (unused), 16 B
-  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
-  d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
-  return d;
-}
-
 // Instruction descriptor, kind::f8f6f4: D fp32, A = B = e4m3, both K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_f8(int n) {
   return (1u << 4)                      // D format f32
@@ -75,34 +58,6 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// 16 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 8 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct Params {
   const int32_t* offsets;
@@ -124,23 +79,6 @@ struct Smem {
   static constexpr int kTileA = TT * kBK;     // TT * 128 B
   static constexpr int kStage = kTileW + kTileA;
 };
-
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
-  if constexpr (N == 4) {
-    uint32_t r[4];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-  } else if constexpr (N == 8) {
-    tmem_ld8(taddr, v);
-  } else {
-#pragma unroll
-    for (int c = 0; c < N; c += 16) tmem_ld16(taddr + c, v + c);
-  }
-}
 
 // Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the activation
 // scales of the current token tile sa[kb][TT], the weight-block scales of the current unit
