@@ -37,6 +37,37 @@ ftmoe_status check_bank(const ftmoe_expert_bank* w) {
   return FTMOE_OK;
 }
 
+// NVFP4: the grouped layout on the block-scaled tensor-core kernel only (no streaming
+// kernel for e2m1 codes). Scale rows of k/16 bytes are read by TMA, so k % 256 == 0.
+ftmoe_status grouped_gemm_nvfp4(const ftmoe_act* a, const ftmoe_routes* routes, const ftmoe_expert_bank* w,
+                                float* out, int64_t ld_out, const ftmoe_tile* tile, int variant, void* stream) {
+  if (routes->kind == FTMOE_ROUTES_SLOTS) return FTMOE_UNSUPPORTED;
+  if (routes->kind != FTMOE_ROUTES_GROUPED || !routes->offsets) return FTMOE_INVALID_ARG;
+  if (a->rows == 0) return FTMOE_OK;
+  if (!a->global_scale) return FTMOE_INVALID_ARG;
+  if (variant == 1) return FTMOE_UNSUPPORTED;
+  NvGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a_q = a->q;
+  g.a_sf = static_cast<const uint8_t*>(a->scales);
+  g.a_gscale = a->global_scale;
+  g.a_rows = a->rows;
+  g.w_q = w->q;
+  g.w_sf = static_cast<const uint8_t*>(w->scales);
+  g.w_gscale = w->global_scale;
+  g.out = out;
+  g.ld_out = ld_out;
+  g.n = w->n;
+  g.k = w->k;
+  g.E = w->num_experts;
+  g.offsets = routes->offsets;
+  g.tok_tile = (tile && tile->tok_tile) ? tile->tok_tile : pick_tile_value(a->rows, w->num_experts);
+  int unsupported = 0;
+  cudaError_t e = launch_nvfp4_gemm(g, as_stream(stream), &unsupported);
+  if (unsupported) return FTMOE_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const ftmoe_expert_bank* w,
                           float* out, int64_t ld_out, const ftmoe_tile* tile, void* stream,
                           bool is_down) {
@@ -50,7 +81,7 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
     return FTMOE_INVALID_ARG;
   if (tile && (tile->variant < 0 || tile->variant > 2)) return FTMOE_INVALID_ARG;
   const int variant = tile ? tile->variant : 0;
-  if (w->format != FTMOE_FMT_FP8) return FTMOE_UNSUPPORTED;  // NVFP4 GEMMs: grouped path only (below)
+  if (w->format == FTMOE_FMT_NVFP4) return grouped_gemm_nvfp4(a, routes, w, out, ld_out, tile, variant, stream);
   // both GEMM kernels read K-contiguous rows through TMA: 16-byte aligned rows
   if (w->k % 16 != 0 || (uintptr_t)w->q % 16 != 0 || (a->rows > 0 && (uintptr_t)a->q % 16 != 0))
     return FTMOE_UNSUPPORTED;
@@ -144,7 +175,7 @@ constexpr int64_t kSlotPathMaxTokens = 2;
 
 bool use_grouped(const ftmoe_moe_shape* s) {
   if (s->path == 1) return false;
-  if (s->path == 2) return true;
+  if (s->path == 2 || s->format == FTMOE_FMT_NVFP4) return true;
   return s->tokens > kSlotPathMaxTokens;
 }
 
@@ -334,22 +365,24 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   const Layout L = make_layout(s);
   if (!workspace) return FTMOE_INVALID_ARG;
   if (workspace_bytes < L.l.total) return FTMOE_WORKSPACE_TOO_SMALL;
-  if (f != FTMOE_FMT_FP8) return FTMOE_UNSUPPORTED;
+  if (f == FTMOE_FMT_NVFP4 && !L.grouped) return FTMOE_UNSUPPORTED;  // no route-slot kernel for e2m1
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t R = T * s->topk;
   cudaStream_t strm = as_stream(stream);
   uint8_t* xq = ws + L.l.x_q;
-  float* xs = reinterpret_cast<float*>(ws + L.l.x_scales);
+  void* xs = ws + L.l.x_scales;
+  float* xg = f == FTMOE_FMT_NVFP4 ? reinterpret_cast<float*>(ws + L.l.x_gscale) : nullptr;
   float* gu = reinterpret_cast<float*>(ws + L.l.gateup);
   uint8_t* aq = ws + L.l.act_q;
-  float* as = reinterpret_cast<float*>(ws + L.l.act_scales);
+  void* as = ws + L.l.act_scales;
+  float* ag = f == FTMOE_FMT_NVFP4 ? reinterpret_cast<float*>(ws + L.l.act_gscale) : nullptr;
   float* y = reinterpret_cast<float*>(ws + L.l.down);
   ftmoe_tile tile;
   memset(&tile, 0, sizeof(tile));
   tile.tok_tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, (int32_t)E);
 
-  st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, nullptr, stream);
+  st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, xg, stream);
   if (st != FTMOE_OK) return st;
   if (!L.grouped) {
     ftmoe_routes rt;
@@ -358,12 +391,12 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
     rt.topk = s->topk;
     rt.tokens = T;
     rt.slots = args->expert_ids;
-    ftmoe_act a1 = {f, 0, T, H, xq, xs, nullptr};
+    ftmoe_act a1 = {f, 0, T, H, xq, xs, xg};
     st = ftmoe_grouped_gemm_gateup(&a1, &rt, &wg, gu, 2 * I, &tile, stream);
     if (st != FTMOE_OK) return st;
-    st = ftmoe_silu_mul(gu, R, I, 2 * I, nullptr, f, aq, as, nullptr, stream);
+    st = ftmoe_silu_mul(gu, R, I, 2 * I, nullptr, f, aq, as, ag, stream);
     if (st != FTMOE_OK) return st;
-    ftmoe_act a2 = {f, 0, R, I, aq, as, nullptr};
+    ftmoe_act a2 = {f, 0, R, I, aq, as, ag};
     st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
     if (st != FTMOE_OK) return st;
     return ftmoe_combine(y, H, nullptr, args->expert_ids, args->route_weights, T, s->topk, H,
@@ -374,23 +407,23 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   int32_t* dst2src = reinterpret_cast<int32_t*>(ws + L.l.dst2src);
   int32_t* route2dst = reinterpret_cast<int32_t*>(ws + L.l.route2dst);
   uint8_t* rq = ws + L.l.rows_q;
-  float* rs = reinterpret_cast<float*>(ws + L.l.rows_scales);
+  void* rs = ws + L.l.rows_scales;
   st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src,
                             route2dst, stream);
   if (st != FTMOE_OK) return st;
-  st = ftmoe_gather_rows_scales(xq, xs, T, H, (int64_t)scale_row_bytes(f, H), dst2src, R,
+  st = ftmoe_gather_rows_scales(xq, xs, T, (int64_t)code_row_bytes(f, H), (int64_t)scale_row_bytes(f, H), dst2src, R,
                                 offsets + E, rq, rs, stream);
   if (st != FTMOE_OK) return st;
   ftmoe_routes rt;
   memset(&rt, 0, sizeof(rt));
   rt.kind = FTMOE_ROUTES_GROUPED;
   rt.offsets = offsets;
-  ftmoe_act a1 = {f, 0, R, H, rq, rs, nullptr};
+  ftmoe_act a1 = {f, 0, R, H, rq, rs, xg};
   st = ftmoe_grouped_gemm_gateup(&a1, &rt, &wg, gu, 2 * I, &tile, stream);
   if (st != FTMOE_OK) return st;
-  st = ftmoe_silu_mul(gu, R, I, 2 * I, offsets + E, f, aq, as, nullptr, stream);
+  st = ftmoe_silu_mul(gu, R, I, 2 * I, offsets + E, f, aq, as, ag, stream);
   if (st != FTMOE_OK) return st;
-  ftmoe_act a2 = {f, 0, R, I, aq, as, nullptr};
+  ftmoe_act a2 = {f, 0, R, I, aq, as, ag};
   st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
   if (st != FTMOE_OK) return st;
   return ftmoe_combine(y, H, route2dst, args->expert_ids, args->route_weights, T, s->topk, H,
@@ -401,7 +434,7 @@ ftmoe_status ftmoe_read_error_flags(uint32_t* flags) {
   if (!flags) return FTMOE_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return FTMOE_CUDA_ERROR;
   *flags = read_err_quant() | read_err_segment() | read_err_gather() | read_err_stream_gemm() |
-           read_err_tc_gemm() | read_err_act();
+           read_err_tc_gemm() | read_err_nvfp4() | read_err_act();
   return FTMOE_OK;
 }
 

@@ -21,6 +21,9 @@ int sm_count();
 // outer dims); false if the driver entry point is missing or the encoding is rejected
 bool encode_u8_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                     const uint32_t* box);
+// the same without swizzle (small tiles such as scale rows)
+bool encode_u8_tmap_plain(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box);
 
 // quant.cu
 cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
@@ -86,6 +89,25 @@ struct TcGemmArgs {
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s, int* unsupported);
 uint32_t read_err_tc_gemm();
+
+// tc_nvfp4.cu: grouped NVFP4 GEMM on the block-scaled tcgen05 MMA
+struct NvGemmArgs {
+  const uint8_t* a_q;       // e2m1 codes [a_rows][k/2]
+  const uint8_t* a_sf;      // e4m3 block scales [a_rows][k/16]
+  const float* a_gscale;    // device float[1]
+  int64_t a_rows;
+  const uint8_t* w_q;       // [E][n][k/2]
+  const uint8_t* w_sf;      // [E][n][k/16]
+  const float* w_gscale;    // device float[E]
+  float* out;
+  int64_t ld_out;
+  int64_t n, k;
+  int32_t E;
+  const int32_t* offsets;
+  int32_t tok_tile;
+};
+cudaError_t launch_nvfp4_gemm(const NvGemmArgs& a, cudaStream_t s, int* unsupported);
+uint32_t read_err_nvfp4();
 
 // act.cu: silu_mul and combine
 cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,

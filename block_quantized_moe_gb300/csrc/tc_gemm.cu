@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
 // host side
 // ---------------------------------------------------------------------------------
 
-bool encode_u8_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                    const uint32_t* box) {
+static bool encode_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                      const uint32_t* box, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t d[3], st[2];
@@ -357,8 +357,18 @@ bool encode_u8_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t
   }
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_u8_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box) {
+  return encode_u8(map, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_u8_tmap_plain(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box) {
+  return encode_u8(map, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 EncodeTiledFn encode_fn() {

@@ -1,0 +1,430 @@
+// Grouped NVFP4 GEMM on the block-scaled tensor-core MMA (tcgen05 kind::mxf4nvf4).
+//
+// out[row, n] = g_a * g_w[e] * sum_k (a[row,k] * sa[row, k/16]) * (w[e,n,k] * sw[e,n,k/16])
+// with e2m1 codes a, w (two per byte, even element in the low nibble), e4m3 block scales
+// sa, sw (one per 16 elements) and fp32 tensor scales g_a, g_w[e] -- the NVFP4 variant of
+// the prefill GEMM (the dsfp4 page names the format; the two-level recipe is fixed in the
+// design notes). Unlike the FP8 path, the block scales are native to the MMA
+// (tcgen05.mma ... kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per instruction, one
+// ue4m3 scale per 16 elements of each row), so a unit accumulates all of K in TMEM and the
+// epilogue only applies g_a * g_w once.
+//
+// Work layout as in the FP8 kernel: MMA M = 128 weight rows, MMA N = the token tile; one
+// persistent CTA per SM over a contiguous range of (expert, token tile, weight block) units.
+// Roles: warp 0 TMA producer (code tiles with the 128-byte swizzle, scale tiles plain);
+// warp 1 MMA issuer and TMEM owner; warps 2-5 move each stage's scale factors from shared
+// memory into TMEM, warps 6-13 epilogue. Every wait is bounded.
+//
+// Scale factors in TMEM, per operand and MMA step (K = 64, four e4m3 scales per row): four
+// 32-bit columns; column c of lane l holds the four scales of row l + 32c, and every lane
+// quarter holds the same copy (each sub-partition reads the scales it needs from its own
+// quarter). This is the 128x4 block-scale chunk layout (32 rows of 16 bytes) replicated
+// into the four quarters.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ftmoe {
+
+namespace nv {
+
+constexpr int kBM = 128;           // weight rows per tile (MMA M)
+constexpr int kBKB = 128;          // code bytes per row per stage = 256 elements
+constexpr int kSfPerStage = 16;    // scale bytes per row per stage
+constexpr int kScaleWarp0 = 2, kScaleWarps = 4;
+constexpr int kEpiWarp0 = kScaleWarp0 + kScaleWarps, kEpiWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // 448
+constexpr int kMaxExperts = 1024;
+constexpr int kAcc = 2;            // accumulators: the next unit's MMAs run during this unit's epilogue
+
+template <int TT>
+struct Sz {
+  static constexpr int kW = kBM * kBKB;             // 16 KiB of weight codes
+  static constexpr int kA = TT * kBKB;              // token codes
+  static constexpr int kSW = kBM * kSfPerStage;     // weight scales
+  static constexpr int kSA = TT * kSfPerStage;      // token scales
+  static constexpr int kStage = ((kW + kA + kSW + kSA) + 1023) / 1024 * 1024;
+};
+
+// Instruction descriptor of kind::mxf4nvf4: A = B = E2M1, ue4m3 scale factors, both
+// operands K-major, M = 128, N = n, K = 64, scale-factor ids 0 (all four scales of a
+// 32-bit column are used by scale_vec::4X).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
+  return (1u << 7)                          // A format: E2M1
+         | (1u << 10)                       // B format: E2M1
+         | ((uint32_t)(n >> 3) << 17)       // N >> 3
+         | (0u << 23)                       // scale format: UE4M3
+         | ((uint32_t)(kBM >> 4) << 24);    // M >> 4
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(acc)
+      : "memory");
+}
+
+struct Params {
+  const int32_t* offsets;
+  const float* g_a;   // [1]
+  const float* g_w;   // [E]
+  float* out;
+  int64_t ld_out;
+  int64_t a_rows;
+  int n, E, kb_count, nb_count, stages;
+};
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a,
+                      const __grid_constant__ CUtensorMap map_sw, const __grid_constant__ CUtensorMap map_sa,
+                      Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int S = p.stages;
+  uint8_t* tiles = smem;
+  int* cum = reinterpret_cast<int*>(smem + (size_t)S * Sz<TT>::kStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(cum + kMaxExperts + 2)) + 7) & ~(uintptr_t)7);
+  uint64_t* full = bars;            // TMA landed (codes and scales)
+  uint64_t* empty = bars + S;       // MMAs done reading the stage (for the producer)
+  uint64_t* sfree = bars + 2 * S;   // MMAs done reading the stage's TMEM scales (for the scale warps)
+  uint64_t* sfull = bars + 3 * S;   // scale factors in TMEM
+  uint64_t* tfull = bars + 4 * S;
+  uint64_t* tempty = bars + 4 * S + kAcc;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, NB = p.nb_count, KB = p.kb_count;
+  // TMEM columns: accumulators [0, kAcc*TT), then 32 scale columns per stage
+  // (16 for the weight rows, 16 for the token rows)
+  const uint32_t sf0 = (uint32_t)((kAcc * TT + 31) / 32 * 32);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+      mbar_init(smem_u32(&sfree[i]), 1);
+      mbar_init(smem_u32(&sfull[i]), kScaleWarps);
+    }
+    for (int i = 0; i < kAcc; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), kEpiWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int u = 0;
+      if (e < E) {
+        int lo = p.offsets[e], hi = p.offsets[e + 1];
+        if (lo < 0) lo = 0;
+        if (hi > p.a_rows) hi = (int)p.a_rows;
+        const int m = hi > lo ? hi - lo : 0;
+        u = ((m + TT - 1) / TT) * NB;
+      }
+      int inc = u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (e < E) cum[e] = run + inc - u;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) cum[E] = run;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int total_units = cum[E];
+  const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
+  const int u_end = (int)(((int64_t)(blockIdx.x + 1) * total_units) / gridDim.x);
+
+  auto decode = [&](int u, int& e, int& nb, int& row0, int& rows) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    int s0 = p.offsets[e], s1 = p.offsets[e + 1];
+    if (s0 < 0) s0 = 0;
+    if (s1 > p.a_rows) s1 = (int)p.a_rows;
+    const int local = u - cum[e];
+    const int tt = local / NB;
+    nb = local - tt * NB;
+    row0 = s0 + tt * TT;
+    rows = min(TT, s1 - row0);
+  };
+
+  if (warp == 0) {
+    // ------------------------------- TMA producer -------------------------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int u = u_begin; u < u_end && !s_abort; ++u) {
+        int e, nb, row0, rows;
+        decode(u, e, nb, row0, rows);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int st = it % S;
+          if (!mbar_wait(smem_u32(&empty[st]), ((it / S) & 1) ^ 1, &s_abort)) break;
+          uint8_t* t0 = tiles + (size_t)st * Sz<TT>::kStage;
+          const uint32_t fb = smem_u32(&full[st]);
+          mbar_expect_tx(fb, Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW + Sz<TT>::kSA);
+          tma_load_3d(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e);
+          tma_load_2d(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0);
+          tma_load_3d(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e);
+          tma_load_2d(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0);
+        }
+      }
+      const uint32_t issued = it;
+      for (int st = 0; st < S && (uint32_t)st < issued; ++st) {
+        const uint32_t last = issued - 1 - ((issued - 1 - st) % S);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&full[st]), (last / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------- MMA issuer --------------------------------
+    if (lane == 0) {
+      uint32_t it = 0, uc = 0;
+      constexpr uint32_t idesc = idesc_nvf4(TT);
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok && !s_abort; ++u, ++uc) {
+        const uint32_t acc = uc % kAcc;
+        if (!mbar_wait(smem_u32(&tempty[acc]), ((uc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
+        fence_after();
+        const uint32_t d = tmem_base + acc * TT;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int st = it % S;
+          if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&sfull[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
+          fence_after();
+          const uint32_t tw = smem_u32(tiles + (size_t)st * Sz<TT>::kStage);
+          const uint32_t ta = tw + Sz<TT>::kW;
+          const uint32_t sfa = tmem_base + sf0 + 32u * st;
+          const uint32_t sfb = sfa + 16u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_nvf4(d, smem_desc_sw128(tw + 32 * j), smem_desc_sw128(ta + 32 * j), idesc, sfa + 4 * j, sfb + 4 * j,
+                     (kb | j) != 0 ? 1u : 0u);
+          mma_commit(smem_u32(&empty[st]));
+          mma_commit(smem_u32(&sfree[st]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&tfull[acc]));
+      }
+      // drain: the last commit of each accumulator before the CTA may free TMEM
+      for (uint32_t b = 0; b < (uint32_t)kAcc && b < uc; ++b) {
+        const uint32_t last = uc - 1 - ((uc - 1 - b) % kAcc);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&tfull[b]), (last / kAcc) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      for (uint32_t st = 0; st < (uint32_t)S && st < it; ++st) {
+        const uint32_t last = it - 1 - ((it - 1 - st) % S);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&sfree[st]), (last / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------- scale factors -> TMEM -------------------------
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    uint32_t it = 0;
+    for (int u = u_begin; u < u_end; ++u) {
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int st = it % S;
+        int got = mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort) ? 1 : 0;
+        if (got) got = mbar_wait(smem_u32(&sfree[st]), ((it / S) & 1) ^ 1, &s_abort) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        fence_after();
+        const uint8_t* sw_t = tiles + (size_t)st * Sz<TT>::kStage + Sz<TT>::kW + Sz<TT>::kA;
+        const uint8_t* sa_t = sw_t + Sz<TT>::kSW;
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + sf0 + 32u * st;
+        // column 4j + c of lane l (in every lane quarter): the four scales of MMA step j
+        // for row l + 32c
+        uint32_t r[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sw_t + (lane + 32 * c) * kSfPerStage);
+          r[c] = v.x;
+          r[4 + c] = v.y;
+          r[8 + c] = v.z;
+          r[12 + c] = v.w;
+        }
+        tmem_st16(taddr, r);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (lane + 32 * c < TT) v = *reinterpret_cast<const uint4*>(sa_t + (lane + 32 * c) * kSfPerStage);
+          r[c] = v.x;
+          r[4 + c] = v.y;
+          r[8 + c] = v.z;
+          r[12 + c] = v.w;
+        }
+        tmem_st16(taddr + 16u, r);
+        tmem_st_wait();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sfull[st]));
+      }
+      if (!ok) break;
+    }
+  } else {
+    // --------------------------------- epilogue ---------------------------------
+    const int ew = warp - kEpiWarp0;   // 0..7
+    const int half = ew >> 2;          // token-column half
+    const int quarter = warp & 3;
+    constexpr int HC = TT / 2;
+    uint32_t uc = 0;
+    for (int u = u_begin; u < u_end; ++u, ++uc) {
+      int e, nb, row0, rows;
+      decode(u, e, nb, row0, rows);
+      const float f = __ldg(p.g_a) * __ldg(p.g_w + e);
+      const uint32_t acc = uc % kAcc;
+      const int got = mbar_wait(smem_u32(&tfull[acc]), (uc / kAcc) & 1, &s_abort) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, got)) break;
+      fence_after();
+      const int n = nb * kBM + 32 * quarter + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + acc * TT + half * HC;
+#pragma unroll
+      for (int c0 = 0; c0 < HC; c0 += (HC < 16 ? HC : 16)) {
+        float d[16];
+        if constexpr (HC == 8) {
+          tmem_ld8(taddr + c0, d);
+        } else {
+          tmem_ld16(taddr + c0, d);
+        }
+        tmem_ld_wait();
+        if (n < p.n) {
+#pragma unroll
+          for (int c = 0; c < (HC < 16 ? HC : 16); ++c) {
+            const int r = half * HC + c0 + c;
+            if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = d[c] * f;
+          }
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+  }
+}
+
+}  // namespace nv
+
+template <int TT>
+static cudaError_t launch_nv(const NvGemmArgs& a, cudaStream_t st, int* unsupported) {
+  const int KB = (int)cdiv(a.k, 256), NB = (int)cdiv(a.n, 128);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static size_t budget[64] = {};
+  size_t max_smem = (dev >= 0 && dev < 64) ? budget[dev] : 0;
+  if (max_smem == 0) {
+    cudaFuncAttributes fattr;
+    if (cudaFuncGetAttributes(&fattr, nv::nvfp4_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
+    if (dev >= 0 && dev < 64) budget[dev] = max_smem;
+  }
+  const size_t fixed = 1024 + (nv::kMaxExperts + 2) * 4 + 8;
+  // TMEM: accumulators plus 32 scale columns per stage must fit 512 columns
+  const int tmem_stages = (512 - (nv::kAcc * TT + 31) / 32 * 32) / 32;
+  int stages = tmem_stages < 8 ? tmem_stages : 8;
+  while (stages > 2 && fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8 > max_smem)
+    --stages;
+  const size_t smem = fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8;
+  if (smem > max_smem || stages < 2) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  CUtensorMap mw, ma, msw, msa;
+  {
+    const uint64_t dims[3] = {(uint64_t)(a.k / 2), (uint64_t)a.n, (uint64_t)a.E};
+    const uint64_t strides[2] = {(uint64_t)(a.k / 2), (uint64_t)(a.k / 2) * (uint64_t)a.n};
+    const uint32_t box[3] = {(uint32_t)nv::kBKB, (uint32_t)nv::kBM, 1};
+    if (!encode_u8_tmap(&mw, a.w_q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)(a.k / 2), (uint64_t)a.a_rows};
+    const uint64_t strides[1] = {(uint64_t)(a.k / 2)};
+    const uint32_t box[2] = {(uint32_t)nv::kBKB, (uint32_t)TT};
+    if (!encode_u8_tmap(&ma, a.a_q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)(a.k / 16), (uint64_t)a.n, (uint64_t)a.E};
+    const uint64_t strides[2] = {(uint64_t)(a.k / 16), (uint64_t)(a.k / 16) * (uint64_t)a.n};
+    const uint32_t box[3] = {(uint32_t)nv::kSfPerStage, (uint32_t)nv::kBM, 1};
+    if (!encode_u8_tmap_plain(&msw, a.w_sf, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)(a.k / 16), (uint64_t)a.a_rows};
+    const uint64_t strides[1] = {(uint64_t)(a.k / 16)};
+    const uint32_t box[2] = {(uint32_t)nv::kSfPerStage, (uint32_t)TT};
+    if (!encode_u8_tmap_plain(&msa, a.a_sf, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  nv::Params p;
+  p.offsets = a.offsets;
+  p.g_a = a.a_gscale;
+  p.g_w = a.w_gscale;
+  p.out = a.out;
+  p.ld_out = a.ld_out;
+  p.a_rows = a.a_rows;
+  p.n = (int)a.n;
+  p.E = a.E;
+  p.kb_count = KB;
+  p.nb_count = NB;
+  p.stages = stages;
+  static size_t granted[64] = {};
+  if (dev < 0 || dev >= 64 || smem > granted[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(nv::nvfp4_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) granted[dev] = smem;
+  }
+  nv::nvfp4_gemm_kernel<TT><<<sm_count(), nv::kThreads, smem, st>>>(mw, ma, msw, msa, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_gemm(const NvGemmArgs& a, cudaStream_t st, int* unsupported) {
+  *unsupported = 0;
+  // TMA: code rows of k/2 bytes and scale rows of k/16 bytes must be 16-byte multiples
+  if (a.k % 256 != 0 || (uintptr_t)a.w_q % 16 != 0 || (uintptr_t)a.a_q % 16 != 0 || (uintptr_t)a.w_sf % 16 != 0 ||
+      (uintptr_t)a.a_sf % 16 != 0 || a.E > nv::kMaxExperts || a.n > (1 << 30) || a.a_rows > (1 << 30)) {
+    *unsupported = 1;
+    return cudaSuccess;
+  }
+  switch (a.tok_tile) {
+    case 16: return launch_nv<16>(a, st, unsupported);
+    case 32: return launch_nv<32>(a, st, unsupported);
+    case 64: return launch_nv<64>(a, st, unsupported);
+    case 128: return launch_nv<128>(a, st, unsupported);
+    default: *unsupported = 1; return cudaSuccess;
+  }
+}
+
+FTMOE_DEFINE_ERR_READER(read_err_nvfp4)
+
+}  // namespace ftmoe

@@ -96,20 +96,131 @@ def requant_flip_bound(res, expert_ids, weights, bank_gu, bank_dn):
     return extra
 
 
+# The block-scaled tensor-core MMA accumulates e2m1 x e2m1 products with their e4m3 scales;
+# its error is bounded here like an fp32 sum, with 4x the FP8 allowance for the unknown
+# internal order of the 64-wide K steps.
+NVFP4_SUM_REL = 2.0 ** -20
+
+
+def _silu_mul_error(gu, absum, rel_sum):
+    """Bound on the kernels' fp32 error in silu(g)*u from the gate/up outputs' errors."""
+    inter = gu.shape[0] // 2
+    eg = rel_sum * absum + 2.0 ** -21 * np.abs(gu)
+    g, u = gu[:inter], gu[inter:]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    return np.abs(dsilu * u) * eg[:inter] + np.abs(g * sig) * eg[inter:]
+
+
+def nvfp4_requant_flip_bound(res, expert_ids, weights, bank_gu, bank_dn):
+    """requant_flip_bound for the NVFP4 intermediate: the tensor scale g (from the amax over
+    all routes), each 16-block's e4m3 scale and each e2m1 code are decisions the kernels
+    take from fp32 values; where one lies within their error of a rounding midpoint either
+    neighbour is correct. An ambiguous block scale moves every element of the block by at
+    most one quantization error per candidate (<= one effective scale each); an ambiguous
+    code moves its element by the gap between the two codes. Oracle values only."""
+    from oracle import formats as F
+    ids = np.asarray(expert_ids)
+    w = np.asarray(weights, np.float64)
+    T = ids.shape[0]
+    H = res["out"].shape[1]
+    extra = np.zeros((T, H))
+    e2 = F.E2M1_VALUES[:8]
+    mids2 = (e2[:-1] + e2[1:]) / 2
+    e4 = F.E4M3_VALUES[:0x7F]
+    mids4 = (e4[:-1] + e4[1:]) / 2
+    keys = sorted(res["a"].keys())
+    if not keys:
+        return extra
+    eas = {}
+    for (t, j) in keys:
+        e = int(ids[t, j])
+        gu = res["gu"][(t, j)]
+        absum = np.abs(bank_gu.dequant(e)) @ np.abs(res["xdeq"][t])
+        a = res["a"][(t, j)]
+        eas[(t, j)] = _silu_mul_error(gu, absum, NVFP4_SUM_REL) + 2.0 ** -21 * np.abs(a)
+    allabs = np.stack([np.abs(res["a"][k].astype(np.float32).astype(np.float64)) for k in keys])
+    alle = np.stack([eas[k] for k in keys])
+    am = np.unravel_index(np.argmax(allabs), allabs.shape)
+    gamax = allabs[am]
+    if gamax == 0:
+        return extra
+    g = float(np.float32(np.float32(gamax) / np.float32(448.0 * 6.0)))
+    rel_g = alle[am] / gamax + 2.0 ** -22
+    six_g = float(np.float32(np.float32(6.0) * np.float32(g)))
+    for (t, j) in res["y"].keys():
+        a32 = res["a"][(t, j)].astype(np.float32).astype(np.float64)
+        ea = eas[(t, j)]
+        e = int(ids[t, j])
+        wd = None
+        for b0 in range(0, a32.shape[0], 16):
+            blk = np.abs(a32[b0:b0 + 16])
+            amax_b = np.max(blk)
+            if amax_b == 0:
+                continue
+            if wd is None:
+                wd = np.abs(bank_dn.dequant(e))
+            xb = amax_b / six_g
+            rel_b = ea[b0 + np.argmax(blk)] / amax_b + rel_g + 2.0 ** -21
+            kb = np.clip(np.searchsorted(mids4, xb), 1, len(mids4) - 1)
+            db = min(abs(xb - mids4[kb - 1]), abs(xb - mids4[kb]))
+            code = int(F.encode_e4m3(np.float32(xb)))
+            if db <= rel_b * xb:
+                c2 = [c for c in (code - 1, code + 1) if 0 <= c < 0x7F]
+                effs = F.E4M3_VALUES[code] * g + max(F.E4M3_VALUES[c] for c in c2) * g
+                extra[t] += abs(w[t, j]) * effs * wd[:, b0:b0 + 16].sum(axis=1)
+                continue
+            eff = float(np.float32(np.float32(F.E4M3_VALUES[code]) * np.float32(g)))
+            if eff == 0:
+                continue
+            v = blk / eff
+            ev = ea[b0:b0 + 16] / eff + v * (rel_g + 2.0 ** -21)
+            k2 = np.clip(np.searchsorted(mids2, v), 1, len(mids2) - 1)
+            d = np.minimum(np.abs(v - mids2[k2 - 1]), np.abs(v - mids2[k2]))
+            near = np.where(np.abs(v - mids2[k2 - 1]) <= np.abs(v - mids2[k2]), k2 - 1, k2)
+            amb = np.nonzero(d <= ev)[0]
+            if amb.size == 0:
+                continue
+            step = (e2[near[amb] + 1] - e2[near[amb]]) * eff
+            extra[t] += abs(w[t, j]) * (wd[:, b0 + amb] @ step)
+    return extra
+
+
 class Problem:
     """A seeded MoE FFN problem: activations, routes, weights, GPU bank, oracle bank."""
 
     _bank_cache = {}
 
-    def __init__(self, T, H, I, E, topk, seed, device="cuda", active=None, ids=None):
+    def __init__(self, T, H, I, E, topk, seed, device="cuda", active=None, ids=None, fmt="fp8"):
         import block_quantized_moe_gb300 as ft
         self.T, self.H, self.I, self.E, self.topk, self.seed, self.dev = T, H, I, E, topk, seed, device
+        self.fmt = fmt
+        self.ft_fmt = ft.FMT_FP8 if fmt == "fp8" else ft.FMT_NVFP4
         self.x = synth.activations_bf16(T, H, seed, device)
         if ids is None:
             ids = synth.routes(T, topk, E, seed, active_per_token=active, device=device)
         self.ids = ids.to(device)
         self.w = synth.routing_weights(T, topk, seed, device)
-        key = (H, I, E, seed, device)
+        key = (H, I, E, seed, device, fmt)
+        if key not in Problem._bank_cache and fmt == "nvfp4":
+            parts = []
+            for n, k, raw in ((2 * I, H, self.raw_gateup), (H, I, self.raw_down)):
+                q = torch.empty(E, n, k // 2, dtype=torch.uint8, device=device)
+                sf = torch.empty(E, n, k // 16, dtype=torch.uint8, device=device)
+                gs = torch.empty(E, dtype=torch.float32, device=device)
+                for e in range(E):
+                    ft.ftmoe_quantize_weights(raw(e)[None], q[e:e + 1], sf[e:e + 1], gs[e:e + 1],
+                                              fmt=ft.FMT_NVFP4)
+                parts.append((q, sf, gs))
+            obg = M.LazyBank(lambda e: self.raw_gateup(e).cpu().numpy(), 2 * I, "nvfp4")
+            obd = M.LazyBank(lambda e: self.raw_down(e).cpu().numpy(), H, "nvfp4")
+            Problem._bank_cache[key] = (parts[0], parts[1], obg, obd)
+        if fmt == "nvfp4":
+            (gq, gs, gg), (dq, ds, dg), self.obank_gu, self.obank_dn = Problem._bank_cache[key]
+            self.bank_gu = ft.make_bank(gq, gs, gg, fmt=ft.FMT_NVFP4)
+            self.bank_dn = ft.make_bank(dq, ds, dg, fmt=ft.FMT_NVFP4)
+            self._keep = (gq, gs, gg, dq, ds, dg)
+            return
         if key not in Problem._bank_cache:
             gq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
             gs = torch.empty(E, -(-2 * I // 128), -(-H // 128), dtype=torch.float32, device=device)
@@ -136,7 +247,7 @@ class Problem:
         weights = self.w if weights is None else weights
         x = self.x if x is None else x
         return M.moe_forward(x.float().cpu().numpy(), ids.cpu().numpy(), weights.cpu().numpy(),
-                             self.obank_gu, self.obank_dn, tokens_subset=tokens_subset)
+                             self.obank_gu, self.obank_dn, fmt=self.fmt, tokens_subset=tokens_subset)
 
     def check(self, out, ids=None, weights=None, x=None, tokens_subset=None):
         """Compare a GPU output with the oracle: the stated tolerance plus the bound for
@@ -146,7 +257,8 @@ class Problem:
         res = self.oracle(ids=ids, weights=weights, x=x, tokens_subset=tokens_subset)
         ref = res["out"]
         wv = torch.where(ids >= 0, weights, torch.zeros_like(weights)).cpu().numpy()
-        extra = requant_flip_bound(res, ids.cpu().numpy(), wv, self.obank_gu, self.obank_dn)
+        bound = requant_flip_bound if self.fmt == "fp8" else nvfp4_requant_flip_bound
+        extra = bound(res, ids.cpu().numpy(), wv, self.obank_gu, self.obank_dn)
         got = out.float().cpu().numpy()
         rows = list(range(self.T)) if tokens_subset is None else list(tokens_subset)
         assert_within_tolerance(got[rows], ref[rows], extra=extra[rows])
@@ -157,7 +269,8 @@ class Problem:
         ids = self.ids if ids is None else ids
         weights = self.w if weights is None else weights
         x = self.x if x is None else x
-        shape = ft.moe_shape(self.T, self.H, self.I, self.topk, self.E, tok_tile=tok_tile, path=path)
+        shape = ft.moe_shape(self.T, self.H, self.I, self.topk, self.E, fmt=self.ft_fmt, tok_tile=tok_tile,
+                             path=path)
         if ws is None:
             ws = torch.empty(ft.ftmoe_forward_workspace_bytes(shape), dtype=torch.uint8, device=self.dev)
         if out is None:
