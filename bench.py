@@ -57,8 +57,34 @@ WORKLOADS = {
     # a 32-expert bank with the same rows per expert (96) as the 24,576-route case: small
     # enough (1.4 GB of weights) for multi-pass profiler captures
     "prefill-fp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
+    # NVFP4 weights and activations (e2m1, one e4m3 scale per 16 elements, fp32 tensor
+    # scales) on the same prefill geometry
+    "prefill-nvfp4-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
+    "prefill-nvfp4-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
+    "prefill-nvfp4-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
 }
 DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
+
+
+def workload_format(name):
+    return "nvfp4" if "-nvfp4-" in name else "fp8"
+
+
+def code_bytes(fmt, n):
+    """Bytes of one quantized row of n elements."""
+    return n if fmt == "fp8" else n // 2
+
+
+def scale_bytes(fmt, n):
+    """Bytes of the scales of one quantized activation row of n elements."""
+    return 4 * (-(-n // 128)) if fmt == "fp8" else n // 16
+
+
+def weight_bytes(fmt, n, k):
+    """Bytes of one expert matrix [n, k] with its scales."""
+    if fmt == "fp8":
+        return n * k + 4 * (-(-n // 128)) * (-(-k // 128))
+    return n * k // 2 + n * k // 16 + 4
 
 
 def recorded_traffic(workload):
@@ -192,17 +218,26 @@ class MoeWorkload:
             self.path = path
         if T >= 256:
             self.NSETS = 2
-        gq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
-        gs = torch.empty(E, -(-2 * I // 128), -(-H // 128), dtype=torch.float32, device=device)
-        dq = torch.empty(E, H, I, dtype=torch.uint8, device=device)
-        ds = torch.empty(E, -(-H // 128), -(-I // 128), dtype=torch.float32, device=device)
-        for e in range(E):
-            ft.ftmoe_quantize_weights(synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", device)[None],
-                                      gq[e:e + 1], gs[e:e + 1])
-            ft.ftmoe_quantize_weights(synth.expert_weight_fp32(H, I, seed, e, "down", device)[None],
-                                      dq[e:e + 1], ds[e:e + 1])
-        self.gq, self.gs, self.dq, self.ds = gq, gs, dq, ds
-        self.bank_gu, self.bank_dn = ft.make_bank(gq, gs), ft.make_bank(dq, ds)
+        self.fmt = workload_format(name)
+        self.ft_fmt = ft.FMT_FP8 if self.fmt == "fp8" else ft.FMT_NVFP4
+        banks = []
+        for n, kk, tag in ((2 * I, H, "gateup"), (H, I, "down")):
+            if self.fmt == "fp8":
+                q = torch.empty(E, n, kk, dtype=torch.uint8, device=device)
+                sc = torch.empty(E, -(-n // 128), -(-kk // 128), dtype=torch.float32, device=device)
+                gsc = None
+            else:
+                q = torch.empty(E, n, kk // 2, dtype=torch.uint8, device=device)
+                sc = torch.empty(E, n, kk // 16, dtype=torch.uint8, device=device)
+                gsc = torch.empty(E, dtype=torch.float32, device=device)
+            for e in range(E):
+                ft.ftmoe_quantize_weights(synth.expert_weight_fp32(n, kk, seed, e, tag, device)[None],
+                                          q[e:e + 1], sc[e:e + 1], None if gsc is None else gsc[e:e + 1],
+                                          fmt=self.ft_fmt)
+            banks.append((q, sc, gsc))
+        self._banks = banks
+        self.bank_gu = ft.make_bank(*banks[0], fmt=self.ft_fmt)
+        self.bank_dn = ft.make_bank(*banks[1], fmt=self.ft_fmt)
         self.sets = []
         for i in range(self.NSETS):
             s = seed + 17 * (i + 1)
@@ -210,13 +245,15 @@ class MoeWorkload:
                    synth.routes(T, k, E, s, active_per_token=active, device=device))
             self.sets.append((synth.activations_bf16(T, H, s, device), ids,
                               synth.routing_weights(T, k, s, device)))
-        self.shape = ft.moe_shape(T, H, I, k, E, path=path)
+        self.shape = ft.moe_shape(T, H, I, k, E, fmt=self.ft_fmt, path=path)
         self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
         self.x_in = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
         self.w_in = torch.empty(T, k, dtype=torch.float32, device=device)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
-        self.launches_per_step = 5 if path == 1 else 7
+        # kernels per forward: quantize, [segment, gather,] gate/up, SiLU-and-mul, down, combine;
+        # each NVFP4 quantizer adds an amax pass and the tensor-scale conversion
+        self.launches_per_step = (5 if path == 1 else 7) + (4 if self.fmt == "nvfp4" else 0)
 
     # algorithmic bytes/flops of one forward on route set i
     def work(self, i):
@@ -226,19 +263,22 @@ class MoeWorkload:
         uniq = len(set(int(e) for e in ids.reshape(-1) if e >= 0))
         ra = int((ids >= 0).sum())
         R = T * k
-        sc = lambda n: 4 * (-(-n // 128))  # noqa: E731 - fp32 scale bytes of an n-wide row
-        w_gu = 2 * I * H + 4 * (-(-2 * I // 128)) * (-(-H // 128))
-        w_dn = H * I + 4 * (-(-H // 128)) * (-(-I // 128))
+        f = self.fmt
+        row = lambda n: code_bytes(f, n) + scale_bytes(f, n)  # noqa: E731 - one quantized row
+        w_gu = weight_bytes(f, 2 * I, H)
+        w_dn = weight_bytes(f, H, I)
         out_rows = R if self.path == 1 else ra   # the route-slot path also writes zero rows
-        gateup = uniq * w_gu + (T if self.path == 1 else ra) * (H + sc(H)) + out_rows * 2 * I * 4
-        down = uniq * w_dn + out_rows * (I + sc(I)) + out_rows * H * 4
-        total = (T * H * 2 + T * (H + sc(H))                       # quantize
+        gateup = uniq * w_gu + (T if self.path == 1 else ra) * row(H) + out_rows * 2 * I * 4
+        down = uniq * w_dn + out_rows * row(I) + out_rows * H * 4
+        total = (T * H * 2 + T * row(H)                            # quantize
                  + gateup
-                 + out_rows * 2 * I * 4 + out_rows * (I + sc(I))     # silu_mul
+                 + out_rows * 2 * I * 4 + out_rows * row(I)        # silu_mul
                  + down
-                 + ra * H * 4 + T * k * 8 + T * H * 2)               # combine
+                 + ra * H * 4 + T * k * 8 + T * H * 2)             # combine
+        if f == "nvfp4":
+            total += T * H * 2 + out_rows * 2 * I * 4              # amax passes of the tensor scales
         if self.path == 2:
-            total += T * k * 4 * 3 + ra * (H + sc(H)) * 2           # segment + gather
+            total += T * k * 4 * 3 + ra * row(H) * 2               # segment + gather
         flops = 2 * ra * (2 * I * H + H * I)
         return dict(bytes=total, gateup_bytes=gateup, flops=flops, gateup_flops=2 * ra * 2 * I * H,
                     uniq=uniq, active=ra)
@@ -266,13 +306,20 @@ class MoeWorkload:
             return "stream_gemm_kernel (gate/up, route slots)", lambda: ft.ftmoe_grouped_gemm_gateup(
                 act, routes, self.bank_gu, gu, variant=1)
         R = T * k
-        rq = self.ws[lay["rows_q"]:lay["rows_q"] + R * H].view(R, H)
-        rs = self.ws[lay["rows_scales"]:lay["rows_scales"] + R * (-(-H // 128)) * 4].view(torch.float32).view(R, -1)
+        f = self.fmt
+        rq = self.ws[lay["rows_q"]:lay["rows_q"] + R * code_bytes(f, H)].view(R, -1)
+        rs = self.ws[lay["rows_scales"]:lay["rows_scales"] + R * scale_bytes(f, H)]
+        rs = rs.view(torch.float32).view(R, -1) if f == "fp8" else rs.view(R, -1)
         off = self.ws[lay["offsets"]:lay["offsets"] + (self.E + 1) * 4].view(torch.int32)
-        act, routes = ft.make_act(rq, rs), ft.grouped_routes(off)
         tile = ft.ftmoe_pick_tile(R, self.E)
-        return f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)", lambda: ft.ftmoe_grouped_gemm_gateup(
-            act, routes, self.bank_gu, gu, tok_tile=tile, variant=2)
+        if f == "fp8":
+            act, kname = ft.make_act(rq, rs), f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)"
+        else:
+            xg = self.ws[lay["x_gscale"]:lay["x_gscale"] + 4].view(torch.float32)
+            act = ft.make_act(rq, rs, xg, fmt=ft.FMT_NVFP4)
+            kname = f"nvfp4_gemm_kernel<{tile}> (gate/up, grouped, tcgen05 block-scaled)"
+        routes = ft.grouped_routes(off)
+        return kname, lambda: ft.ftmoe_grouped_gemm_gateup(act, routes, self.bank_gu, gu, tok_tile=tile, variant=2)
 
 
 def time_events(fn, prep, steps, stream):
@@ -349,7 +396,9 @@ def run_gpu(args, rank, world, local):
     gu_bytes_avg = float(np.mean([w["gateup_bytes"] for w in works]))
     gu_flops_avg = float(np.mean([w["gateup_flops"] for w in works]))
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
-    fp8_peak = 2.0 * bf16_peak  # dense FP8 = 2x bf16 (nominal ratio 4.5 / 2.25)
+    # dense FP8 = 2x bf16 and dense FP4 = 6x bf16 (nominal ratios 4.5 / 2.25 and 13.5 / 2.25)
+    mma_peak = (2.0 if wl.fmt == "fp8" else 6.0) * bf16_peak
+    mma_name = "fp8" if wl.fmt == "fp8" else "fp4"
 
     # dominant kernel alone (gate/up GEMM), captured once in a graph so that host-side
     # launch preparation stays out of the timed region; events on the launching stream
@@ -411,7 +460,8 @@ def run_gpu(args, rank, world, local):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8-e4m3 (fp32 accumulate)",
+        "dtype": ("fp8-e4m3 (fp32 accumulate)" if wl.fmt == "fp8" else
+                  "nvfp4-e2m1 with e4m3 block scales (fp32 accumulate)"),
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
@@ -421,14 +471,15 @@ def run_gpu(args, rank, world, local):
         "us_per_call_per_gpu": round(us_per_call_rank, 3),
         "hbm_gbs": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9, 1),
         "hbm_frac_of_peak": round(bytes_avg / (us_per_call_rank * 1e-6) / 1e9 / hbm_peak, 4),
-        "fp8_tflops": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12, 3),
-        "fp8_frac_of_dense_peak": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12 / fp8_peak, 5),
+        f"{mma_name}_tflops": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12, 3),
+        f"{mma_name}_frac_of_dense_peak": round(flops_avg / (us_per_call_rank * 1e-6) / 1e12 / mma_peak, 5),
         "algorithmic_bytes_per_call": int(bytes_avg),
         "roofline": {"kernel": kname, "bound": "hbm",
                      "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(k_gbs / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
                      "launch_us": round(k_us, 3), "algorithmic_bytes_per_launch": int(gu_bytes_avg),
-                     "fp8_tflops": round(k_tflops, 2), "fp8_frac_of_dense_peak": round(k_tflops / fp8_peak, 4),
+                     f"{mma_name}_tflops": round(k_tflops, 2),
+                     f"{mma_name}_frac_of_dense_peak": round(k_tflops / mma_peak, 4),
                      "peak_source": peak_src},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -448,31 +499,42 @@ def run_gpu(args, rank, world, local):
 def _oracle_problem(name, seed=0xF7E00002, max_tokens=None):
     from oracle import moe as M
     T, H, I, E, k, active, _ = WORKLOADS[name]
+    fmt = workload_format(name)
     x = synth.activations_bf16(T, H, seed + 17, "cpu")
     ids = (synth.routes_fast(T, k, E, seed + 17, "cpu") if active == k and T * k > 256 else
            synth.routes(T, k, E, seed + 17, active_per_token=active, device="cpu"))
     w = synth.routing_weights(T, k, seed + 17, "cpu")
-    if max_tokens is not None:  # per-token FP8 quantization: a token subset is exact
+    if max_tokens is not None:  # the first tokens of the call
         ids, x, w = ids[:max_tokens], x[:max_tokens], w[:max_tokens]
     used = sorted(set(int(e) for e in ids.reshape(-1).tolist() if e >= 0))
-    bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I)
-    bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H)
+    bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
+    bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
     for e in used:  # the quantized bank is an input; build it before timing
         bg.parts(e)
         bd.parts(e)
-    return M, x.float().numpy(), ids.numpy(), w.numpy(), bg, bd, T
+    return M, x.float().numpy(), ids.numpy(), w.numpy(), bg, bd, T, fmt
+
+
+def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
+    """The oracle's forward for token t alone. FP8 quantizes per token, so one token of the
+    call is exact; the NVFP4 tensor scales span the whole call, so there the token is run
+    as a call of its own (the same work per token)."""
+    if fmt == "fp8":
+        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[t])
+    else:
+        M.moe_forward(x[t:t + 1], ids[t:t + 1], w[t:t + 1], bg, bd, fmt="nvfp4")
 
 
 def cpu_baseline(name, budget_s=20.0, repeats=None):
     """Time the oracle's forward on a bounded sample of tokens; scale to one full call."""
     T_full = WORKLOADS[name][0]
-    M, x, ids, w, bg, bd, T = _oracle_problem(name, max_tokens=min(T_full, 4))
+    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(name, max_tokens=min(T_full, 4))
     T = T_full
     t0 = time.perf_counter()
     done = 0
     toks = []
     while done < ids.shape[0] and (time.perf_counter() - t0) < budget_s:
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[done])
+        _oracle_token(M, x, ids, w, bg, bd, fmt, done)
         toks.append(done)
         done += 1
     el = time.perf_counter() - t0
@@ -486,14 +548,14 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     T_full = WORKLOADS[args.workload][0]
-    M, x, ids, w, bg, bd, T = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
+    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
     T = T_full
     ns = ids.shape[0]
     for i in range(args.warmup):
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % ns])
+        _oracle_token(M, x, ids, w, bg, bd, fmt, i % ns)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[i % ns])
+        _oracle_token(M, x, ids, w, bg, bd, fmt, i % ns)
     el = time.perf_counter() - t0
     us = el / args.steps * T * 1e6
     return {"impl": "reference", "metric": "MoE FFN us/call", "value": round(us, 1), "unit": "us/call",

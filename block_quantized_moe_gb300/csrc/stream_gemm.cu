@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kThreads) stream_gemm_kernel(const __grid_cons
   if (warp == 0) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();  // the weight stream is read once
       uint32_t it = 0;
       bool ok = true;
       for (int i = i_begin; i < i_end && ok && !s_abort; ++i) {
@@ -216,7 +217,10 @@ __global__ void __launch_bounds__(kThreads) stream_gemm_kernel(const __grid_cons
             if (!mbar_wait(smem_u32(&empty[s]), ((it / kStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
             const uint32_t fb = smem_u32(&full[s]);
             mbar_expect_tx(fb, kTile);
-            tma_load_3d(smem_u32(ring + s * kTile), &map_w, fb, kb * kGroup, n0, itm.e);
+            if (passes == 1)
+              tma_load_3d_hint(smem_u32(ring + s * kTile), &map_w, fb, kb * kGroup, n0, itm.e, pol_w);
+            else  // the tile is read again by the next pass
+              tma_load_3d(smem_u32(ring + s * kTile), &map_w, fb, kb * kGroup, n0, itm.e);
           }
         }
       }

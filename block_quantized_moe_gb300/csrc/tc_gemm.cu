@@ -177,6 +177,9 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   if (warp == 0) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
+      // weight blocks are read once; the activation tile is read again by every weight
+      // block of the expert
+      const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       uint32_t it = 0;
       for (int u = u_begin; u < u_end && !s_abort; ++u) {
         int e, nb, tt, row0, rows;
@@ -189,8 +192,8 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
           uint8_t* ta = tw + Smem<TT>::kTileW;
           const uint32_t fb = smem_u32(&full[st]);
           mbar_expect_tx(fb, Smem<TT>::kStage);
-          tma_load_3d(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e);
-          tma_load_2d(smem_u32(ta), &map_a, fb, kb * kBK, row0);
+          tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
+          tma_load_2d_hint(smem_u32(ta), &map_a, fb, kb * kBK, row0, pol_a);
         }
       }
       // loads still in flight complete on their full barrier: wait for the last phase

@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
+      // weight tiles are read once; the token tile is read again by every weight block
+      const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       uint32_t it = 0;
       for (int u = u_begin; u < u_end && !s_abort; ++u) {
         int e, nb, row0, rows;
@@ -182,10 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* t0 = tiles + (size_t)st * Sz<TT>::kStage;
           const uint32_t fb = smem_u32(&full[st]);
           mbar_expect_tx(fb, Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW + Sz<TT>::kSA);
-          tma_load_3d(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e);
-          tma_load_2d(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0);
-          tma_load_3d(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e);
-          tma_load_2d(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0);
+          tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
+          tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0, pol_a);
+          tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
+          tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0,
+                           pol_a);
         }
       }
       const uint32_t issued = it;
