@@ -152,26 +152,84 @@ def max_over_ranks(v, world, device):
 # ------------------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons during the timed region.
 
-    def __init__(self, gpu_index):
+    Sampled about every millisecond from a thread through NVML (libnvidia-ml via ctypes,
+    read-only queries), so that even a region of a few milliseconds gets samples; falls
+    back to `nvidia-smi -lms 50` when NVML cannot be loaded."""
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import ctypes
+        self.ct = ctypes
+        self.device = device
+        self.samples = []
+        self.thread = None
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
-        self.gpu = gpu_index
+        self.nv = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            pr = torch.cuda.get_device_properties(device)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + bus)
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # 1 = SM clock
+                raise OSError("max clock query failed")
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            if self.reasons_fn is None:
+                self.reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.max_mhz = nv, h, float(mx.value)
+        except (OSError, AttributeError):
+            self.nv = None
+
+    @classmethod
+    def summarize(cls, samples, max_mhz):
+        """(sm MHz, reason bit mask) samples -> the bench line's clocks object."""
+        if not samples:
+            return None
+        reasons = sorted({name for _, r in samples for bit, name in cls.REASON_BITS.items() if r & bit})
+        return {"sm_mhz": float(np.median([c for c, _ in samples])), "sm_max_mhz": max_mhz,
+                "reasons": reasons, "samples": len(samples), "source": "nvml"}
+
+    def _poll(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag:
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(self.h, ct.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.001)
 
     def start(self):
+        if self.nv is not None:
+            import threading
+            self.stop_flag = False
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{self.device.index or 0}.csv")
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device.index or 0),
+                                          f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            return self.summarize(self.samples, self.max_mhz)
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -197,7 +255,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 # ------------------------------------------------------------------------------------
@@ -375,7 +433,7 @@ def run_gpu(args, rank, world, local):
         run_step()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()

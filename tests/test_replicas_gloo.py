@@ -47,3 +47,12 @@ def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
     bench.barrier(1)
     assert not dist.is_initialized() or torch.distributed.get_world_size() >= 1
+
+
+def test_clock_summary_names_throttle_reasons():
+    import bench
+    # bits: 0x1 idle (not reported), 0x4 sw power cap, 0x40 hw thermal slowdown
+    got = bench.ClockSampler.summarize([(2070.0, 0x0), (1980.0, 0x4), (2070.0, 0x41)], 2070.0)
+    assert got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0 and got["samples"] == 3
+    assert got["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler.summarize([], 2070.0) is None
