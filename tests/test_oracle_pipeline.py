@@ -326,6 +326,72 @@ def test_forward_matches_per_element_brute_force():
     assert np.allclose(got, ref, rtol=1e-9, atol=1e-12 * scale)
 
 
+def _dense_ffn_brute_nvfp4(x, ids, wts, bank_gu, bank_dn):
+    """The NVFP4 FFN in per-element loops, in two passes: every active route's SiLU-and-mul
+    row first (its tensor scale is taken over all of them), then the down projection."""
+    T, H = x.shape
+    k = ids.shape[1]
+    I2 = bank_gu.q.shape[1]
+    I = I2 // 2
+
+    def w_val(bank, e, n, c):
+        return F.E2M1_VALUES[bank.q[e][n, c]] * F.E4M3_VALUES[bank.s[e][n, c // 16]] * float(bank.g[e])
+
+    xq, xsb, xg = M.quantize_nvfp4(x)
+    acts = {}
+    for t in range(T):
+        xrow = [F.E2M1_VALUES[xq[t, c]] * F.E4M3_VALUES[xsb[t, c // 16]] * float(xg) for c in range(H)]
+        for j in range(k):
+            e = int(ids[t, j])
+            if e < 0:
+                continue
+            gu = [math.fsum(w_val(bank_gu, e, n, c) * xrow[c] for c in range(H)) for n in range(I2)]
+            acts[(t, j)] = [gu[i] / (1.0 + math.exp(-gu[i])) * gu[I + i] for i in range(I)]
+    out = np.zeros((T, H))
+    if not acts:
+        return out
+    amax = max(abs(np.float32(v)) for row in acts.values() for v in row)
+    for (t, j), act in acts.items():
+        e = int(ids[t, j])
+        aq, asb, ag = M.quantize_nvfp4(np.array([act], np.float32), amax)
+        arow = [F.E2M1_VALUES[aq[0, c]] * F.E4M3_VALUES[asb[0, c // 16]] * float(ag) for c in range(I)]
+        for h in range(H):
+            y = math.fsum(w_val(bank_dn, e, h, c) * arow[c] for c in range(I))
+            out[t, h] += float(wts[t, j]) * y
+    return out
+
+
+def test_nvfp4_forward_matches_per_element_brute_force():
+    x, ids, wts, _, _ = _tiny_problem(21)
+    rng = np.random.default_rng(21)
+    wg = (rng.standard_normal((4, 256, 256)) * 0.02).astype(np.float32)
+    wd = (rng.standard_normal((4, 256, 128)) * 0.02).astype(np.float32)
+    bg, bd = M.quantize_bank(wg, "nvfp4"), M.quantize_bank(wd, "nvfp4")
+    ids[2, 1] = -1
+    ref = _dense_ffn_brute_nvfp4(x, ids, wts, bg, bd)
+    got = M.moe_forward(x, ids, wts, bg, bd, fmt="nvfp4")["out"]
+    assert np.allclose(got, ref, rtol=1e-9, atol=1e-12 * np.max(np.abs(ref)))
+
+
+def test_nvfp4_token_subset_keeps_the_call_wide_tensor_scales():
+    # a subset evaluates fewer tokens but quantizes with the whole call's amaxes, so its
+    # rows are the full call's rows
+    x, ids, wts, _, _ = _tiny_problem(22, T=5)
+    rng = np.random.default_rng(22)
+    bg = M.quantize_bank((rng.standard_normal((4, 256, 256)) * 0.02).astype(np.float32), "nvfp4")
+    bd = M.quantize_bank((rng.standard_normal((4, 256, 128)) * 0.02).astype(np.float32), "nvfp4")
+    x[4] *= 8.0  # the largest activation and intermediate sit in a token left out below
+    full = M.moe_forward(x, ids, wts, bg, bd, fmt="nvfp4")["out"]
+    sub = M.moe_forward(x, ids, wts, bg, bd, fmt="nvfp4", tokens_subset=[0, 2])["out"]
+    scale = np.max(np.abs(full))
+    # BLAS may order the down GEMM's sums differently for fewer stacked rows
+    assert np.allclose(sub[[0, 2]], full[[0, 2]], rtol=1e-12, atol=1e-15 * scale)
+    assert not np.any(sub[[1, 3, 4]])
+    alone = M.moe_forward(x[:1], ids[:1], wts[:1], bg, bd, fmt="nvfp4")["out"]
+    # a call of its own has its own tensor scales: a quantization-level difference
+    assert np.max(np.abs(alone[0] - full[0])) > 1e-4 * scale
+
+
 def test_grouped_rows_equal_per_route_rows():
     # segment + gather + per-expert GEMM over grouped rows == per-route GEMM on token rows
     x, ids, wts, bg, bd = _tiny_problem(13, T=9, E=5, k=3)
