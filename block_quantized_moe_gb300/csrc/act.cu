@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
     const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
     const int32_t* __restrict__ rows_dev, uint8_t* __restrict__ q, float* __restrict__ s,
     int64_t ng) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   int64_t limit = rows;
   if (rows_dev != nullptr) {
     const int64_t d = *rows_dev;
@@ -77,11 +79,8 @@ cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, in
   const bool vec = (ld_gu % 4 == 0) && (inter % 4 == 0) && ((uintptr_t)gu % 16 == 0) &&
                    ((uintptr_t)q % 4 == 0);
   const int grid = grid_cap(cdiv(rows * ng, 8));
-  if (vec)
-    silu_mul_fp8_kernel<true><<<grid, 256, 0, st>>>(gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
-  else
-    silu_mul_fp8_kernel<false><<<grid, 256, 0, st>>>(gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
-  return cudaGetLastError();
+  return launch_kernel(vec ? silu_mul_fp8_kernel<true> : silu_mul_fp8_kernel<false>, dim3(grid), dim3(256), 0, st,
+                       true, gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
 }
 
 // ---- NVFP4: pass 1 amax of a over the valid rows, pass 2 quantize, pass 3 amax -> g ----
@@ -89,6 +88,8 @@ __global__ void __launch_bounds__(256) silu_amax_kernel(const float* __restrict_
                                                         int64_t inter, int64_t ld,
                                                         const int32_t* __restrict__ rows_dev,
                                                         float* __restrict__ amax_out) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   int64_t limit = rows;
   if (rows_dev != nullptr) {
     const int64_t d = *rows_dev;
@@ -115,6 +116,8 @@ __global__ void __launch_bounds__(256) silu_quant_nvfp4_kernel(
     const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
     const int32_t* __restrict__ rows_dev, const float* __restrict__ amax_in,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sb) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   int64_t limit = rows;
   if (rows_dev != nullptr) {
     const int64_t d = *rows_dev;
@@ -152,19 +155,25 @@ __global__ void __launch_bounds__(256) silu_quant_nvfp4_kernel(
   }
 }
 
-__global__ void amax_to_gscale_1(float* g) { g[0] = div_rn(g[0], kE4M3Max * kE2M1Max); }
+__global__ void amax_to_gscale_1(float* g) {
+  pdl_wait();
+  pdl_trigger();
+  g[0] = div_rn(g[0], kE4M3Max * kE2M1Max);
+}
 
 cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
                                   const int32_t* rows_dev, uint8_t* q, uint8_t* scales,
                                   float* gscale, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(gscale, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
-  silu_amax_kernel<<<grid_cap(cdiv(rows * inter, 256 * 8)), 256, 0, st>>>(gu, rows, inter, ld_gu,
-                                                                           rows_dev, gscale);
-  silu_quant_nvfp4_kernel<<<grid_cap(cdiv(rows * inter / kNvfp4Block, 256)), 256, 0, st>>>(
-      gu, rows, inter, ld_gu, rows_dev, gscale, q, scales);
-  amax_to_gscale_1<<<1, 1, 0, st>>>(gscale);
-  return cudaGetLastError();
+  // the first kernel follows the memset, which takes part in no overlap
+  e = launch_kernel(silu_amax_kernel, dim3(grid_cap(cdiv(rows * inter, 256 * 8))), dim3(256), 0, st, false, gu, rows,
+                    inter, ld_gu, rows_dev, gscale);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(silu_quant_nvfp4_kernel, dim3(grid_cap(cdiv(rows * inter / kNvfp4Block, 256))), dim3(256), 0, st,
+                    true, gu, rows, inter, ld_gu, rows_dev, gscale, q, scales);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(amax_to_gscale_1, dim3(1), dim3(1), 0, st, true, gscale);
 }
 
 // ---- combine: out[t, h] = bf16( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
@@ -175,6 +184,8 @@ __global__ void __launch_bounds__(128) combine_kernel(
     const float* __restrict__ y, int64_t ld_y, const int32_t* __restrict__ route2dst,
     const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t tokens, int32_t topk,
     int64_t hidden, uint16_t* __restrict__ out, int64_t ld_out) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   const int64_t t = blockIdx.y;
   const int64_t h0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (h0 >= hidden) return;
@@ -254,11 +265,8 @@ cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2ds
   const bool vec = (hidden % 4 == 0) && (ld_y % 4 == 0) && ((uintptr_t)y % 16 == 0) &&
                    (ld_out % 4 == 0) && ((uintptr_t)out % 8 == 0);
   dim3 grid((unsigned)cdiv(hidden, 4 * 128), (unsigned)tokens);
-  if (vec)
-    combine_kernel<true><<<grid, 128, 0, st>>>(y, ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
-  else
-    combine_kernel<false><<<grid, 128, 0, st>>>(y, ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
-  return cudaGetLastError();
+  return launch_kernel(vec ? combine_kernel<true> : combine_kernel<false>, grid, dim3(128), 0, st, true, y, ld_y,
+                       route2dst, ids, w, tokens, topk, hidden, out, ld_out);
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_act)

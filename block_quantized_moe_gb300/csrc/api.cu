@@ -8,7 +8,21 @@
 
 using namespace ftmoe;
 
+namespace ftmoe {
+bool& pdl_enabled() {
+  static thread_local bool on = false;
+  return on;
+}
+}  // namespace ftmoe
+
 namespace {
+
+// Lets the forward's kernels after the first start while their predecessor finishes
+// (programmatic dependent launch), and turns that off again on every way out.
+struct OverlapScope {
+  ~OverlapScope() { pdl_enabled() = false; }
+  void enable() { pdl_enabled() = true; }
+};
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline ftmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FTMOE_OK : FTMOE_CUDA_ERROR; }
@@ -382,8 +396,10 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   memset(&tile, 0, sizeof(tile));
   tile.tok_tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, (int32_t)E);
 
+  OverlapScope overlap;
   st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, xg, stream);
   if (st != FTMOE_OK) return st;
+  overlap.enable();
   if (!L.grouped) {
     ftmoe_routes rt;
     memset(&rt, 0, sizeof(rt));

@@ -22,6 +22,14 @@ static __device__ unsigned int g_err_word;
 
 __device__ __forceinline__ void raise_error(unsigned int bit) { atomicOr(&g_err_word, bit); }
 
+// Programmatic dependent launch. Inside the fused forward a kernel may start while its
+// predecessor is still running; it waits here before it reads anything the predecessor
+// writes (or writes anything it reads), and only then lets its own dependent start. So when
+// a kernel starts, every kernel two or more launches earlier has completed. Outside such a
+// launch both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 #define FTMOE_DEFINE_ERR_READER(fname)                                                \
   uint32_t fname() {                                                                  \
     unsigned int v = 0, zero = 0;                                                     \

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(
     int64_t row_bytes, int64_t scale_bytes, const int32_t* __restrict__ map, int64_t n_dst,
     const int32_t* __restrict__ n_dst_dev, uint8_t* __restrict__ dst, uint8_t* __restrict__ dst_s,
     int64_t tile_bytes, int scale_mode /*0 bytes, 1 words, 2 vec16*/) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   int64_t limit = n_dst;
   if (n_dst_dev != nullptr) {
     const int64_t d = *n_dst_dev;
@@ -82,15 +84,9 @@ cudaError_t launch_gather(const uint8_t* src, const uint8_t* src_scales, int64_t
   if (tiles < 1) tiles = 1;
   const int64_t rows_grid = n_dst < 65535 ? n_dst : 65535;
   dim3 grid((unsigned)tiles, (unsigned)(rows_grid > 0 ? rows_grid : 1));
-  if (vec)
-    gather_kernel<true><<<grid, kGatherThreads, 0, st>>>(src, src_scales, n_src, row_bytes,
-                                                         scale_bytes, dst2src, n_dst, n_dst_dev,
-                                                         dst, dst_scales, tile_bytes, scale_mode);
-  else
-    gather_kernel<false><<<grid, kGatherThreads, 0, st>>>(src, src_scales, n_src, row_bytes,
-                                                          scale_bytes, dst2src, n_dst, n_dst_dev,
-                                                          dst, dst_scales, tile_bytes, scale_mode);
-  return cudaGetLastError();
+  return launch_kernel(vec ? gather_kernel<true> : gather_kernel<false>, grid, dim3(kGatherThreads), 0, st, true, src,
+                       src_scales, n_src, row_bytes, scale_bytes, dst2src, n_dst, n_dst_dev, dst, dst_scales,
+                       tile_bytes, scale_mode);
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_gather)

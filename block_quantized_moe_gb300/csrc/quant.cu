@@ -16,6 +16,8 @@ template <bool kVec>
 __global__ void __launch_bounds__(256) quantize_act_fp8_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t k, int64_t ld_x,
     uint8_t* __restrict__ q, float* __restrict__ s, int64_t ng) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows * ng;
@@ -67,11 +69,8 @@ cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, 
   const int64_t ng = cdiv(k, kGroup);
   const bool vec = ((uintptr_t)x % 8 == 0) && (ld_x % 4 == 0) && ((uintptr_t)q % 4 == 0) && (k % 4 == 0);
   const int grid = grid_for(rows * ng, 8);
-  if (vec)
-    quantize_act_fp8_kernel<true><<<grid, 256, 0, st>>>(x, rows, k, ld_x, q, scales, ng);
-  else
-    quantize_act_fp8_kernel<false><<<grid, 256, 0, st>>>(x, rows, k, ld_x, q, scales, ng);
-  return cudaGetLastError();
+  return launch_kernel(vec ? quantize_act_fp8_kernel<true> : quantize_act_fp8_kernel<false>, dim3(grid), dim3(256), 0,
+                       st, true, x, rows, k, ld_x, q, scales, ng);
 }
 
 // ---------------------------------------------------------------------------------
@@ -91,6 +90,8 @@ __global__ void __launch_bounds__(256) tensor_amax_kernel(const T* __restrict__ 
                                                           int64_t k, int64_t ld,
                                                           int64_t matrix_stride,
                                                           float* __restrict__ amax_out) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   // blockIdx.y selects a matrix (experts of a weight bank); one amax word per matrix
   const T* xm = x + (int64_t)blockIdx.y * matrix_stride;
   float m = 0.0f;
@@ -116,6 +117,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
     const T* __restrict__ x, int64_t rows, int64_t k, int64_t ld, int64_t matrix_stride,
     const float* __restrict__ amax_in, uint8_t* __restrict__ q, uint8_t* __restrict__ sb) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   const int64_t nblk = k / kNvfp4Block;
   const int64_t mat = blockIdx.y;
   const T* xm = x + mat * matrix_stride;
@@ -152,6 +155,8 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
 }
 
 __global__ void amax_to_global_scale_kernel(float* g, int n) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) g[i] = div_rn(g[i], kE4M3Max * kE2M1Max);
 }
@@ -161,12 +166,13 @@ cudaError_t launch_quantize_act_nvfp4(const uint16_t* x, int64_t rows, int64_t k
                                       cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(gscale, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
-  tensor_amax_kernel<uint16_t><<<dim3(grid_for(rows * k, 256 * 8), 1), 256, 0, st>>>(
-      x, rows, k, ld_x, 0, gscale);
-  quantize_nvfp4_kernel<uint16_t><<<dim3(grid_for(rows * k / kNvfp4Block, 256), 1), 256, 0, st>>>(
-      x, rows, k, ld_x, 0, gscale, q, scales);
-  amax_to_global_scale_kernel<<<1, 32, 0, st>>>(gscale, 1);
-  return cudaGetLastError();
+  // the first kernel follows the memset, which takes part in no overlap
+  e = launch_kernel(tensor_amax_kernel<uint16_t>, dim3(grid_for(rows * k, 256 * 8), 1), dim3(256), 0, st, false, x,
+                    rows, k, ld_x, 0, gscale);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(quantize_nvfp4_kernel<uint16_t>, dim3(grid_for(rows * k / kNvfp4Block, 256), 1), dim3(256), 0,
+                    st, true, x, rows, k, ld_x, 0, gscale, q, scales);
+  return launch_kernel(amax_to_global_scale_kernel, dim3(1), dim3(32), 0, st, true, gscale, 1);
 }
 
 // ---------------------------------------------------------------------------------

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(
     const int32_t* __restrict__ ids, int64_t routes, int32_t topk, int32_t E,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ dst2src,
     int32_t* __restrict__ route2dst) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   __shared__ int sh[33];
   const int e = blockIdx.x;
   const int64_t per = (routes + blockDim.x - 1) / blockDim.x;
@@ -82,9 +84,8 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(
 cudaError_t launch_segment(const int32_t* ids, int64_t routes, int32_t topk, int32_t E,
                            int32_t* counts, int32_t* offsets, int32_t* dst2src,
                            int32_t* route2dst, cudaStream_t st) {
-  segment_kernel<<<E, kSegThreads, 0, st>>>(ids, routes, topk, E, counts, offsets, dst2src,
-                                            route2dst);
-  return cudaGetLastError();
+  return launch_kernel(segment_kernel, dim3(E), dim3(kSegThreads), 0, st, true, ids, routes, topk, E, counts, offsets,
+                       dst2src, route2dst);
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_segment)

@@ -131,6 +131,8 @@ __device__ __forceinline__ int member_count(const Params& p, const Item& it) {
 }
 
 __global__ void __launch_bounds__(kThreads) stream_gemm_kernel(const __grid_constant__ CUtensorMap map_w, Params p) {
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int kStages = p.stages;
@@ -411,8 +413,7 @@ static cudaError_t launch_part(const StreamGemmArgs& a, const CUtensorMap& map, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) granted[dev] = smem;
   }
-  st::stream_gemm_kernel<<<(unsigned)grid, st::kThreads, smem, stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_kernel(st::stream_gemm_kernel, dim3((unsigned)grid), dim3(st::kThreads), smem, stream, true, map, p);
 }
 
 cudaError_t launch_stream_gemm(const StreamGemmArgs& a, cudaStream_t stream) {

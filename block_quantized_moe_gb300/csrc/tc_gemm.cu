@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       const int e = base + lane;
       int u = 0;
       if (e < E) {
-        int lo = p.offsets[e], hi = p.offsets[e + 1];
+        // the segment offsets come from a kernel two launches back, complete by now (see
+        // pdl_wait); read them from L2
+        int lo = __ldcg(p.offsets + e), hi = __ldcg(p.offsets + e + 1);
         if (lo < 0) lo = 0;
         if (hi > p.a_rows) hi = (int)p.a_rows;
         const int m = hi > lo ? hi - lo : 0;
@@ -149,6 +151,10 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   fence_before();
   __syncthreads();
   fence_after();
+  // everything above overlapped the previous kernel's tail; the token rows and their
+  // scales come from the previous kernel
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
   // a contiguous range of units per CTA; units run (expert, token tile, weight block) with
@@ -476,8 +482,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  tc::tc_gemm_kernel<TT><<<sm_count(), 64 + 32 * tc::kEpiWarps, smem, st>>>(mw, ma, p);
-  return cudaGetLastError();
+  return launch_kernel(tc::tc_gemm_kernel<TT>, dim3(sm_count()), dim3(64 + 32 * tc::kEpiWarps), smem, st, true, mw,
+                       ma, p);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {

@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = base + lane;
       int u = 0;
       if (e < E) {
-        int lo = p.offsets[e], hi = p.offsets[e + 1];
+        // the segment offsets come from a kernel two launches back, complete by now (see
+        // pdl_wait); read them from L2
+        int lo = __ldcg(p.offsets + e), hi = __ldcg(p.offsets + e + 1);
         if (lo < 0) lo = 0;
         if (hi > p.a_rows) hi = (int)p.a_rows;
         const int m = hi > lo ? hi - lo : 0;
@@ -147,6 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
+  // everything above overlapped the previous kernel's tail; the token rows and their
+  // scales come from the previous kernel
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
   const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
@@ -407,8 +413,8 @@ static cudaError_t launch_nv(const NvGemmArgs& a, cudaStream_t st, int* unsuppor
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) granted[dev] = smem;
   }
-  nv::nvfp4_gemm_kernel<TT><<<sm_count(), nv::kThreads, smem, st>>>(mw, ma, msw, msa, p);
-  return cudaGetLastError();
+  return launch_kernel(nv::nvfp4_gemm_kernel<TT>, dim3(sm_count()), dim3(nv::kThreads), smem, st, true, mw, ma, msw,
+                       msa, p);
 }
 
 cudaError_t launch_nvfp4_gemm(const NvGemmArgs& a, cudaStream_t st, int* unsupported) {
