@@ -8,7 +8,8 @@ combine). Other workloads (--workload) are available for measurement runs.
 
 Timing: W warm-up steps, then K timed steps; before every step the inputs of the
 next route set are copied into the graph's input buffers and L2 is flushed (a 512 MiB
-write), both outside the timed events; each step is bracketed by CUDA events on the
+write, then a 256 MiB read that writes the flush's dirty lines back), both outside the
+timed events; each step is bracketed by CUDA events on the
 launching stream; barrier + synchronize on both sides of the timed loop; max over
 ranks. `value` is microseconds per call for the whole job (time / calls of all ranks).
 
@@ -64,6 +65,11 @@ WORKLOADS = {
     "prefill-nvfp4-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
 }
 DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
+
+# The fused FP8 row + scale gather alone: name -> (k, tokens, top-k). Source rows are random
+# FP8 bytes [tokens x k] with fp32 scales U(1e-3, 1) per 128 columns; the map has
+# tokens * top-k entries drawn by randint over [0, tokens) (duplicates expected).
+GATHER_WORKLOADS = {f"gather-k{k}-t{t}": (k, t, 8) for k in (7168, 2048, 896) for t in (1, 8, 64, 1024)}
 
 
 def workload_format(name):
@@ -380,6 +386,45 @@ class MoeWorkload:
         return kname, lambda: ft.ftmoe_grouped_gemm_gateup(act, routes, self.bank_gu, gu, tok_tile=tile, variant=2)
 
 
+class L2Flush:
+    """Replaces L2's contents between timed steps: a 512 MiB write (larger than the 126 MB
+    L2), then a 256 MiB read of another buffer, so that the dirty lines the write leaves are
+    written back before the timed region instead of during the next kernel's misses."""
+    DESC = "flushed before every timed step (512 MiB write, then a 256 MiB read)"
+
+    def __init__(self, device):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+def time_in_graph(fn, prep, steps):
+    """Device time (ms, summed over `steps` replays) of fn between two event nodes recorded
+    inside its own CUDA graph, so the graph's own launch latency is not counted; None
+    when this PyTorch cannot record events inside a graph."""
+    try:
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    total = 0.0
+    for i in range(steps):
+        prep(i)
+        g.replay()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total
+
+
 def time_events(fn, prep, steps, stream):
     """Sum of per-call CUDA-event durations (ms) over `steps` calls; prep() runs outside."""
     total = 0.0
@@ -404,11 +449,11 @@ def run_gpu(args, rank, world, local):
     torch.cuda.set_device(dev)
     wl = MoeWorkload(args.workload, dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def prep(i):
         wl.load_set(i % wl.NSETS)
-        flush.zero_()
+        flush()
 
     # eager warm-up, then capture one graph of the whole forward (--eager: direct launches,
     # e.g. for profilers that replay kernels one by one)
@@ -458,18 +503,23 @@ def run_gpu(args, rank, world, local):
     mma_peak = (2.0 if wl.fmt == "fp8" else 6.0) * bf16_peak
     mma_name = "fp8" if wl.fmt == "fp8" else "fp4"
 
-    # dominant kernel alone (gate/up GEMM), captured once in a graph so that host-side
-    # launch preparation stays out of the timed region; events on the launching stream
+    # dominant kernel alone (gate/up GEMM), captured in a graph so that host-side launch
+    # preparation stays out of the timed region; timed by event nodes inside that graph
+    # (L2 flushed before each replay), else by events around the graph's launch
     kname, kern = wl.dominant_kernel()
     for i in range(3):
         prep(i)
         kern()
     torch.cuda.synchronize()
-    kgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(kgraph):
-        kern()
-    torch.cuda.synchronize()
-    kms = time_events(kgraph.replay, prep, args.steps, stream)
+    kms = time_in_graph(kern, prep, args.steps)
+    k_timing = "event nodes inside the kernel's graph"
+    if kms is None:
+        kgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kgraph):
+            kern()
+        torch.cuda.synchronize()
+        kms = time_events(kgraph.replay, prep, args.steps, stream)
+        k_timing = "events around a one-kernel graph (includes the graph's launch latency)"
     k_us = kms * 1e3 / args.steps
     k_gbs = gu_bytes_avg / (k_us * 1e-6) / 1e9
     k_tflops = gu_flops_avg / (k_us * 1e-6) / 1e12
@@ -497,7 +547,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     e2e_total = 0.0
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step(i)
@@ -523,7 +573,7 @@ def run_gpu(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
-                   "l2": "flushed before every timed step (512 MiB write)", "parallelism": f"replicas x{world}",
+                   "l2": L2Flush.DESC, "parallelism": f"replicas x{world}",
                    "graph": ("direct launches (--eager)" if args.eager else
                              "one CUDA graph replayed; inputs copied in place between steps")},
         "us_per_call_per_gpu": round(us_per_call_rank, 3),
@@ -535,7 +585,8 @@ def run_gpu(args, rank, world, local):
         "roofline": {"kernel": kname, "bound": "hbm",
                      "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(k_gbs / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
-                     "launch_us": round(k_us, 3), "algorithmic_bytes_per_launch": int(gu_bytes_avg),
+                     "launch_us": round(k_us, 3), "timing": k_timing,
+                     "algorithmic_bytes_per_launch": int(gu_bytes_avg),
                      f"{mma_name}_tflops": round(k_tflops, 2),
                      f"{mma_name}_frac_of_dense_peak": round(k_tflops / mma_peak, 4),
                      "peak_source": peak_src},
@@ -547,6 +598,110 @@ def run_gpu(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl.name, budget_s=args.cpu_budget)
+    return result
+
+
+def run_gather(args, rank, world, local):
+    """The gather-alone workload: one ftmoe_gather_rows_scales per step from a CUDA graph,
+    the map of the next set copied in and L2 flushed before every step."""
+    import block_quantized_moe_gb300 as ft
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    k, T, topk = GATHER_WORKLOADS[args.workload]
+    n_dst, ng, nsets = T * topk, -(-k // 128), 8
+    seed = 0xF7E00003
+    src = synth.random_bytes(T, k, seed, "gather-src", dev)
+    sc = synth.uniform_f32(T, ng, 1e-3, 1.0, seed, "gather-scales", dev)
+    maps = [synth.randint_map(n_dst, T, seed + i, "gather-map", dev) for i in range(nsets)]
+    map_in = torch.empty(n_dst, dtype=torch.int32, device=dev)
+    dst = torch.empty(n_dst, k, dtype=torch.uint8, device=dev)
+    dsc = torch.empty(n_dst, ng, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ft.ftmoe_gather_rows_scales(src, sc, map_in, dst, dsc)
+
+    def prep(i):
+        map_in.copy_(maps[i % nsets])
+        flush()
+
+    prep(0)
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        prep(i)
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    ms = time_events(graph.replay, prep, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world, dev)
+    us_rank = ms_max * 1e3 / args.steps
+    value = ms_max * 1e3 / (args.steps * world)
+    kms = time_in_graph(step, prep, args.steps)
+    k_timing = "event nodes inside the kernel's graph"
+    if kms is None:
+        kms, k_timing = ms, "events around the graph's launch"
+    k_us = kms * 1e3 / args.steps
+    row = k + 4 * ng
+    distinct = [len(set(m.cpu().tolist())) for m in maps]
+    bytes_avg = float(np.mean([n_dst * row + d * row + 4 * n_dst for d in
+                               (distinct[i % nsets] for i in range(args.steps))]))
+    hbm_peak, _, _, peak_src = peaks()
+    # end to end: source rows, scales and map from pinned host memory, gathered rows back
+    hsrc = torch.empty(T, k, dtype=torch.uint8, pin_memory=True)
+    hsc = torch.empty(T, ng, dtype=torch.float32, pin_memory=True)
+    hmap = [torch.empty(n_dst, dtype=torch.int32, pin_memory=True) for _ in range(nsets)]
+    hsrc.copy_(src)
+    hsc.copy_(sc)
+    for i in range(nsets):
+        hmap[i].copy_(maps[i])
+    hdst = torch.empty(n_dst, k, dtype=torch.uint8, pin_memory=True)
+    hdsc = torch.empty(n_dst, ng, dtype=torch.float32, pin_memory=True)
+    e2e_total = 0.0
+    for i in range(args.steps + 3):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        src.copy_(hsrc, non_blocking=True)
+        sc.copy_(hsc, non_blocking=True)
+        map_in.copy_(hmap[i % nsets], non_blocking=True)
+        graph.replay()
+        hdst.copy_(dst, non_blocking=True)
+        hdsc.copy_(dsc, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_total += time.perf_counter() - t0
+    e2e_us = max_over_ranks(e2e_total, world, dev) * 1e6 / (args.steps * world)
+    result = {
+        "metric": "gather us/call", "value": round(value, 3), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8 (FP8 bytes) + fp32 scales",
+        "data": "synthetic (seeded random FP8 bytes, U(1e-3, 1) scales, randint maps with duplicates)",
+        "config": {"workload": args.workload, "k": k, "tokens": T, "topk": topk, "rows": n_dst,
+                   "maps_rotated": nsets, "l2": L2Flush.DESC,
+                   "parallelism": f"replicas x{world}", "graph": "one CUDA graph replayed; map copied in between steps"},
+        "hbm_gbs": round(bytes_avg / (us_rank * 1e-6) / 1e9, 1),
+        "algorithmic_bytes_per_call": int(bytes_avg),
+        "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": round(bytes_avg / (k_us * 1e-6) / 1e9, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(bytes_avg / (k_us * 1e-6) / 1e9 / hbm_peak, 4),
+                     "traffic": None, "launch_us": round(k_us, 3), "timing": k_timing, "peak_source": peak_src},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": T * k + T * ng * 4 + n_dst * 4,
+                "d2h_bytes_per_step": n_dst * row},
+        "gpu_launches": args.steps, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_gather(args.workload, budget_s=min(args.cpu_budget, 10.0))
     return result
 
 
@@ -602,9 +757,49 @@ def cpu_baseline(name, budget_s=20.0, repeats=None):
                       f"{el:.1f} s of CPU work, scaled to the full call"}
 
 
+def _gather_oracle_problem(name, seed=0xF7E00003):
+    from oracle import moe as M
+    k, T, topk = GATHER_WORKLOADS[name]
+    src = synth.random_bytes(T, k, seed, "gather-src", "cpu").numpy()
+    sc = synth.uniform_f32(T, -(-k // 128), 1e-3, 1.0, seed, "gather-scales", "cpu").numpy()
+    mp = synth.randint_map(T * topk, T, seed, "gather-map", "cpu").numpy()
+    return M, src, sc, mp
+
+
+def cpu_baseline_gather(name, budget_s=10.0):
+    """The oracle's gather (numpy indexing, single thread) on the whole call, repeated
+    within the budget."""
+    M, src, sc, mp = _gather_oracle_problem(name)
+    t0 = time.perf_counter()
+    n = 0
+    while n < 3 or (time.perf_counter() - t0) < min(budget_s, 1.0):
+        M.gather_rows_scales(src, sc, mp)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(el / n * 1e6, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole calls (numpy, single thread), {el:.2f} s"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    if args.workload in GATHER_WORKLOADS:
+        M, src, sc, mp = _gather_oracle_problem(args.workload)
+        for _ in range(args.warmup):
+            M.gather_rows_scales(src, sc, mp)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            M.gather_rows_scales(src, sc, mp)
+        us = (time.perf_counter() - t0) / args.steps * 1e6
+        return {"impl": "reference", "metric": "gather us/call", "value": round(us, 1), "unit": "us/call",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+                "config": {"workload": args.workload},
+                "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                                 "sample": "whole calls (numpy, single thread)"},
+                "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     T_full = WORKLOADS[args.workload][0]
     M, x, ids, w, bg, bd, T, fmt = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
     T = T_full
@@ -631,7 +826,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ftmoe", choices=["ftmoe", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(GATHER_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the forward directly instead of a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -641,6 +836,8 @@ def main():
     rank, world, local = dist_init()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.workload in GATHER_WORKLOADS:
+        res = run_gather(args, rank, world, local)
     else:
         res = run_gpu(args, rank, world, local)
     if rank == 0 and res is not None:

@@ -72,6 +72,7 @@ struct Params {
 constexpr int kEpiWarps = 16;                    // 4 column groups x 4 TMEM lane quarters
 constexpr int kGroups = kEpiWarps / 4;
 constexpr int kMaxKB = 128;                      // K <= 16384
+constexpr int kMaxStages = 12;
 
 template <int TT>
 struct Smem {
@@ -92,8 +93,10 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   uint8_t* tiles = smem;
   float* sa = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT>::kStage);  // [KB][TT]
   float* swt = sa + (size_t)p.kb_count * TT;                                  // [kGroups][kMaxKB]
-  int* cum = reinterpret_cast<int*>(swt + kGroups * kMaxKB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(cum + kMaxExperts + 2)) + 7) & ~(uintptr_t)7);
+  int* cum = reinterpret_cast<int*>(swt + kGroups * kMaxKB);  // [E+2] unit prefix
+  int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
+  int* seg_hi = seg_lo + p.E;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   constexpr int kAcc = acc_count(TT);
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
         if (hi > p.a_rows) hi = (int)p.a_rows;
         const int m = hi > lo ? hi - lo : 0;
         u = ((m + TT - 1) / TT) * NB;
+        seg_lo[e] = lo;  // kept in shared memory: no global load at unit boundaries
+        seg_hi[e] = hi > lo ? hi : lo;
       }
       int inc = u;
 #pragma unroll
@@ -152,9 +157,13 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   __syncthreads();
   fence_after();
   // everything above overlapped the previous kernel's tail; the token rows and their
-  // scales come from the previous kernel
-  pdl_wait();
-  pdl_trigger();
+  // scales come from the previous kernel (the producer thread waits after it has sent the
+  // first weight tiles, which do not depend on it)
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
   // a contiguous range of units per CTA; units run (expert, token tile, weight block) with
@@ -170,9 +179,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       if (cum[mid] <= u) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    int s0 = p.offsets[e], s1 = p.offsets[e + 1];
-    if (s0 < 0) s0 = 0;
-    if (s1 > p.a_rows) s1 = (int)p.a_rows;
+    const int s0 = seg_lo[e], s1 = seg_hi[e];
     const int local = u - cum[e];
     tt = local / NB;
     nb = local - tt * NB;
@@ -187,20 +194,46 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       // block of the expert
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       uint32_t it = 0;
-      for (int u = u_begin; u < u_end && !s_abort; ++u) {
-        int e, nb, tt, row0, rows;
-        decode(u, e, nb, tt, row0, rows);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
-          uint8_t* tw = tiles + (size_t)st * Smem<TT>::kStage;
-          uint8_t* ta = tw + Smem<TT>::kTileW;
-          const uint32_t fb = smem_u32(&full[st]);
-          mbar_expect_tx(fb, Smem<TT>::kStage);
-          tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
-          tma_load_2d_hint(smem_u32(ta), &map_a, fb, kb * kBK, row0, pol_a);
+      int u = u_begin, kb = 0, e = 0, nb = 0, tt = 0, row0 = 0, rows = 0;
+      if (u < u_end) decode(u, e, nb, tt, row0, rows);
+      auto advance = [&]() {
+        if (++kb == KB) {
+          kb = 0;
+          if (++u < u_end) decode(u, e, nb, tt, row0, rows);
         }
+      };
+      // The weight tiles of the first pass over the ring go out before the wait: they do
+      // not depend on the previous kernel. Their token tiles follow once it is complete.
+      int pre_kb[kMaxStages], pre_row0[kMaxStages];
+      int npre = 0;
+      while (npre < S && u < u_end) {
+        uint8_t* tw = tiles + (size_t)npre * Smem<TT>::kStage;
+        const uint32_t fb = smem_u32(&full[npre]);
+        mbar_expect_tx(fb, Smem<TT>::kStage);
+        tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
+        pre_kb[npre] = kb;
+        pre_row0[npre] = row0;
+        ++npre;
+        ++it;
+        advance();
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d_hint(smem_u32(tiles + (size_t)i * Smem<TT>::kStage + Smem<TT>::kTileW), &map_a,
+                         smem_u32(&full[i]), pre_kb[i] * kBK, pre_row0[i], pol_a);
+      while (u < u_end && !s_abort) {
+        const int st = it % S;
+        const uint32_t ph = (it / S) & 1;
+        if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
+        uint8_t* tw = tiles + (size_t)st * Smem<TT>::kStage;
+        uint8_t* ta = tw + Smem<TT>::kTileW;
+        const uint32_t fb = smem_u32(&full[st]);
+        mbar_expect_tx(fb, Smem<TT>::kStage);
+        tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
+        tma_load_2d_hint(smem_u32(ta), &map_a, fb, kb * kBK, row0, pol_a);
+        ++it;
+        advance();
       }
       // loads still in flight complete on their full barrier: wait for the last phase
       // issued on each stage (a bounded wait; the phase completes once its bytes land)
@@ -413,7 +446,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     return cudaSuccess;
   }
   const size_t scale_bytes = (size_t)KB * TT * 4 + (size_t)tc::kGroups * tc::kMaxKB * 4;
-  const size_t fixed = 1024 /*align*/ + scale_bytes + (tc::kMaxExperts + 2) * 4 + 8;
+  const size_t fixed = 1024 /*align*/ + scale_bytes + (size_t)(3 * a.E + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
   int dev = 0;
@@ -429,7 +462,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     if (dev >= 0 && dev < 64) budget[dev] = max_smem;
   }
   constexpr int kAcc = tc::acc_count(TT);
-  int stages = 12;
+  int stages = tc::kMaxStages;
   while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
     --stages;
   const size_t smem = fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8;

@@ -36,6 +36,7 @@ constexpr int kEpiWarp0 = kScaleWarp0 + kScaleWarps, kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // 448
 constexpr int kMaxExperts = 1024;
 constexpr int kAcc = 2;            // accumulators: the next unit's MMAs run during this unit's epilogue
+constexpr int kMaxStages = 8;      // TMEM holds 32 scale columns per stage
 
 template <int TT>
 struct Sz {
@@ -86,8 +87,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
   uint8_t* tiles = smem;
-  int* cum = reinterpret_cast<int*>(smem + (size_t)S * Sz<TT>::kStage);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(cum + kMaxExperts + 2)) + 7) & ~(uintptr_t)7);
+  int* cum = reinterpret_cast<int*>(smem + (size_t)S * Sz<TT>::kStage);  // [E+2] unit prefix
+  int* seg_lo = cum + p.E + 2;                                            // [E] rows [seg_lo, seg_hi)
+  int* seg_hi = seg_lo + p.E;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
   uint64_t* full = bars;            // TMA landed (codes and scales)
   uint64_t* empty = bars + S;       // MMAs done reading the stage (for the producer)
   uint64_t* sfree = bars + 2 * S;   // MMAs done reading the stage's TMEM scales (for the scale warps)
@@ -130,6 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (hi > p.a_rows) hi = (int)p.a_rows;
         const int m = hi > lo ? hi - lo : 0;
         u = ((m + TT - 1) / TT) * NB;
+        seg_lo[e] = lo;  // kept in shared memory: no global load at unit boundaries
+        seg_hi[e] = hi > lo ? hi : lo;
       }
       int inc = u;
 #pragma unroll
@@ -150,9 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after();
   // everything above overlapped the previous kernel's tail; the token rows and their
-  // scales come from the previous kernel
-  pdl_wait();
-  pdl_trigger();
+  // scales come from the previous kernel (the producer thread waits after it has sent the
+  // first weight tiles, which do not depend on it)
+  if (!(warp == 0 && lane == 0)) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
   const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
@@ -165,9 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cum[mid] <= u) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    int s0 = p.offsets[e], s1 = p.offsets[e + 1];
-    if (s0 < 0) s0 = 0;
-    if (s1 > p.a_rows) s1 = (int)p.a_rows;
+    const int s0 = seg_lo[e], s1 = seg_hi[e];
     const int local = u - cum[e];
     const int tt = local / NB;
     nb = local - tt * NB;
@@ -181,21 +187,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight tiles are read once; the token tile is read again by every weight block
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       uint32_t it = 0;
-      for (int u = u_begin; u < u_end && !s_abort; ++u) {
-        int e, nb, row0, rows;
-        decode(u, e, nb, row0, rows);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % S;
-          if (!mbar_wait(smem_u32(&empty[st]), ((it / S) & 1) ^ 1, &s_abort)) break;
-          uint8_t* t0 = tiles + (size_t)st * Sz<TT>::kStage;
-          const uint32_t fb = smem_u32(&full[st]);
-          mbar_expect_tx(fb, Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW + Sz<TT>::kSA);
-          tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
-          tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0, pol_a);
-          tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
-          tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0,
-                           pol_a);
+      int u = u_begin, kb = 0, e = 0, nb = 0, row0 = 0, rows = 0;
+      if (u < u_end) decode(u, e, nb, row0, rows);
+      auto advance = [&]() {
+        if (++kb == KB) {
+          kb = 0;
+          if (++u < u_end) decode(u, e, nb, row0, rows);
         }
+      };
+      constexpr uint32_t kBytes = Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW + Sz<TT>::kSA;
+      // The weight tiles (codes and scales) of the first pass over the ring go out before
+      // the wait: they do not depend on the previous kernel. The token tiles follow.
+      int pre_kb[kMaxStages], pre_row0[kMaxStages];
+      int npre = 0;
+      while (npre < S && u < u_end) {
+        uint8_t* t0 = tiles + (size_t)npre * Sz<TT>::kStage;
+        const uint32_t fb = smem_u32(&full[npre]);
+        mbar_expect_tx(fb, kBytes);
+        tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
+        tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
+        pre_kb[npre] = kb;
+        pre_row0[npre] = row0;
+        ++npre;
+        ++it;
+        advance();
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < npre; ++i) {
+        uint8_t* t0 = tiles + (size_t)i * Sz<TT>::kStage;
+        const uint32_t fb = smem_u32(&full[i]);
+        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, pre_kb[i] * kBKB, pre_row0[i], pol_a);
+        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, pre_kb[i] * kSfPerStage,
+                         pre_row0[i], pol_a);
+      }
+      while (u < u_end && !s_abort) {
+        const int st = it % S;
+        if (!mbar_wait(smem_u32(&empty[st]), ((it / S) & 1) ^ 1, &s_abort)) break;
+        uint8_t* t0 = tiles + (size_t)st * Sz<TT>::kStage;
+        const uint32_t fb = smem_u32(&full[st]);
+        mbar_expect_tx(fb, kBytes);
+        tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
+        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0, pol_a);
+        tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
+        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0,
+                         pol_a);
+        ++it;
+        advance();
       }
       const uint32_t issued = it;
       for (int st = 0; st < S && (uint32_t)st < issued; ++st) {
@@ -359,10 +397,10 @@ static cudaError_t launch_nv(const NvGemmArgs& a, cudaStream_t st, int* unsuppor
     max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
     if (dev >= 0 && dev < 64) budget[dev] = max_smem;
   }
-  const size_t fixed = 1024 + (nv::kMaxExperts + 2) * 4 + 8;
+  const size_t fixed = 1024 + (size_t)(3 * a.E + 2) * 4 + 8;
   // TMEM: accumulators plus 32 scale columns per stage must fit 512 columns
   const int tmem_stages = (512 - (nv::kAcc * TT + 31) / 32 * 32) / 32;
-  int stages = tmem_stages < 8 ? tmem_stages : 8;
+  int stages = tmem_stages < nv::kMaxStages ? tmem_stages : nv::kMaxStages;
   while (stages > 2 && fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8 > max_smem)
     --stages;
   const size_t smem = fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8;
