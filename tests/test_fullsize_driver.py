@@ -1,0 +1,33 @@
+"""The full-size oracle driver (tests/fullsize_oracle.py) against the oracle itself.
+
+The driver splits the FFN by expert across spawned workers; on a small problem its rows
+must equal `oracle.moe.moe_forward` evaluated directly (only the order of float64 sums
+differs), and its re-quantization allowance must equal the single-process bound's."""
+import numpy as np
+import pytest
+
+import synth
+from common import nvfp4_requant_flip_bound, requant_flip_bound
+from fullsize_oracle import forward_subsample
+from oracle import moe as M
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_driver_equals_the_oracle_forward(fmt):
+    T, H, I, E, k, seed = 12, 256, 128, 6, 3, 77
+    x = synth.activations_bf16(T, H, seed, "cpu").float().numpy()
+    ids = synth.routes(T, k, E, seed, active_per_token=[3, 2, 0, 3] * 3, device="cpu").numpy()
+    w = synth.routing_weights(T, k, seed, "cpu").numpy()
+    sub = [0, 3, 4, 7, 11]
+    got, extra = forward_subsample(x, ids, w, sub, H, I, E, seed, fmt, workers=2)
+    bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
+    bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
+    res = M.moe_forward(x, ids, w, bg, bd, fmt=fmt, tokens_subset=sub)
+    ref = res["out"]
+    scale = np.max(np.abs(ref))
+    assert np.allclose(got[sub], ref[sub], rtol=1e-12, atol=1e-15 * scale)
+    assert not np.any(got[[t for t in range(T) if t not in sub]])
+    wv = np.where(ids >= 0, w, 0.0)
+    bound = requant_flip_bound if fmt == "fp8" else nvfp4_requant_flip_bound
+    ref_extra = bound(res, ids, wv, bg, bd)
+    assert np.allclose(extra[sub], ref_extra[sub], rtol=1e-6, atol=1e-12 * scale)
