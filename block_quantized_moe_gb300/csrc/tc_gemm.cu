@@ -74,24 +74,35 @@ constexpr int kGroups = kEpiWarps / 4;
 constexpr int kMaxKB = 128;                      // K <= 16384
 constexpr int kMaxStages = 12;
 
-template <int TT>
+// K blocks per pipeline stage (KBS). One TMA box brings all of them: the tensor maps carry
+// the K-block index as a dimension of its own, and each K block lands as its own canonical
+// 128-byte-swizzled sub-tile (1024-byte aligned), exactly as in a one-block stage. Each TMA
+// instruction costs the SM a fixed time, so fewer, larger boxes move more bytes per SM: four
+// K blocks per box up to token tile 64, two at 128 (two or three stages still fit). A K that
+// is not a multiple of 128 keeps one K block per stage and the per-row maps, whose x extent
+// is K itself, so the partial last block is zero-filled rather than read past the row.
+__host__ __device__ constexpr int kbs_for(int tt) { return tt <= 64 ? 4 : 2; }
+
+template <int TT, int KBS>
 struct Smem {
-  static constexpr int kTileW = kBM * kBK;    // 16 KiB
-  static constexpr int kTileA = TT * kBK;     // TT * 128 B
+  static constexpr int kSubW = kBM * kBK;     // 16 KiB: one K block of weights
+  static constexpr int kSubA = TT * kBK;      // TT * 128 B: one K block of tokens
+  static constexpr int kTileW = kSubW * KBS;
+  static constexpr int kTileA = kSubA * KBS;
   static constexpr int kStage = kTileW + kTileA;
 };
 
 // Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the activation
 // scales of the current token tile sa[kb][TT], the weight-block scales of the current unit
 // per column group sw[kGroups][kMaxKB], the unit prefix table and the barriers.
-template <int TT>
+template <int TT, int KBS>
 __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
   uint8_t* tiles = smem;
-  float* sa = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT>::kStage);  // [KB][TT]
+  float* sa = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT, KBS>::kStage);  // [KB][TT]
   float* swt = sa + (size_t)p.kb_count * TT;                                  // [kGroups][kMaxKB]
   int* cum = reinterpret_cast<int*>(swt + kGroups * kMaxKB);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
@@ -193,25 +204,39 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       // weight blocks are read once; the activation tile is read again by every weight
       // block of the expert
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
+      // stage sp of a unit: K blocks [sp * KBS, sp * KBS + KBS)
+      auto load_w = [&](uint32_t dst, uint32_t bar, int sp, int nb, int e, uint64_t pol) {
+        if constexpr (KBS == 1)
+          tma_load_3d_hint(dst, &map_w, bar, sp * kBK, nb * kBM, e, pol);
+        else
+          tma_load_4d_hint(dst, &map_w, bar, 0, nb * kBM, sp * KBS, e, pol);
+      };
+      auto load_a = [&](uint32_t dst, uint32_t bar, int sp, int row0, uint64_t pol) {
+        if constexpr (KBS == 1)
+          tma_load_2d_hint(dst, &map_a, bar, sp * kBK, row0, pol);
+        else
+          tma_load_3d_hint(dst, &map_a, bar, 0, row0, sp * KBS, pol);
+      };
       uint32_t it = 0;
-      int u = u_begin, kb = 0, e = 0, nb = 0, tt = 0, row0 = 0, rows = 0;
+      const int SP = (KB + KBS - 1) / KBS;  // stages per unit
+      int u = u_begin, sp = 0, e = 0, nb = 0, tt = 0, row0 = 0, rows = 0;
       if (u < u_end) decode(u, e, nb, tt, row0, rows);
       auto advance = [&]() {
-        if (++kb == KB) {
-          kb = 0;
+        if (++sp == SP) {
+          sp = 0;
           if (++u < u_end) decode(u, e, nb, tt, row0, rows);
         }
       };
       // The weight tiles of the first pass over the ring go out before the wait: they do
       // not depend on the previous kernel. Their token tiles follow once it is complete.
-      int pre_kb[kMaxStages], pre_row0[kMaxStages];
+      int pre_sp[kMaxStages], pre_row0[kMaxStages];
       int npre = 0;
       while (npre < S && u < u_end) {
-        uint8_t* tw = tiles + (size_t)npre * Smem<TT>::kStage;
+        uint8_t* tw = tiles + (size_t)npre * Smem<TT, KBS>::kStage;
         const uint32_t fb = smem_u32(&full[npre]);
-        mbar_expect_tx(fb, Smem<TT>::kStage);
-        tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
-        pre_kb[npre] = kb;
+        mbar_expect_tx(fb, Smem<TT, KBS>::kStage);
+        load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
+        pre_sp[npre] = sp;
         pre_row0[npre] = row0;
         ++npre;
         ++it;
@@ -220,18 +245,18 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       pdl_wait();
       pdl_trigger();
       for (int i = 0; i < npre; ++i)
-        tma_load_2d_hint(smem_u32(tiles + (size_t)i * Smem<TT>::kStage + Smem<TT>::kTileW), &map_a,
-                         smem_u32(&full[i]), pre_kb[i] * kBK, pre_row0[i], pol_a);
+        load_a(smem_u32(tiles + (size_t)i * Smem<TT, KBS>::kStage + Smem<TT, KBS>::kTileW), smem_u32(&full[i]),
+               pre_sp[i], pre_row0[i], pol_a);
       while (u < u_end && !s_abort) {
         const int st = it % S;
         const uint32_t ph = (it / S) & 1;
         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
-        uint8_t* tw = tiles + (size_t)st * Smem<TT>::kStage;
-        uint8_t* ta = tw + Smem<TT>::kTileW;
+        uint8_t* tw = tiles + (size_t)st * Smem<TT, KBS>::kStage;
+        uint8_t* ta = tw + Smem<TT, KBS>::kTileW;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, Smem<TT>::kStage);
-        tma_load_3d_hint(smem_u32(tw), &map_w, fb, kb * kBK, nb * kBM, e, pol_w);
-        tma_load_2d_hint(smem_u32(ta), &map_a, fb, kb * kBK, row0, pol_a);
+        mbar_expect_tx(fb, Smem<TT, KBS>::kStage);
+        load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
+        load_a(smem_u32(ta), fb, sp, row0, pol_a);
         ++it;
         advance();
       }
@@ -251,22 +276,28 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
     if (lane == 0) {
       uint32_t it = 0, kc = 0;
       constexpr uint32_t idesc = idesc_f8(TT);
+      const int SP = (KB + KBS - 1) / KBS;
       for (int u = u_begin; u < u_end && !s_abort; ++u) {
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+        for (int sp = 0; sp < SP && ok; ++sp, ++it) {
           const int st = it % S;
-          const uint32_t acc = kc % kAcc;
           if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&tempty[acc]), ((kc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
-          fence_after();
-          const uint32_t tw = smem_u32(tiles + (size_t)st * Smem<TT>::kStage);
-          const uint32_t ta = tw + Smem<TT>::kTileW;
-          const uint32_t d = tmem_base + acc * TT;
+          const uint32_t tw = smem_u32(tiles + (size_t)st * Smem<TT, KBS>::kStage);
+          const uint32_t ta = tw + Smem<TT, KBS>::kTileW;
+          // the stage's K blocks (a last stage of an odd K has one; TMA zero-filled the other)
+          for (int h = 0; h < KBS && sp * KBS + h < KB; ++h, ++kc) {
+            const uint32_t acc = kc % kAcc;
+            if (!mbar_wait(smem_u32(&tempty[acc]), ((kc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
+            fence_after();
+            const uint32_t d = tmem_base + acc * TT;
+            const uint32_t tw_h = tw + h * Smem<TT, KBS>::kSubW, ta_h = ta + h * Smem<TT, KBS>::kSubA;
 #pragma unroll
-          for (int j = 0; j < kBK / 32; ++j)
-            mma_f8(d, smem_desc_sw128(tw + 32 * j), smem_desc_sw128(ta + 32 * j), idesc, j > 0 ? 1u : 0u);
+            for (int j = 0; j < kBK / 32; ++j)
+              mma_f8(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&tfull[acc]));
+          }
+          if (!ok) break;
           mma_commit(smem_u32(&empty[st]));
-          mma_commit(smem_u32(&tfull[acc]));
         }
         if (!ok) break;
       }
@@ -391,8 +422,8 @@ static bool encode_u8(CUtensorMap* map, const void* base, int rank, const uint64
                       const uint32_t* box, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t d[3], st[2];
-  cuuint32_t b[3], es[3] = {1, 1, 1};
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5] = {1, 1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];
@@ -433,7 +464,7 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int TT>
+template <int TT, int KBS>
 static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
@@ -455,7 +486,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   size_t max_smem = (dev >= 0 && dev < 64) ? budget[dev] : 0;
   if (max_smem == 0) {
     cudaFuncAttributes fattr;
-    if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
+    if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT, KBS>) != cudaSuccess) return cudaErrorInvalidValue;
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
@@ -463,32 +494,33 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   }
   constexpr int kAcc = tc::acc_count(TT);
   int stages = tc::kMaxStages;
-  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
+  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT, KBS>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
     --stages;
-  const size_t smem = fixed + (size_t)stages * tc::Smem<TT>::kStage + (2 * stages + 2 * kAcc) * 8;
+  const size_t smem = fixed + (size_t)stages * tc::Smem<TT, KBS>::kStage + (2 * stages + 2 * kAcc) * 8;
   if (smem > max_smem) {
     *unsupported = 1;
     return cudaSuccess;
   }
+  // KBS > 1: weights as (128-byte K chunk, row, K block, expert) and tokens as (128-byte K
+  // chunk, row, K block), one box holding KBS K blocks. KBS = 1: rows of K bytes.
   CUtensorMap mw, ma;
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)a.k, (cuuint64_t)a.n, (cuuint64_t)a.E};
-    cuuint64_t strides[2] = {(cuuint64_t)a.k, (cuuint64_t)a.k * (cuuint64_t)a.n};
-    cuuint32_t box[3] = {128, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w_q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if constexpr (KBS > 1) {
+    const uint64_t wd[4] = {128, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
+    const uint64_t ws[3] = {(uint64_t)a.k, 128, (uint64_t)a.k * (uint64_t)a.n};
+    const uint32_t wb[4] = {128, 128, (uint32_t)KBS, 1};
+    const uint64_t ad[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
+    const uint64_t as[2] = {(uint64_t)a.k, 128};
+    const uint32_t ab[3] = {128, (uint32_t)TT, (uint32_t)KBS};
+    if (!encode_u8_tmap(&mw, a.w_q, 4, wd, ws, wb) || !encode_u8_tmap(&ma, a.a_q, 3, ad, as, ab))
       return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)a.k, (cuuint64_t)a.a_rows};
-    cuuint64_t strides[1] = {(cuuint64_t)a.k};
-    cuuint32_t box[2] = {128, (cuuint32_t)TT};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.a_q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  } else {
+    const uint64_t wd[3] = {(uint64_t)a.k, (uint64_t)a.n, (uint64_t)a.E};
+    const uint64_t ws[2] = {(uint64_t)a.k, (uint64_t)a.k * (uint64_t)a.n};
+    const uint32_t wb[3] = {128, 128, 1};
+    const uint64_t ad[2] = {(uint64_t)a.k, (uint64_t)a.a_rows};
+    const uint64_t as[1] = {(uint64_t)a.k};
+    const uint32_t ab[2] = {128, (uint32_t)TT};
+    if (!encode_u8_tmap(&mw, a.w_q, 3, wd, ws, wb) || !encode_u8_tmap(&ma, a.a_q, 2, ad, as, ab))
       return cudaErrorInvalidValue;
   }
   tc::Params p;
@@ -508,14 +540,14 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   // any earlier one on this device (the attribute is per function and device)
   static size_t granted[64] = {};
   if (dev >= 0 && dev < 64 && smem > granted[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     granted[dev] = smem;
   } else if (dev < 0 || dev >= 64) {
-    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(tc::tc_gemm_kernel<TT>, dim3(sm_count()), dim3(64 + 32 * tc::kEpiWarps), smem, st, true, mw,
+  return launch_kernel(tc::tc_gemm_kernel<TT, KBS>, dim3(sm_count()), dim3(64 + 32 * tc::kEpiWarps), smem, st, true, mw,
                        ma, p);
 }
 
@@ -528,11 +560,13 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupporte
     *unsupported = 1;
     return cudaSuccess;
   }
+  const bool ragged = a.k % 128 != 0;  // a partial last K block: one K block per stage
   switch (a.tok_tile) {
-    case 16: return launch_tt<16>(a, st, unsupported);
-    case 32: return launch_tt<32>(a, st, unsupported);
-    case 64: return launch_tt<64>(a, st, unsupported);
-    case 128: return launch_tt<128>(a, st, unsupported);
+    case 16: return ragged ? launch_tt<16, 1>(a, st, unsupported) : launch_tt<16, tc::kbs_for(16)>(a, st, unsupported);
+    case 32: return ragged ? launch_tt<32, 1>(a, st, unsupported) : launch_tt<32, tc::kbs_for(32)>(a, st, unsupported);
+    case 64: return ragged ? launch_tt<64, 1>(a, st, unsupported) : launch_tt<64, tc::kbs_for(64)>(a, st, unsupported);
+    case 128:
+      return ragged ? launch_tt<128, 1>(a, st, unsupported) : launch_tt<128, tc::kbs_for(128)>(a, st, unsupported);
     default: *unsupported = 1; return cudaSuccess;
   }
 }
