@@ -36,15 +36,27 @@ constexpr int kEpiWarp0 = kScaleWarp0 + kScaleWarps, kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // 448
 constexpr int kMaxExperts = 1024;
 constexpr int kAcc = 2;            // accumulators: the next unit's MMAs run during this unit's epilogue
-constexpr int kMaxStages = 8;      // TMEM holds 32 scale columns per stage
+constexpr int kMaxStages = 8;
+constexpr int kMaxSfSlots = 8;     // TMEM scale slots (32 columns each, one K block)
+// K blocks (256 elements) per shared-memory stage: one TMA box per operand brings all of them
+// (the tensor maps carry the K-block index as a dimension), because each TMA instruction
+// costs the SM a fixed time; two at token tile 128, where a stage is largest.
+__host__ __device__ constexpr int kbs_for(int tt) { return tt <= 64 ? 4 : 2; }
 
-template <int TT>
+// One stage: weight codes [KBS][128 rows][128 B] (each K block a canonical 128-byte-swizzled
+// sub-tile), token codes [KBS][TT][128 B], weight scales [KBS][128][16 B], token scales
+// [KBS][TT][16 B].
+template <int TT, int KBS>
 struct Sz {
-  static constexpr int kW = kBM * kBKB;             // 16 KiB of weight codes
-  static constexpr int kA = TT * kBKB;              // token codes
-  static constexpr int kSW = kBM * kSfPerStage;     // weight scales
-  static constexpr int kSA = TT * kSfPerStage;      // token scales
-  static constexpr int kStage = ((kW + kA + kSW + kSA) + 1023) / 1024 * 1024;
+  static constexpr int kW = kBM * kBKB;             // 16 KiB of weight codes per K block
+  static constexpr int kA = TT * kBKB;              // token codes per K block
+  static constexpr int kSW = kBM * kSfPerStage;     // weight scales per K block
+  static constexpr int kSA = TT * kSfPerStage;      // token scales per K block
+  static constexpr int kOffA = KBS * kW;
+  static constexpr int kOffSW = kOffA + KBS * kA;
+  static constexpr int kOffSA = kOffSW + KBS * kSW;
+  static constexpr int kBytes = kOffSA + KBS * kSA;
+  static constexpr int kStage = (kBytes + 1023) / 1024 * 1024;
 };
 
 // Instruction descriptor of kind::mxf4nvf4: A = B = E2M1, ue4m3 scale factors, both
@@ -75,34 +87,34 @@ struct Params {
   float* out;
   int64_t ld_out;
   int64_t a_rows;
-  int n, E, kb_count, nb_count, stages;
+  int n, E, kb_count, nb_count, stages, sf_slots;
 };
 
-template <int TT>
+template <int TT, int KBS>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_sw, const __grid_constant__ CUtensorMap map_sa,
                       Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int S = p.stages;
+  const int S = p.stages, SF = p.sf_slots;
   uint8_t* tiles = smem;
-  int* cum = reinterpret_cast<int*>(smem + (size_t)S * Sz<TT>::kStage);  // [E+2] unit prefix
+  int* cum = reinterpret_cast<int*>(smem + (size_t)S * Sz<TT, KBS>::kStage);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                            // [E] rows [seg_lo, seg_hi)
   int* seg_hi = seg_lo + p.E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
-  uint64_t* full = bars;            // TMA landed (codes and scales)
+  uint64_t* full = bars;            // TMA landed (codes and scales of the stage's K blocks)
   uint64_t* empty = bars + S;       // MMAs done reading the stage (for the producer)
-  uint64_t* sfree = bars + 2 * S;   // MMAs done reading the stage's TMEM scales (for the scale warps)
-  uint64_t* sfull = bars + 3 * S;   // scale factors in TMEM
-  uint64_t* tfull = bars + 4 * S;
-  uint64_t* tempty = bars + 4 * S + kAcc;
+  uint64_t* sfree = bars + 2 * S;   // [SF] MMAs done reading a TMEM scale slot (for the scale warps)
+  uint64_t* sfull = sfree + SF;     // [SF] scale factors of one K block in TMEM
+  uint64_t* tfull = sfull + SF;
+  uint64_t* tempty = tfull + kAcc;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, NB = p.nb_count, KB = p.kb_count;
-  // TMEM columns: accumulators [0, kAcc*TT), then 32 scale columns per stage
+  // TMEM columns: accumulators [0, kAcc*TT), then 32 scale columns per TMEM scale slot
   // (16 for the weight rows, 16 for the token rows)
   const uint32_t sf0 = (uint32_t)((kAcc * TT + 31) / 32 * 32);
 
@@ -111,6 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < SF; ++i) {
       mbar_init(smem_u32(&sfree[i]), 1);
       mbar_init(smem_u32(&sfull[i]), kScaleWarps);
     }
@@ -187,26 +201,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight tiles are read once; the token tile is read again by every weight block
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       uint32_t it = 0;
-      int u = u_begin, kb = 0, e = 0, nb = 0, row0 = 0, rows = 0;
+      const int SP = (KB + KBS - 1) / KBS;  // stages per unit
+      int u = u_begin, sp = 0, e = 0, nb = 0, row0 = 0, rows = 0;
       if (u < u_end) decode(u, e, nb, row0, rows);
       auto advance = [&]() {
-        if (++kb == KB) {
-          kb = 0;
+        if (++sp == SP) {
+          sp = 0;
           if (++u < u_end) decode(u, e, nb, row0, rows);
         }
       };
-      constexpr uint32_t kBytes = Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW + Sz<TT>::kSA;
+      // one box per operand and stage: K blocks [sp * KBS, sp * KBS + KBS)
+      auto load_w = [&](uint8_t* t0, uint32_t fb) {
+        tma_load_4d_hint(smem_u32(t0), &map_w, fb, 0, nb * kBM, sp * KBS, e, pol_w);
+        tma_load_4d_hint(smem_u32(t0 + Sz<TT, KBS>::kOffSW), &map_sw, fb, 0, nb * kBM, sp * KBS, e, pol_w);
+      };
+      auto load_a = [&](uint8_t* t0, uint32_t fb, int s_sp, int s_row0) {
+        tma_load_3d_hint(smem_u32(t0 + Sz<TT, KBS>::kOffA), &map_a, fb, 0, s_row0, s_sp * KBS, pol_a);
+        tma_load_3d_hint(smem_u32(t0 + Sz<TT, KBS>::kOffSA), &map_sa, fb, 0, s_row0, s_sp * KBS, pol_a);
+      };
       // The weight tiles (codes and scales) of the first pass over the ring go out before
       // the wait: they do not depend on the previous kernel. The token tiles follow.
-      int pre_kb[kMaxStages], pre_row0[kMaxStages];
+      int pre_sp[kMaxStages], pre_row0[kMaxStages];
       int npre = 0;
       while (npre < S && u < u_end) {
-        uint8_t* t0 = tiles + (size_t)npre * Sz<TT>::kStage;
+        uint8_t* t0 = tiles + (size_t)npre * Sz<TT, KBS>::kStage;
         const uint32_t fb = smem_u32(&full[npre]);
-        mbar_expect_tx(fb, kBytes);
-        tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
-        tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
-        pre_kb[npre] = kb;
+        mbar_expect_tx(fb, Sz<TT, KBS>::kBytes);
+        load_w(t0, fb);
+        pre_sp[npre] = sp;
         pre_row0[npre] = row0;
         ++npre;
         ++it;
@@ -214,24 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       pdl_wait();
       pdl_trigger();
-      for (int i = 0; i < npre; ++i) {
-        uint8_t* t0 = tiles + (size_t)i * Sz<TT>::kStage;
-        const uint32_t fb = smem_u32(&full[i]);
-        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, pre_kb[i] * kBKB, pre_row0[i], pol_a);
-        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, pre_kb[i] * kSfPerStage,
-                         pre_row0[i], pol_a);
-      }
+      for (int i = 0; i < npre; ++i)
+        load_a(tiles + (size_t)i * Sz<TT, KBS>::kStage, smem_u32(&full[i]), pre_sp[i], pre_row0[i]);
       while (u < u_end && !s_abort) {
         const int st = it % S;
         if (!mbar_wait(smem_u32(&empty[st]), ((it / S) & 1) ^ 1, &s_abort)) break;
-        uint8_t* t0 = tiles + (size_t)st * Sz<TT>::kStage;
+        uint8_t* t0 = tiles + (size_t)st * Sz<TT, KBS>::kStage;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, kBytes);
-        tma_load_3d_hint(smem_u32(t0), &map_w, fb, kb * kBKB, nb * kBM, e, pol_w);
-        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW), &map_a, fb, kb * kBKB, row0, pol_a);
-        tma_load_3d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA), &map_sw, fb, kb * kSfPerStage, nb * kBM, e, pol_w);
-        tma_load_2d_hint(smem_u32(t0 + Sz<TT>::kW + Sz<TT>::kA + Sz<TT>::kSW), &map_sa, fb, kb * kSfPerStage, row0,
-                         pol_a);
+        mbar_expect_tx(fb, Sz<TT, KBS>::kBytes);
+        load_w(t0, fb);
+        load_a(t0, fb, sp, row0);
         ++it;
         advance();
       }
@@ -246,62 +260,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------- MMA issuer --------------------------------
     if (lane == 0) {
-      uint32_t it = 0, uc = 0;
+      uint32_t it = 0, uc = 0, kc = 0;
       constexpr uint32_t idesc = idesc_nvf4(TT);
+      const int SP = (KB + KBS - 1) / KBS;
       bool ok = true;
       for (int u = u_begin; u < u_end && ok && !s_abort; ++u, ++uc) {
         const uint32_t acc = uc % kAcc;
         if (!mbar_wait(smem_u32(&tempty[acc]), ((uc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
         fence_after();
         const uint32_t d = tmem_base + acc * TT;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int sp = 0; sp < SP && ok; ++sp, ++it) {
           const int st = it % S;
           if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&sfull[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
-          fence_after();
-          const uint32_t tw = smem_u32(tiles + (size_t)st * Sz<TT>::kStage);
-          const uint32_t ta = tw + Sz<TT>::kW;
-          const uint32_t sfa = tmem_base + sf0 + 32u * st;
-          const uint32_t sfb = sfa + 16u;
+          const uint32_t t0 = smem_u32(tiles + (size_t)st * Sz<TT, KBS>::kStage);
+          for (int h = 0; h < KBS && sp * KBS + h < KB; ++h, ++kc) {
+            const uint32_t slot = kc % SF;
+            if (!mbar_wait(smem_u32(&sfull[slot]), (kc / SF) & 1, &s_abort)) { ok = false; break; }
+            fence_after();
+            const uint32_t tw = t0 + h * Sz<TT, KBS>::kW, ta = t0 + Sz<TT, KBS>::kOffA + h * Sz<TT, KBS>::kA;
+            const uint32_t sfa = tmem_base + sf0 + 32u * slot;
+            const uint32_t sfb = sfa + 16u;
+            const int kb = sp * KBS + h;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_nvf4(d, smem_desc_sw128(tw + 32 * j), smem_desc_sw128(ta + 32 * j), idesc, sfa + 4 * j, sfb + 4 * j,
-                     (kb | j) != 0 ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)
+              mma_nvf4(d, smem_desc_sw128(tw + 32 * j), smem_desc_sw128(ta + 32 * j), idesc, sfa + 4 * j, sfb + 4 * j,
+                       (kb | j) != 0 ? 1u : 0u);
+            mma_commit(smem_u32(&sfree[slot]));
+          }
+          if (!ok) break;
           mma_commit(smem_u32(&empty[st]));
-          mma_commit(smem_u32(&sfree[st]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&tfull[acc]));
       }
-      // drain: the last commit of each accumulator before the CTA may free TMEM
+      // drain: the last commit of each accumulator and scale slot before the CTA may free TMEM
       for (uint32_t b = 0; b < (uint32_t)kAcc && b < uc; ++b) {
         const uint32_t last = uc - 1 - ((uc - 1 - b) % kAcc);
         const unsigned long long t0 = globaltimer();
         while (!mbar_try_wait(smem_u32(&tfull[b]), (last / kAcc) & 1) && globaltimer() - t0 < kTimeoutNs) {
         }
       }
-      for (uint32_t st = 0; st < (uint32_t)S && st < it; ++st) {
-        const uint32_t last = it - 1 - ((it - 1 - st) % S);
+      for (uint32_t sl = 0; sl < (uint32_t)SF && sl < kc; ++sl) {
+        const uint32_t last = kc - 1 - ((kc - 1 - sl) % SF);
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(smem_u32(&sfree[st]), (last / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        while (!mbar_try_wait(smem_u32(&sfree[sl]), (last / SF) & 1) && globaltimer() - t0 < kTimeoutNs) {
         }
       }
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------- scale factors -> TMEM -------------------------
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    uint32_t it = 0;
+    const int SP = (KB + KBS - 1) / KBS;
+    uint32_t it = 0, kc = 0;
     for (int u = u_begin; u < u_end; ++u) {
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+      for (int sp = 0; sp < SP && ok; ++sp, ++it) {
         const int st = it % S;
+        for (int h = 0; h < KBS && sp * KBS + h < KB; ++h, ++kc) {
+        const uint32_t slot = kc % SF;
         int got = mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort) ? 1 : 0;
-        if (got) got = mbar_wait(smem_u32(&sfree[st]), ((it / S) & 1) ^ 1, &s_abort) ? 1 : 0;
+        if (got) got = mbar_wait(smem_u32(&sfree[slot]), ((kc / SF) & 1) ^ 1, &s_abort) ? 1 : 0;
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         fence_after();
-        const uint8_t* sw_t = tiles + (size_t)st * Sz<TT>::kStage + Sz<TT>::kW + Sz<TT>::kA;
-        const uint8_t* sa_t = sw_t + Sz<TT>::kSW;
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + sf0 + 32u * st;
+        const uint8_t* t0 = tiles + (size_t)st * Sz<TT, KBS>::kStage;
+        const uint8_t* sw_t = t0 + Sz<TT, KBS>::kOffSW + h * Sz<TT, KBS>::kSW;
+        const uint8_t* sa_t = t0 + Sz<TT, KBS>::kOffSA + h * Sz<TT, KBS>::kSA;
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + sf0 + 32u * slot;
         // column 4j + c of lane l (in every lane quarter): the four scales of MMA step j
         // for row l + 32c
         uint32_t r[16];
@@ -327,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sfull[st]));
+        if (lane == 0) mbar_arrive(smem_u32(&sfull[slot]));
+        }
       }
       if (!ok) break;
     }
@@ -384,54 +409,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int TT>
 static cudaError_t launch_nv(const NvGemmArgs& a, cudaStream_t st, int* unsupported) {
-  const int KB = (int)cdiv(a.k, 256), NB = (int)cdiv(a.n, 128);
+  constexpr int KBS = nv::kbs_for(TT);
+  using Z = nv::Sz<TT, KBS>;
+  const int KB = (int)(a.k / 256), NB = (int)cdiv(a.n, 128);
   int dev = 0;
   cudaGetDevice(&dev);
   static size_t budget[64] = {};
   size_t max_smem = (dev >= 0 && dev < 64) ? budget[dev] : 0;
   if (max_smem == 0) {
     cudaFuncAttributes fattr;
-    if (cudaFuncGetAttributes(&fattr, nv::nvfp4_gemm_kernel<TT>) != cudaSuccess) return cudaErrorInvalidValue;
+    if (cudaFuncGetAttributes(&fattr, nv::nvfp4_gemm_kernel<TT, KBS>) != cudaSuccess) return cudaErrorInvalidValue;
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
     if (dev >= 0 && dev < 64) budget[dev] = max_smem;
   }
-  const size_t fixed = 1024 + (size_t)(3 * a.E + 2) * 4 + 8;
-  // TMEM: accumulators plus 32 scale columns per stage must fit 512 columns
-  const int tmem_stages = (512 - (nv::kAcc * TT + 31) / 32 * 32) / 32;
-  int stages = tmem_stages < nv::kMaxStages ? tmem_stages : nv::kMaxStages;
-  while (stages > 2 && fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8 > max_smem)
-    --stages;
-  const size_t smem = fixed + (size_t)stages * nv::Sz<TT>::kStage + (size_t)(4 * stages + 2 * nv::kAcc) * 8;
-  if (smem > max_smem || stages < 2) {
+  // TMEM: the accumulators, then 32 scale columns per scale slot, within 512 columns
+  const int sf_free = (512 - (nv::kAcc * TT + 31) / 32 * 32) / 32;
+  const int sf_slots = sf_free < nv::kMaxSfSlots ? sf_free : nv::kMaxSfSlots;
+  const size_t fixed = 1024 + (size_t)(3 * a.E + 2) * 4 + 8 + (size_t)(2 * sf_slots + 2 * nv::kAcc) * 8;
+  int stages = nv::kMaxStages;
+  while (stages > 2 && fixed + (size_t)stages * Z::kStage + (size_t)(2 * stages) * 8 > max_smem) --stages;
+  const size_t smem = fixed + (size_t)stages * Z::kStage + (size_t)(2 * stages) * 8;
+  if (smem > max_smem || stages < 2 || sf_slots < 2) {
     *unsupported = 1;
     return cudaSuccess;
   }
+  // codes as (128-byte chunk, row, K block[, expert]) and scales as (16-byte chunk, row,
+  // K block[, expert]): one box per operand holds KBS K blocks of 256 elements
   CUtensorMap mw, ma, msw, msa;
+  const uint64_t kc = (uint64_t)(a.k / 2), ks = (uint64_t)(a.k / 16);
   {
-    const uint64_t dims[3] = {(uint64_t)(a.k / 2), (uint64_t)a.n, (uint64_t)a.E};
-    const uint64_t strides[2] = {(uint64_t)(a.k / 2), (uint64_t)(a.k / 2) * (uint64_t)a.n};
-    const uint32_t box[3] = {(uint32_t)nv::kBKB, (uint32_t)nv::kBM, 1};
-    if (!encode_u8_tmap(&mw, a.w_q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t d[4] = {128, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
+    const uint64_t sd[3] = {kc, 128, kc * (uint64_t)a.n};
+    const uint32_t bx[4] = {128, (uint32_t)nv::kBM, (uint32_t)KBS, 1};
+    if (!encode_u8_tmap(&mw, a.w_q, 4, d, sd, bx)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {(uint64_t)(a.k / 2), (uint64_t)a.a_rows};
-    const uint64_t strides[1] = {(uint64_t)(a.k / 2)};
-    const uint32_t box[2] = {(uint32_t)nv::kBKB, (uint32_t)TT};
-    if (!encode_u8_tmap(&ma, a.a_q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t d[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
+    const uint64_t sd[2] = {kc, 128};
+    const uint32_t bx[3] = {128, (uint32_t)TT, (uint32_t)KBS};
+    if (!encode_u8_tmap(&ma, a.a_q, 3, d, sd, bx)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)(a.k / 16), (uint64_t)a.n, (uint64_t)a.E};
-    const uint64_t strides[2] = {(uint64_t)(a.k / 16), (uint64_t)(a.k / 16) * (uint64_t)a.n};
-    const uint32_t box[3] = {(uint32_t)nv::kSfPerStage, (uint32_t)nv::kBM, 1};
-    if (!encode_u8_tmap_plain(&msw, a.w_sf, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t d[4] = {16, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
+    const uint64_t sd[3] = {ks, 16, ks * (uint64_t)a.n};
+    const uint32_t bx[4] = {16, (uint32_t)nv::kBM, (uint32_t)KBS, 1};
+    if (!encode_u8_tmap_plain(&msw, a.w_sf, 4, d, sd, bx)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {(uint64_t)(a.k / 16), (uint64_t)a.a_rows};
-    const uint64_t strides[1] = {(uint64_t)(a.k / 16)};
-    const uint32_t box[2] = {(uint32_t)nv::kSfPerStage, (uint32_t)TT};
-    if (!encode_u8_tmap_plain(&msa, a.a_sf, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t d[3] = {16, (uint64_t)a.a_rows, (uint64_t)KB};
+    const uint64_t sd[2] = {ks, 16};
+    const uint32_t bx[3] = {16, (uint32_t)TT, (uint32_t)KBS};
+    if (!encode_u8_tmap_plain(&msa, a.a_sf, 3, d, sd, bx)) return cudaErrorInvalidValue;
   }
   nv::Params p;
   p.offsets = a.offsets;
@@ -445,14 +475,16 @@ static cudaError_t launch_nv(const NvGemmArgs& a, cudaStream_t st, int* unsuppor
   p.kb_count = KB;
   p.nb_count = NB;
   p.stages = stages;
+  p.sf_slots = sf_slots;
   static size_t granted[64] = {};
   if (dev < 0 || dev >= 64 || smem > granted[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(nv::nvfp4_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(nv::nvfp4_gemm_kernel<TT, KBS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) granted[dev] = smem;
   }
-  return launch_kernel(nv::nvfp4_gemm_kernel<TT>, dim3(sm_count()), dim3(nv::kThreads), smem, st, true, mw, ma, msw,
-                       msa, p);
+  return launch_kernel(nv::nvfp4_gemm_kernel<TT, KBS>, dim3(sm_count()), dim3(nv::kThreads), smem, st, true, mw, ma,
+                       msw, msa, p);
 }
 
 cudaError_t launch_nvfp4_gemm(const NvGemmArgs& a, cudaStream_t st, int* unsupported) {
