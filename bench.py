@@ -51,7 +51,11 @@ WORKLOADS = {
     "decode-h2048-i768-e8-t1-a2": (1, 2048, 768, 8, 8, 2, 0),
     # one path forced, to compare them
     "decode-h4096-i1024-e64-t8-a8-slots": (8, 4096, 1024, 64, 8, 8, 1),
-    "decode-h4096-i1024-e64-t1-a8-grouped": (1, 4096, 1024, 64, 8, 8, 2),
+    "decode-h4096-i1024-e64-t1-a8-slots": (1, 4096, 1024, 64, 8, 8, 1),
+    "decode-h4096-i1024-e64-t1-a2-slots": (1, 4096, 1024, 64, 8, 2, 1),
+    "decode-h2048-i768-e8-t1-a2-slots": (1, 2048, 768, 8, 8, 2, 1),
+    "decode-h4096-i1024-e64-t2-a8": (2, 4096, 1024, 64, 8, 8, 0),
+    "decode-h4096-i1024-e64-t2-a8-slots": (2, 4096, 1024, 64, 8, 8, 1),
     "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
@@ -277,8 +281,8 @@ class MoeWorkload:
         T, H, I, E, k, active, path = WORKLOADS[name]
         self.name, self.T, self.H, self.I, self.E, self.k, self.active, self.path = name, T, H, I, E, k, active, path
         self.dev = device
-        if path == 0:  # the forward's automatic choice (route slots up to two tokens)
-            path = 1 if T <= 2 else 2
+        if path == 0:  # the forward's automatic choice: the grouped path
+            path = 2
             self.path = path
         if T >= 256:
             self.NSETS = 2

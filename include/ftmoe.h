@@ -218,8 +218,8 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
 /* ------------------------------------------------------------------------------------
  * Fused forward. Launch shapes depend only on the shape below, never on route content,
  * so one captured CUDA graph can be replayed while routes and inputs change in place.
- * path: 0 = automatic (tokens <= 2 -> route-slot streaming path, else grouped
- * tensor-core path), 1 = route-slot path, 2 = grouped path.
+ * path: 0 = automatic (the grouped tensor-core path at every batch size), 1 = route-slot
+ * streaming path (FP8 only), 2 = grouped path.
  * ------------------------------------------------------------------------------------ */
 typedef struct ftmoe_moe_shape {
   int64_t tokens;     /* T */

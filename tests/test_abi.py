@@ -87,8 +87,10 @@ def test_forward_workspace_layout(ft):
     for key in ("x_q", "x_scales", "gateup", "act_q", "act_scales", "down"):
         assert lay[key] % 256 == 0
     assert lay["rows_q"] > 0  # eight tokens take the grouped path: gather buffers
-    slot = ft.ftmoe_forward_workspace_layout(ft.moe_shape(2, 4096, 1024, 8, 64))
-    assert slot["rows_q"] == 0 and slot["dst2src"] == 0  # one or two tokens: route-slot path
+    auto2 = ft.ftmoe_forward_workspace_layout(ft.moe_shape(2, 4096, 1024, 8, 64))
+    assert auto2["rows_q"] > 0  # the automatic path is the grouped one at every batch size
+    slot = ft.ftmoe_forward_workspace_layout(ft.moe_shape(2, 4096, 1024, 8, 64, path=1))
+    assert slot["rows_q"] == 0 and slot["dst2src"] == 0  # route-slot path: no gather buffers
     g = ft.ftmoe_forward_workspace_layout(ft.moe_shape(256, 7168, 2048, 6, 256))
     assert g["rows_q"] > 0 and g["dst2src"] > 0
     bad = ft.moe_shape(8, 4096, 1024, 8, 64, tok_tile=48)

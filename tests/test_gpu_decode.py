@@ -1,4 +1,5 @@
-"""Decode MoE FFN (the route-slot streaming path) against the oracle, through the C ABI.
+"""Decode MoE FFN (the grouped path and the route-slot streaming path) against the oracle,
+through the C ABI.
 
 Workloads of the FreeToken decode page ("perf(moe): skip inactive block-fp8 decode
 routes", GPU decode A/B): batch 1 (and 8), top-k 8, FP8 block-scaled expert banks,
@@ -29,11 +30,12 @@ def _check(prob, out, ids=None, weights=None, x=None):
     return prob.check(out, ids=ids, weights=weights, x=x)
 
 
-def test_decode_2048_768_two_of_eight_active(ft):
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_decode_2048_768_two_of_eight_active(ft, path):
     # hidden 2048, intermediate 768, 8 resident experts, top-k 8, 6 of 8 slots -1
     p = Problem(1, 2048, 768, 8, 8, seed=0xF7E00001, active=2)
     assert int((p.ids >= 0).sum()) == 2
-    out, _, _ = p.forward()
+    out, _, _ = p.forward(path=path)
     torch.cuda.synchronize()
     _check(p, out)
 
