@@ -39,7 +39,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 WORKLOADS = {
     # name: (tokens, hidden, inter, experts, topk, active per token,
-    #        path: 0 automatic, 1 route slots (streaming kernel), 2 grouped (tcgen05))
+    #        path: 0 automatic, 1 route slots (streaming kernel), 2 grouped (tcgen05) with the
+    #        separate SiLU-and-mul kernel, 3 grouped with SiLU-and-mul fused into gate/up)
     "decode-h4096-i1024-e64-t8-a8": (8, 4096, 1024, 64, 8, 8, 0),
     "decode-h4096-i1024-e64-t1-a8": (1, 4096, 1024, 64, 8, 8, 0),
     "decode-h4096-i1024-e64-t8-a4": (8, 4096, 1024, 64, 8, 4, 0),
@@ -56,12 +57,17 @@ WORKLOADS = {
     "decode-h2048-i768-e8-t1-a2-slots": (1, 2048, 768, 8, 8, 2, 1),
     "decode-h4096-i1024-e64-t2-a8": (2, 4096, 1024, 64, 8, 8, 0),
     "decode-h4096-i1024-e64-t2-a8-slots": (2, 4096, 1024, 64, 8, 8, 1),
-    "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 2),
-    "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
-    "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
+    "decode-h4096-i1024-e64-t8-a8-sep": (8, 4096, 1024, 64, 8, 8, 2),
+    "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 0),
+    "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 0),
+    "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 0),
+    "prefill-fp8-h7168-i2048-e256-r1536-sep": (256, 7168, 2048, 256, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e256-r6144-sep": (1024, 7168, 2048, 256, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e256-r24576-sep": (4096, 7168, 2048, 256, 6, 6, 2),
     # a 32-expert bank with the same rows per expert (96) as the 24,576-route case: small
     # enough (1.4 GB of weights) for multi-pass profiler captures
-    "prefill-fp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 0),
+    "prefill-fp8-h7168-i2048-e32-r3072-sep": (512, 7168, 2048, 32, 6, 6, 2),
     # NVFP4 weights and activations (e2m1, one e4m3 scale per 16 elements, fp32 tensor
     # scales) on the same prefill geometry
     "prefill-nvfp4-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
@@ -281,9 +287,6 @@ class MoeWorkload:
         T, H, I, E, k, active, path = WORKLOADS[name]
         self.name, self.T, self.H, self.I, self.E, self.k, self.active, self.path = name, T, H, I, E, k, active, path
         self.dev = device
-        if path == 0:  # the forward's automatic choice: the grouped path
-            path = 2
-            self.path = path
         if T >= 256:
             self.NSETS = 2
         self.fmt = workload_format(name)
@@ -314,6 +317,11 @@ class MoeWorkload:
             self.sets.append((synth.activations_bf16(T, H, s, device), ids,
                               synth.routing_weights(T, k, s, device)))
         self.shape = ft.moe_shape(T, H, I, k, E, fmt=self.ft_fmt, path=path)
+        # the path the library takes (path 0 is its automatic choice): the route-slot path,
+        # or the grouped path with SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up
+        # buffer in the workspace) or in its own kernel
+        self.grouped = path != 1
+        self.fused = self.grouped and ft.ftmoe_forward_workspace_layout(self.shape)["gateup_bytes"] == 0
         self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
         self.x_in = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
@@ -321,7 +329,8 @@ class MoeWorkload:
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         # kernels per forward: quantize, [segment, gather,] gate/up, SiLU-and-mul, down, combine;
         # each NVFP4 quantizer adds an amax pass and the tensor-scale conversion
-        self.launches_per_step = (5 if path == 1 else 7) + (4 if self.fmt == "nvfp4" else 0)
+        self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) +
+                                  (4 if self.fmt == "nvfp4" else 0))
 
     # algorithmic bytes/flops of one forward on route set i
     def work(self, i):
@@ -335,17 +344,21 @@ class MoeWorkload:
         row = lambda n: code_bytes(f, n) + scale_bytes(f, n)  # noqa: E731 - one quantized row
         w_gu = weight_bytes(f, 2 * I, H)
         w_dn = weight_bytes(f, H, I)
-        out_rows = R if self.path == 1 else ra   # the route-slot path also writes zero rows
-        gateup = uniq * w_gu + (T if self.path == 1 else ra) * row(H) + out_rows * 2 * I * 4
+        out_rows = ra if self.grouped else R     # the route-slot path also writes zero rows
+        if self.fused:   # gate/up + SiLU-and-mul: writes the re-quantized rows, no fp32 rows
+            gateup = uniq * w_gu + ra * row(H) + ra * row(I)
+            silu = 0
+        else:
+            gateup = uniq * w_gu + (ra if self.grouped else T) * row(H) + out_rows * 2 * I * 4
+            silu = out_rows * 2 * I * 4 + out_rows * row(I)
         down = uniq * w_dn + out_rows * row(I) + out_rows * H * 4
         total = (T * H * 2 + T * row(H)                            # quantize
-                 + gateup
-                 + out_rows * 2 * I * 4 + out_rows * row(I)        # silu_mul
+                 + gateup + silu
                  + down
                  + ra * H * 4 + T * k * 8 + T * H * 2)             # combine
         if f == "nvfp4":
             total += T * H * 2 + out_rows * 2 * I * 4              # amax passes of the tensor scales
-        if self.path == 2:
+        if self.grouped:
             total += T * k * 4 * 3 + ra * row(H) * 2               # segment + gather
         flops = 2 * ra * (2 * I * H + H * I)
         return dict(bytes=total, gateup_bytes=gateup, flops=flops, gateup_flops=2 * ra * 2 * I * H,
@@ -367,7 +380,7 @@ class MoeWorkload:
         lay = ft.ftmoe_forward_workspace_layout(self.shape)
         T, H, k = self.T, self.H, self.k
         gu = self.ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(T * k, -1)
-        if self.path == 1:
+        if not self.grouped:
             xq = self.ws[lay["x_q"]:lay["x_q"] + T * H].view(T, H)
             xs = self.ws[lay["x_scales"]:lay["x_scales"] + T * (-(-H // 128)) * 4].view(torch.float32).view(T, -1)
             act, routes = ft.make_act(xq, xs), ft.slot_routes(self.ids_in)
@@ -387,6 +400,11 @@ class MoeWorkload:
             act = ft.make_act(rq, rs, xg, fmt=ft.FMT_NVFP4)
             kname = f"nvfp4_gemm_kernel<{tile}> (gate/up, grouped, tcgen05 block-scaled)"
         routes = ft.grouped_routes(off)
+        if self.fused:
+            aq = self.ws[lay["act_q"]:lay["act_q"] + lay["act_q_bytes"]].view(R, -1)
+            asc = self.ws[lay["act_scales"]:lay["act_scales"] + lay["act_scales_bytes"]].view(torch.float32).view(R, -1)
+            kname = f"tc_gemm_kernel<{tile}, gate/up pairs> (gate/up + SiLU-and-mul + FP8 requant, tcgen05)"
+            return kname, lambda: ft.ftmoe_grouped_gemm_gateup_silu(act, routes, self.bank_gu, aq, asc, tok_tile=tile)
         return kname, lambda: ft.ftmoe_grouped_gemm_gateup(act, routes, self.bank_gu, gu, tok_tile=tile, variant=2)
 
 
@@ -577,6 +595,9 @@ def run_gpu(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
+                   "forward_path": ("route slots (streaming kernel)" if not wl.grouped else
+                                    "grouped, SiLU-and-mul fused into the gate/up GEMM" if wl.fused else
+                                    "grouped, separate SiLU-and-mul kernel"),
                    "l2": L2Flush.DESC, "parallelism": f"replicas x{world}",
                    "graph": ("direct launches (--eager)" if args.eager else
                              "one CUDA graph replayed; inputs copied in place between steps")},

@@ -43,7 +43,7 @@ class Routes(ctypes.Structure):
 
 
 class Tile(ctypes.Structure):
-    _fields_ = [("tok_tile", c_i32), ("variant", c_i32), ("reserved", c_i32 * 2)]
+    _fields_ = [("tok_tile", c_i32), ("variant", c_i32), ("wblocks", c_i32), ("reserved", c_i32)]
 
 
 class MoeShape(ctypes.Structure):
@@ -79,6 +79,9 @@ _SIGNATURES = [
     ("ftmoe_grouped_gemm_gateup", c_i32, [ctypes.POINTER(Act), ctypes.POINTER(Routes),
                                           ctypes.POINTER(ExpertBank), c_ptr, c_i64,
                                           ctypes.POINTER(Tile), c_ptr]),
+    ("ftmoe_grouped_gemm_gateup_silu", c_i32, [ctypes.POINTER(Act), ctypes.POINTER(Routes),
+                                               ctypes.POINTER(ExpertBank), c_ptr, c_ptr,
+                                               ctypes.POINTER(Tile), c_ptr]),
     ("ftmoe_silu_mul", c_i32, [c_ptr, c_i64, c_i64, c_i64, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
     ("ftmoe_grouped_gemm_down", c_i32, [ctypes.POINTER(Act), ctypes.POINTER(Routes),
                                         ctypes.POINTER(ExpertBank), c_ptr, c_i64,
@@ -198,19 +201,26 @@ def slot_routes(expert_ids):
     return Routes(ROUTES_SLOTS, topk, T, None, _p(expert_ids))
 
 
-def _tile(tok_tile=0, variant=0):
-    return Tile(tok_tile, variant, (c_i32 * 2)(0, 0))
+def _tile(tok_tile=0, variant=0, wblocks=0):
+    return Tile(tok_tile, variant, wblocks, 0)
 
 
-def ftmoe_grouped_gemm_gateup(act, routes, bank, out, tok_tile=0, variant=0, stream=None):
-    t = _tile(tok_tile, variant)
+def ftmoe_grouped_gemm_gateup(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, stream=None):
+    t = _tile(tok_tile, variant, wblocks)
     _check("ftmoe_grouped_gemm_gateup", lib().ftmoe_grouped_gemm_gateup(
         ctypes.byref(act), ctypes.byref(routes), ctypes.byref(bank), _p(out), out.stride(0),
         ctypes.byref(t), _stream(stream)))
 
 
-def ftmoe_grouped_gemm_down(act, routes, bank, out, tok_tile=0, variant=0, stream=None):
-    t = _tile(tok_tile, variant)
+def ftmoe_grouped_gemm_gateup_silu(act, routes, bank, q, scales, tok_tile=0, stream=None):
+    t = _tile(tok_tile)
+    _check("ftmoe_grouped_gemm_gateup_silu", lib().ftmoe_grouped_gemm_gateup_silu(
+        ctypes.byref(act), ctypes.byref(routes), ctypes.byref(bank), _p(q), _p(scales),
+        ctypes.byref(t), _stream(stream)))
+
+
+def ftmoe_grouped_gemm_down(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, stream=None):
+    t = _tile(tok_tile, variant, wblocks)
     _check("ftmoe_grouped_gemm_down", lib().ftmoe_grouped_gemm_down(
         ctypes.byref(act), ctypes.byref(routes), ctypes.byref(bank), _p(out), out.stride(0),
         ctypes.byref(t), _stream(stream)))

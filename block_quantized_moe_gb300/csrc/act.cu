@@ -9,10 +9,6 @@
 
 namespace ftmoe {
 
-__device__ __forceinline__ float silu_mul_1(float g, float u) {
-  return g / (1.0f + expf(-g)) * u;
-}
-
 // One warp per (row, 128 outputs); lane owns 4 consecutive outputs.
 template <bool kVec>
 __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(

@@ -90,6 +90,10 @@ __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
 // explicit intrinsic documents that the quantization decision depends on it).
 __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
 
+// silu(g) * u in fp32, the one expression every SiLU-and-mul of the library evaluates (the
+// separate kernel and the gate/up GEMM epilogue give bit-identical results).
+__device__ __forceinline__ float silu_mul_1(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 // Positive floats order like their bit patterns, so a max over |x| can use atomicMax on
 // the bits of a zero-initialised word.
 __device__ __forceinline__ void atomic_max_pos(float* addr, float v) {

@@ -109,7 +109,13 @@ struct TcGemmArgs {
   int32_t E;
   const int32_t* offsets;
   int32_t tok_tile;
+  int32_t wblocks;         // 1: one 128-row weight block per unit, 2: two adjacent blocks
+  int32_t silu;            // 1: gate block j + up block j per unit, SiLU-and-mul + FP8 requant
+  uint8_t* q_out;          // silu: codes [a_rows][n/2]
+  float* s_out;            // silu: scales [a_rows][n/256]
 };
+// whether an n x k weight matrix can run two weight blocks per unit (n % 256, k % 128)
+bool tc_gemm_pairs_ok(int64_t n, int64_t k);
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s, int* unsupported);
 uint32_t read_err_tc_gemm();
 

@@ -38,11 +38,24 @@ namespace ftmoe {
 namespace tc {
 
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
-constexpr int kBK = 128;               // K bytes per stage = one scale block
+constexpr int kBK = 128;               // K bytes per K block = one scale block
 constexpr int kMaxExperts = 1024;
-// TMEM accumulators in rotation: as many TT-column accumulators as 512 columns hold, at
-// most 16, so the MMA can run that many K blocks ahead of the promotion
-__host__ __device__ constexpr int acc_count(int tt) { return 512 / tt > 16 ? 16 : 512 / tt; }
+
+// What one unit of work covers, besides its token tile:
+//   kSingle     one 128-row weight block; fp32 output columns [128 nb, 128 nb + 128)
+//   kPair       two adjacent weight blocks 2p, 2p + 1 that share the token tile; fp32 output
+//   kGateUpSilu gate block j (rows 128 j ..) and up block j (rows I + 128 j ..) of a gate/up
+//               matrix; the epilogue forms silu(g) * u for intermediate columns
+//               [128 j, 128 j + 128) -- exactly one 1x128 group -- and re-quantizes it to FP8
+//               with its group scale, so no fp32 gate/up row is ever written
+// Two weight blocks per token tile halve the token bytes each stage carries for every
+// weight byte, so more weight bytes fit in flight in the same shared memory.
+enum Mode { kSingle = 0, kPair = 1, kGateUpSilu = 2 };
+__host__ __device__ constexpr int wb_of(int mode) { return mode == kSingle ? 1 : 2; }
+
+// TMEM accumulators in rotation: as many (weight blocks x TT)-column accumulators as 512
+// columns hold, at most 16, so the MMA can run that many K blocks ahead of the promotion
+__host__ __device__ constexpr int acc_count(int cols) { return 512 / cols > 16 ? 16 : 512 / cols; }
 
 // Instruction descriptor, kind::f8f6f4: D fp32, A = B = e4m3, both K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_f8(int n) {
@@ -63,8 +76,10 @@ struct Params {
   const int32_t* offsets;
   const float* a_s;   // [a_rows][kb_count]
   const float* w_s;   // [E][nb_count][kb_count]
-  float* out;
+  float* out;         // kSingle, kPair: [a_rows][ld_out]
   int64_t ld_out;
+  uint8_t* q_out;     // kGateUpSilu: FP8 codes [a_rows][n / 2]
+  float* s_out;       // kGateUpSilu: group scales [a_rows][n / 256]
   int64_t a_rows;
   int n, k, E, kb_count, nb_count, stages;
 };
@@ -73,44 +88,80 @@ constexpr int kEpiWarps = 16;                    // 4 column groups x 4 TMEM lan
 constexpr int kGroups = kEpiWarps / 4;
 constexpr int kMaxKB = 128;                      // K <= 16384
 constexpr int kMaxStages = 12;
+constexpr int kSaChunk = 8;                      // K blocks of activation scales staged at once
 
 // K blocks per pipeline stage (KBS). One TMA box brings all of them: the tensor maps carry
 // the K-block index as a dimension of its own, and each K block lands as its own canonical
 // 128-byte-swizzled sub-tile (1024-byte aligned), exactly as in a one-block stage. Each TMA
 // instruction costs the SM a fixed time, so fewer, larger boxes move more bytes per SM: four
-// K blocks per box up to token tile 64, two at 128 (two or three stages still fit). A K that
+// K blocks per box up to token tile 64, two at 128 (two or three stages still fit); with two
+// weight blocks per unit a box already carries twice the weight bytes per K block. A K that
 // is not a multiple of 128 keeps one K block per stage and the per-row maps, whose x extent
 // is K itself, so the partial last block is zero-filled rather than read past the row.
-__host__ __device__ constexpr int kbs_for(int tt) { return tt <= 64 ? 4 : 2; }
+__host__ __device__ constexpr int kbs_for(int tt, int mode) {
+  return mode == kSingle ? (tt <= 64 ? 4 : 2) : (tt <= 32 ? 2 : 1);
+}
 
-template <int TT, int KBS>
-struct Smem {
-  static constexpr int kSubW = kBM * kBK;     // 16 KiB: one K block of weights
-  static constexpr int kSubA = TT * kBK;      // TT * 128 B: one K block of tokens
-  static constexpr int kTileW = kSubW * KBS;
-  static constexpr int kTileA = kSubA * KBS;
-  static constexpr int kStage = kTileW + kTileA;
+// Warp roles. Warp 0 issues TMA, warp 1 issues MMAs, the last kEpiWarps warps promote.
+// Units with two weight blocks at token tile 128 hold 64 fp32 accumulators per epilogue
+// thread; those kernels add two idle warps so that warps 0-3 form a warpgroup that gives
+// registers back (setmaxnreg.dec to kCtlRegs) to the four epilogue warpgroups
+// (setmaxnreg.inc to kEpiRegs). The launch pool is threads x the kernel's register count;
+// the host checks kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps against it before launching,
+// since an increase the pool cannot cover would never complete.
+template <int TT, int MODE>
+struct Warps {
+  static constexpr bool kSplitRegs = TT == 128 && wb_of(MODE) == 2;
+  static constexpr int kCtl = kSplitRegs ? 4 : 2;
+  static constexpr int kThreads = 32 * (kCtl + kEpiWarps);
+  static constexpr int kCtlRegs = 56, kEpiRegs = 104;
+  static constexpr int kRegsNeeded = kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps;
 };
 
-// Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the activation
-// scales of the current token tile sa[kb][TT], the weight-block scales of the current unit
-// per column group sw[kGroups][kMaxKB], the unit prefix table and the barriers.
-template <int TT, int KBS>
-__global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
+template <int TT, int KBS, int MODE>
+struct Smem {
+  static constexpr int kWB = wb_of(MODE);
+  static constexpr int kSubW = kBM * kBK;     // 16 KiB: one K block of one weight block
+  static constexpr int kSubA = TT * kBK;      // TT * 128 B: one K block of tokens
+  static constexpr int kTileW = kSubW * KBS * kWB;
+  static constexpr int kTileA = kSubA * KBS;
+  static constexpr int kStage = kTileW + kTileA;
+  // Byte offset of weight block b, K block h inside a stage's weight tile. kPair boxes are
+  // 256 rows high, so the two blocks of a K block are adjacent; kGateUpSilu boxes carry the
+  // gate half, then the up half, each KBS K blocks long.
+  static __device__ __forceinline__ uint32_t w_off(int b, int h) {
+    return (uint32_t)((MODE == kPair ? h * kWB + b : b * KBS + h) * kSubW);
+  }
+  // epilogue tables (bytes): activation scales [kGroups][2][kSaChunk][TT / kGroups],
+  // weight-block scales [kGroups][kWB][kMaxKB], SiLU group maxima [kGroups][4][TT / kGroups]
+  static constexpr int kSaBytes = 2 * kSaChunk * TT * 4;
+  static constexpr int kSwBytes = kGroups * kWB * kMaxKB * 4;
+  static constexpr int kRedBytes = MODE == kGateUpSilu ? 4 * TT * 4 : 0;
+};
+
+// Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the epilogue tables,
+// the unit prefix table, the expert segment bounds and the barriers.
+template <int TT, int KBS, int MODE>
+__global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a, Params p) {
+  using SM = Smem<TT, KBS, MODE>;
+  using W = Warps<TT, MODE>;
+  constexpr int WB = SM::kWB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
   uint8_t* tiles = smem;
-  float* sa = reinterpret_cast<float*>(smem + (size_t)S * Smem<TT, KBS>::kStage);  // [KB][TT]
-  float* swt = sa + (size_t)p.kb_count * TT;                                  // [kGroups][kMaxKB]
-  int* cum = reinterpret_cast<int*>(swt + kGroups * kMaxKB);  // [E+2] unit prefix
+  float* sa = reinterpret_cast<float*>(smem + (size_t)S * SM::kStage);
+  float* swt = sa + SM::kSaBytes / 4;
+  float* red = swt + SM::kSwBytes / 4;
+  int* cum = reinterpret_cast<int*>(red + SM::kRedBytes / 4);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
   int* seg_hi = seg_lo + p.E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
-  constexpr int kAcc = acc_count(TT);
+  constexpr int kAcc = acc_count(WB * TT);
+  constexpr int kTmemCols = kAcc * WB * TT < 32 ? 32 : kAcc * WB * TT;
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + kAcc;
   __shared__ uint32_t s_tmem;
@@ -118,6 +169,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, NB = p.nb_count, KB = p.kb_count;
+  const int NBU = MODE == kSingle ? NB : NB / 2;  // units per token tile
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -131,7 +183,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // unit prefix: cum[e] = number of units of experts < e (units = token tiles x weight blocks)
+  // unit prefix: cum[e] = number of units of experts < e (units = token tiles x NBU)
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < E; base += 32) {
@@ -144,7 +196,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
         if (lo < 0) lo = 0;
         if (hi > p.a_rows) hi = (int)p.a_rows;
         const int m = hi > lo ? hi - lo : 0;
-        u = ((m + TT - 1) / TT) * NB;
+        u = ((m + TT - 1) / TT) * NBU;
         seg_lo[e] = lo;  // kept in shared memory: no global load at unit boundaries
         seg_hi[e] = hi > lo ? hi : lo;
       }
@@ -161,7 +213,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(kAcc * TT < 32 ? 32 : kAcc * TT));
+                 "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   fence_before();
@@ -178,11 +230,11 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
   // a contiguous range of units per CTA; units run (expert, token tile, weight block) with
-  // the weight block innermost, so the token tile and its scales stay put across units
+  // the weight block innermost, so the token tile stays in L2 across units
   const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
   const int u_end = (int)(((int64_t)(blockIdx.x + 1) * total_units) / gridDim.x);
 
-  // unit -> (expert, weight block, token tile, first row, rows in tile)
+  // unit -> (expert, weight block or block pair, token tile, first row, rows in tile)
   auto decode = [&](int u, int& e, int& nb, int& tt, int& row0, int& rows) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {  // last e with cum[e] <= u
@@ -192,12 +244,19 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
     e = lo;
     const int s0 = seg_lo[e], s1 = seg_hi[e];
     const int local = u - cum[e];
-    tt = local / NB;
-    nb = local - tt * NB;
+    tt = local / NBU;
+    nb = local - tt * NBU;
     row0 = s0 + tt * TT;
     rows = min(TT, s1 - row0);
   };
+  // weight block (row block of the n x k matrix) b of unit index nb
+  auto wblock = [&](int nb, int b) {
+    return MODE == kSingle ? nb : (MODE == kPair ? 2 * nb + b : b * NBU + nb);
+  };
 
+  if (warp < W::kCtl) {
+    // control warpgroup (register split: the whole warpgroup lowers its limit here)
+    if constexpr (W::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(W::kCtlRegs));
   if (warp == 0) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
@@ -206,13 +265,17 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       // stage sp of a unit: K blocks [sp * KBS, sp * KBS + KBS)
       auto load_w = [&](uint32_t dst, uint32_t bar, int sp, int nb, int e, uint64_t pol) {
-        if constexpr (KBS == 1)
+        if constexpr (MODE == kGateUpSilu)
+          tma_load_5d_hint(dst, &map_w, bar, 0, 0, sp * KBS, nb, 2 * e, pol);
+        else if constexpr (MODE == kPair)
+          tma_load_4d_hint(dst, &map_w, bar, 0, nb * 2 * kBM, sp * KBS, e, pol);
+        else if constexpr (KBS == 1)
           tma_load_3d_hint(dst, &map_w, bar, sp * kBK, nb * kBM, e, pol);
         else
           tma_load_4d_hint(dst, &map_w, bar, 0, nb * kBM, sp * KBS, e, pol);
       };
       auto load_a = [&](uint32_t dst, uint32_t bar, int sp, int row0, uint64_t pol) {
-        if constexpr (KBS == 1)
+        if constexpr (KBS == 1 && MODE == kSingle)
           tma_load_2d_hint(dst, &map_a, bar, sp * kBK, row0, pol);
         else
           tma_load_3d_hint(dst, &map_a, bar, 0, row0, sp * KBS, pol);
@@ -232,9 +295,9 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       int pre_sp[kMaxStages], pre_row0[kMaxStages];
       int npre = 0;
       while (npre < S && u < u_end) {
-        uint8_t* tw = tiles + (size_t)npre * Smem<TT, KBS>::kStage;
+        uint8_t* tw = tiles + (size_t)npre * SM::kStage;
         const uint32_t fb = smem_u32(&full[npre]);
-        mbar_expect_tx(fb, Smem<TT, KBS>::kStage);
+        mbar_expect_tx(fb, SM::kStage);
         load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
         pre_sp[npre] = sp;
         pre_row0[npre] = row0;
@@ -245,16 +308,16 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       pdl_wait();
       pdl_trigger();
       for (int i = 0; i < npre; ++i)
-        load_a(smem_u32(tiles + (size_t)i * Smem<TT, KBS>::kStage + Smem<TT, KBS>::kTileW), smem_u32(&full[i]),
-               pre_sp[i], pre_row0[i], pol_a);
+        load_a(smem_u32(tiles + (size_t)i * SM::kStage + SM::kTileW), smem_u32(&full[i]), pre_sp[i], pre_row0[i],
+               pol_a);
       while (u < u_end && !s_abort) {
         const int st = it % S;
         const uint32_t ph = (it / S) & 1;
         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
-        uint8_t* tw = tiles + (size_t)st * Smem<TT, KBS>::kStage;
-        uint8_t* ta = tw + Smem<TT, KBS>::kTileW;
+        uint8_t* tw = tiles + (size_t)st * SM::kStage;
+        uint8_t* ta = tw + SM::kTileW;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, Smem<TT, KBS>::kStage);
+        mbar_expect_tx(fb, SM::kStage);
         load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
         load_a(smem_u32(ta), fb, sp, row0, pol_a);
         ++it;
@@ -282,18 +345,22 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
         for (int sp = 0; sp < SP && ok; ++sp, ++it) {
           const int st = it % S;
           if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) { ok = false; break; }
-          const uint32_t tw = smem_u32(tiles + (size_t)st * Smem<TT, KBS>::kStage);
-          const uint32_t ta = tw + Smem<TT, KBS>::kTileW;
+          const uint32_t tw = smem_u32(tiles + (size_t)st * SM::kStage);
+          const uint32_t ta = tw + SM::kTileW;
           // the stage's K blocks (a last stage of an odd K has one; TMA zero-filled the other)
           for (int h = 0; h < KBS && sp * KBS + h < KB; ++h, ++kc) {
             const uint32_t acc = kc % kAcc;
             if (!mbar_wait(smem_u32(&tempty[acc]), ((kc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
             fence_after();
-            const uint32_t d = tmem_base + acc * TT;
-            const uint32_t tw_h = tw + h * Smem<TT, KBS>::kSubW, ta_h = ta + h * Smem<TT, KBS>::kSubA;
+            const uint32_t ta_h = ta + h * SM::kSubA;
 #pragma unroll
-            for (int j = 0; j < kBK / 32; ++j)
-              mma_f8(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+            for (int b = 0; b < WB; ++b) {
+              const uint32_t d = tmem_base + acc * (WB * TT) + b * TT;
+              const uint32_t tw_h = tw + SM::w_off(b, h);
+#pragma unroll
+              for (int j = 0; j < kBK / 32; ++j)
+                mma_f8(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+            }
             mma_commit(smem_u32(&tfull[acc]));
           }
           if (!ok) break;
@@ -310,19 +377,28 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
         }
       }
     }
+  }
   } else {
     // --------------------------------- epilogue ---------------------------------
+    if constexpr (W::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(W::kEpiRegs));
+    // Every warp of a column group runs the same sequence of group barriers whatever
+    // happens: a failed wait only turns off this warp's TMEM reads and stores for the rest
+    // of the unit, and the group leaves together at the next unit boundary.
     constexpr int HC = TT / kGroups;          // token columns of this warp's group
-    const int ew = warp - 2;                  // 0 .. kEpiWarps-1
+    // TMEM columns read per tcgen05.ld round trip and block (keeps the registers in bounds)
+    constexpr int CH = WB * HC <= 16 ? HC : (W::kSplitRegs ? 4 : 16 / WB);
+    const int ew = warp - W::kCtl;            // 0 .. kEpiWarps-1
     const int grp = ew >> 2;                  // column group
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int tid_g = (ew & 3) * 32 + lane;   // 0..127 within the group
-    float* my_sw = swt + grp * kMaxKB;
+    float* my_sw = swt + grp * WB * kMaxKB;   // [WB][kMaxKB]
+    float* my_sa = sa + grp * 2 * kSaChunk * HC;  // [2][kSaChunk][HC]
+    float* my_red = red + grp * 4 * HC;       // [4][HC] (kGateUpSilu)
     uint32_t kc = 0;
-    int staged_e = -1, staged_tt = -1;
-    float sw_next = 0.0f;
+    float sw_next[WB];
     bool have_next = false;
-    float acc[HC];
+    float acc[WB][HC];
+    const int nchunks = (KB + kSaChunk - 1) / kSaChunk;
     for (int u = u_begin; u < u_end; ++u) {
       int e, nb, tt, row0, rows;
       decode(u, e, nb, tt, row0, rows);
@@ -330,73 +406,129 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
       // previous unit's reads of the scale tables before they are rewritten
       if (named_bar_or(1 + grp, 128, s_abort)) break;
       // weight-block scales of this unit (prefetched during the previous unit)
-      if (tid_g < KB) my_sw[tid_g] = have_next ? sw_next : __ldg(p.w_s + ((int64_t)e * NB + nb) * KB + tid_g);
+      if (tid_g < KB) {
+#pragma unroll
+        for (int b = 0; b < WB; ++b)
+          my_sw[b * kMaxKB + tid_g] =
+              have_next ? sw_next[b] : __ldg(p.w_s + ((int64_t)e * NB + wblock(nb, b)) * KB + tid_g);
+      }
       have_next = false;
       if (u + 1 < u_end && tid_g < KB) {
         int e2, nb2, tt2, r02, rows2;
         decode(u + 1, e2, nb2, tt2, r02, rows2);
-        sw_next = __ldg(p.w_s + ((int64_t)e2 * NB + nb2) * KB + tid_g);
+#pragma unroll
+        for (int b = 0; b < WB; ++b) sw_next[b] = __ldg(p.w_s + ((int64_t)e2 * NB + wblock(nb2, b)) * KB + tid_g);
         have_next = true;
       }
-      // activation scales of the token tile, staged when the token tile changes
-      if (e != staged_e || tt != staged_tt) {
-        for (int i0 = tid_g; i0 < KB * HC; i0 += 128 * 8) {
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int i = i0 + q * 128;
-            v[q] = 0.0f;
-            if (i < KB * HC) {
-              const int c = i / KB, kb = i - c * KB;
-              const int r = grp * HC + c;
-              if (r < rows) v[q] = __ldg(p.a_s + (int64_t)(row0 + r) * KB + kb);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int i = i0 + q * 128;
-            if (i < KB * HC) {
-              const int c = i / KB, kb = i - c * KB;
-              sa[kb * TT + grp * HC + c] = v[q];
-            }
-          }
+      // activation scales of the token tile, kSaChunk K blocks at a time in two buffers,
+      // copied global -> shared by cp.async (no registers held): entry (kbl, c) of chunk ch
+      // is s_a[row0 + grp * HC + c][ch * kSaChunk + kbl], 0 for columns past the rows
+      auto sa_issue = [&](int ch) {
+        for (int i = tid_g; i < kSaChunk * HC; i += 128) {
+          const int kbl = i / HC, c = i - kbl * HC;
+          const int kb = ch * kSaChunk + kbl, r = grp * HC + c;
+          const bool valid = kb < KB && r < rows;
+          cp_async_4(smem_u32(my_sa + (ch & 1) * kSaChunk * HC + i),
+                     valid ? p.a_s + (int64_t)(row0 + r) * KB + kb : p.a_s, valid);
         }
-        staged_e = e;
-        staged_tt = tt;
+        cp_async_commit();
+      };
+      sa_issue(0);
+      if (nchunks > 1) {
+        sa_issue(1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
       }
       named_bar(1 + grp, 128);
 #pragma unroll
-      for (int c = 0; c < HC; ++c) acc[c] = 0.0f;
+      for (int b = 0; b < WB; ++b)
+#pragma unroll
+        for (int c = 0; c < HC; ++c) acc[b][c] = 0.0f;
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
-        const uint32_t b = kc % kAcc;
-        const int got = mbar_wait(smem_u32(&tfull[b]), (kc / kAcc) & 1, &s_abort) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const int ch = kb / kSaChunk, kbl = kb - ch * kSaChunk;
+        if (kbl == 0 && ch > 0) {
+          // chunk ch landed in buffer ch & 1; the barrier publishes it to the group and
+          // shows that chunk ch - 1 (buffer (ch + 1) & 1) is no longer read, so chunk
+          // ch + 1 may be copied there
+          cp_async_wait<0>();
+          named_bar(1 + grp, 128);
+          if (ch + 1 < nchunks) sa_issue(ch + 1);
+        }
+        const uint32_t ab = kc % kAcc;
+        if (ok) {
+          const int got = mbar_wait(smem_u32(&tfull[ab]), (kc / kAcc) & 1, &s_abort) ? 1 : 0;
+          ok = __all_sync(0xffffffffu, got) != 0;
+        }
+        if (!ok) continue;
         fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + b * TT + grp * HC;
-        float d[HC];
-        tmem_ld<HC>(taddr, d);
-        tmem_ld_wait();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
-        const float sw = my_sw[kb];
-        const float4* s4p = reinterpret_cast<const float4*>(sa + kb * TT + grp * HC);
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + ab * (WB * TT) + grp * HC;
+        float sw[WB];
 #pragma unroll
-        for (int c4 = 0; c4 < HC / 4; ++c4) {
-          const float4 s4 = s4p[c4];
-          acc[4 * c4 + 0] = fmaf(d[4 * c4 + 0], s4.x * sw, acc[4 * c4 + 0]);
-          acc[4 * c4 + 1] = fmaf(d[4 * c4 + 1], s4.y * sw, acc[4 * c4 + 1]);
-          acc[4 * c4 + 2] = fmaf(d[4 * c4 + 2], s4.z * sw, acc[4 * c4 + 2]);
-          acc[4 * c4 + 3] = fmaf(d[4 * c4 + 3], s4.w * sw, acc[4 * c4 + 3]);
+        for (int b = 0; b < WB; ++b) sw[b] = my_sw[b * kMaxKB + kb];
+        const float* sap = my_sa + (ch & 1) * kSaChunk * HC + kbl * HC;
+#pragma unroll
+        for (int c0 = 0; c0 < HC; c0 += CH) {
+          float d[WB][CH];
+#pragma unroll
+          for (int b = 0; b < WB; ++b) tmem_ld<CH>(taddr + b * TT + c0, d[b]);
+          tmem_ld_wait();
+          if (c0 + CH == HC) {
+            // every TMEM read of this accumulator is complete: hand it back to the MMA
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+          }
+          const float4* s4p = reinterpret_cast<const float4*>(sap + c0);
+#pragma unroll
+          for (int c4 = 0; c4 < CH / 4; ++c4) {
+            const float4 s4 = s4p[c4];
+#pragma unroll
+            for (int b = 0; b < WB; ++b) {
+              acc[b][c0 + 4 * c4 + 0] = fmaf(d[b][4 * c4 + 0], s4.x * sw[b], acc[b][c0 + 4 * c4 + 0]);
+              acc[b][c0 + 4 * c4 + 1] = fmaf(d[b][4 * c4 + 1], s4.y * sw[b], acc[b][c0 + 4 * c4 + 1]);
+              acc[b][c0 + 4 * c4 + 2] = fmaf(d[b][4 * c4 + 2], s4.z * sw[b], acc[b][c0 + 4 * c4 + 2]);
+              acc[b][c0 + 4 * c4 + 3] = fmaf(d[b][4 * c4 + 3], s4.w * sw[b], acc[b][c0 + 4 * c4 + 3]);
+            }
+          }
         }
       }
-      const int n = nb * kBM + 32 * quarter + lane;
-      if (ok && n < p.n) {
+      const int m = 32 * quarter + lane;  // row of this lane inside a 128-row weight block
+      if constexpr (MODE == kGateUpSilu) {
+        // a = silu(g) * u for intermediate column 128 nb + m; its group is this unit's
+        // 128 rows, so the group maximum is a reduction over the four lane quarters
+#pragma unroll
+        for (int c = 0; c < HC; ++c) acc[0][c] = silu_mul_1(acc[0][c], acc[1][c]);
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          const float mx = warp_max(fabsf(acc[0][c]));
+          if (lane == 0) my_red[quarter * HC + c] = mx;
+        }
+        named_bar(1 + grp, 128);
+        const int ld_q = p.n >> 1, ld_s = NBU;
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
           const int r = grp * HC + c;
-          if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[c];
+          const float amax = fmaxf(fmaxf(my_red[c], my_red[HC + c]), fmaxf(my_red[2 * HC + c], my_red[3 * HC + c]));
+          const float sc = div_rn(amax, kE4M3Max);
+          const uint8_t code = amax > 0.0f ? (uint8_t)(f2_to_e4m3x2(div_rn(acc[0][c], sc), 0.0f) & 0xFF) : (uint8_t)0;
+          if (ok && r < rows) {
+            p.q_out[(int64_t)(row0 + r) * ld_q + nb * kBM + m] = code;
+            if (quarter == 0 && lane == 0) p.s_out[(int64_t)(row0 + r) * ld_s + nb] = sc;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < WB; ++b) {
+          const int n = wblock(nb, b) * kBM + m;
+          if (ok && n < p.n) {
+#pragma unroll
+            for (int c = 0; c < HC; ++c) {
+              const int r = grp * HC + c;
+              if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[b][c];
+            }
+          }
         }
       }
     }
@@ -407,8 +539,7 @@ __global__ void __launch_bounds__(64 + 32 * kEpiWarps, 1)
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kAcc * TT < 32 ? 32 : kAcc * TT));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols));
   }
 }
 
@@ -464,8 +595,9 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int TT, int KBS>
+template <int TT, int KBS, int MODE>
 static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
+  using SM = tc::Smem<TT, KBS, MODE>;
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     *unsupported = 1;
@@ -476,8 +608,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     *unsupported = 1;
     return cudaSuccess;
   }
-  const size_t scale_bytes = (size_t)KB * TT * 4 + (size_t)tc::kGroups * tc::kMaxKB * 4;
-  const size_t fixed = 1024 /*align*/ + scale_bytes + (size_t)(3 * a.E + 2) * 4 + 8;
+  const size_t fixed = 1024 /*align*/ + SM::kSaBytes + SM::kSwBytes + SM::kRedBytes + (size_t)(3 * a.E + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
   int dev = 0;
@@ -486,42 +617,69 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   size_t max_smem = (dev >= 0 && dev < 64) ? budget[dev] : 0;
   if (max_smem == 0) {
     cudaFuncAttributes fattr;
-    if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT, KBS>) != cudaSuccess) return cudaErrorInvalidValue;
+    if (cudaFuncGetAttributes(&fattr, tc::tc_gemm_kernel<TT, KBS, MODE>) != cudaSuccess) return cudaErrorInvalidValue;
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     max_smem = (size_t)optin > fattr.sharedSizeBytes ? (size_t)optin - fattr.sharedSizeBytes : 0;
     if (dev >= 0 && dev < 64) budget[dev] = max_smem;
   }
-  constexpr int kAcc = tc::acc_count(TT);
+  using W = tc::Warps<TT, MODE>;
+  if constexpr (W::kSplitRegs) {
+    // the register split must fit the pool the block is launched with
+    static int regs[64] = {};
+    int nr = (dev >= 0 && dev < 64) ? regs[dev] : 0;
+    if (nr == 0) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, tc::tc_gemm_kernel<TT, KBS, MODE>) != cudaSuccess) return cudaErrorInvalidValue;
+      nr = fa.numRegs;
+      if (dev >= 0 && dev < 64) regs[dev] = nr;
+    }
+    if ((int64_t)nr * W::kThreads < (int64_t)W::kRegsNeeded) {
+      *unsupported = 1;
+      return cudaSuccess;
+    }
+  }
+  constexpr int kAcc = tc::acc_count(SM::kWB * TT);
   int stages = tc::kMaxStages;
-  while (stages > 2 && fixed + (size_t)stages * tc::Smem<TT, KBS>::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem)
-    --stages;
-  const size_t smem = fixed + (size_t)stages * tc::Smem<TT, KBS>::kStage + (2 * stages + 2 * kAcc) * 8;
+  while (stages > 2 && fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem) --stages;
+  const size_t smem = fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc) * 8;
   if (smem > max_smem) {
     *unsupported = 1;
     return cudaSuccess;
   }
-  // KBS > 1: weights as (128-byte K chunk, row, K block, expert) and tokens as (128-byte K
-  // chunk, row, K block), one box holding KBS K blocks. KBS = 1: rows of K bytes.
+  // KBS > 1 or two weight blocks: weights as (128-byte K chunk, row, K block, expert) and
+  // tokens as (128-byte K chunk, row, K block), one box holding KBS K blocks (kPair boxes
+  // are 256 rows high). kGateUpSilu splits the rows into (row in block, block j) and folds
+  // (gate/up half, expert) into one dimension of stride I*k, so one box brings gate block j
+  // and up block j. KBS = 1 with one block: rows of K bytes.
   CUtensorMap mw, ma;
-  if constexpr (KBS > 1) {
+  if constexpr (MODE == tc::kGateUpSilu) {
+    const uint64_t half = (uint64_t)a.n / 2;
+    const uint64_t wd[5] = {128, 128, (uint64_t)KB, half / 128, 2 * (uint64_t)a.E};
+    const uint64_t ws[4] = {(uint64_t)a.k, 128, 128 * (uint64_t)a.k, half * (uint64_t)a.k};
+    const uint32_t wb[5] = {128, 128, (uint32_t)KBS, 1, 2};
+    if (!encode_u8_tmap(&mw, a.w_q, 5, wd, ws, wb)) return cudaErrorInvalidValue;
+  } else if constexpr (MODE == tc::kPair || KBS > 1) {
     const uint64_t wd[4] = {128, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
     const uint64_t ws[3] = {(uint64_t)a.k, 128, (uint64_t)a.k * (uint64_t)a.n};
-    const uint32_t wb[4] = {128, 128, (uint32_t)KBS, 1};
-    const uint64_t ad[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
-    const uint64_t as[2] = {(uint64_t)a.k, 128};
-    const uint32_t ab[3] = {128, (uint32_t)TT, (uint32_t)KBS};
-    if (!encode_u8_tmap(&mw, a.w_q, 4, wd, ws, wb) || !encode_u8_tmap(&ma, a.a_q, 3, ad, as, ab))
-      return cudaErrorInvalidValue;
+    const uint32_t wb[4] = {128, (uint32_t)(128 * SM::kWB), (uint32_t)KBS, 1};
+    if (!encode_u8_tmap(&mw, a.w_q, 4, wd, ws, wb)) return cudaErrorInvalidValue;
   } else {
     const uint64_t wd[3] = {(uint64_t)a.k, (uint64_t)a.n, (uint64_t)a.E};
     const uint64_t ws[2] = {(uint64_t)a.k, (uint64_t)a.k * (uint64_t)a.n};
     const uint32_t wb[3] = {128, 128, 1};
+    if (!encode_u8_tmap(&mw, a.w_q, 3, wd, ws, wb)) return cudaErrorInvalidValue;
+  }
+  if constexpr (MODE != tc::kSingle || KBS > 1) {
+    const uint64_t ad[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
+    const uint64_t as[2] = {(uint64_t)a.k, 128};
+    const uint32_t ab[3] = {128, (uint32_t)TT, (uint32_t)KBS};
+    if (!encode_u8_tmap(&ma, a.a_q, 3, ad, as, ab)) return cudaErrorInvalidValue;
+  } else {
     const uint64_t ad[2] = {(uint64_t)a.k, (uint64_t)a.a_rows};
     const uint64_t as[1] = {(uint64_t)a.k};
     const uint32_t ab[2] = {128, (uint32_t)TT};
-    if (!encode_u8_tmap(&mw, a.w_q, 3, wd, ws, wb) || !encode_u8_tmap(&ma, a.a_q, 2, ad, as, ab))
-      return cudaErrorInvalidValue;
+    if (!encode_u8_tmap(&ma, a.a_q, 2, ad, as, ab)) return cudaErrorInvalidValue;
   }
   tc::Params p;
   p.offsets = a.offsets;
@@ -529,6 +687,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   p.w_s = a.w_s;
   p.out = a.out;
   p.ld_out = a.ld_out;
+  p.q_out = a.q_out;
+  p.s_out = a.s_out;
   p.a_rows = a.a_rows;
   p.n = (int)a.n;
   p.k = (int)a.k;
@@ -540,16 +700,31 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   // any earlier one on this device (the attribute is per function and device)
   static size_t granted[64] = {};
   if (dev >= 0 && dev < 64 && smem > granted[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     granted[dev] = smem;
   } else if (dev < 0 || dev >= 64) {
-    cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(tc::tc_gemm_kernel<TT, KBS>, dim3(sm_count()), dim3(64 + 32 * tc::kEpiWarps), smem, st, true, mw,
+  return launch_kernel(tc::tc_gemm_kernel<TT, KBS, MODE>, dim3(sm_count()), dim3(W::kThreads), smem, st, true, mw,
                        ma, p);
 }
+
+template <int MODE>
+static cudaError_t launch_mode(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
+  switch (a.tok_tile) {
+    case 16: return launch_tt<16, tc::kbs_for(16, MODE), MODE>(a, st, unsupported);
+    case 32: return launch_tt<32, tc::kbs_for(32, MODE), MODE>(a, st, unsupported);
+    case 64: return launch_tt<64, tc::kbs_for(64, MODE), MODE>(a, st, unsupported);
+    case 128: return launch_tt<128, tc::kbs_for(128, MODE), MODE>(a, st, unsupported);
+    default: *unsupported = 1; return cudaSuccess;
+  }
+}
+
+bool tc_gemm_pairs_ok(int64_t n, int64_t k) { return n % 256 == 0 && k % 128 == 0; }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
   *unsupported = 0;
@@ -560,15 +735,24 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupporte
     *unsupported = 1;
     return cudaSuccess;
   }
-  const bool ragged = a.k % 128 != 0;  // a partial last K block: one K block per stage
-  switch (a.tok_tile) {
-    case 16: return ragged ? launch_tt<16, 1>(a, st, unsupported) : launch_tt<16, tc::kbs_for(16)>(a, st, unsupported);
-    case 32: return ragged ? launch_tt<32, 1>(a, st, unsupported) : launch_tt<32, tc::kbs_for(32)>(a, st, unsupported);
-    case 64: return ragged ? launch_tt<64, 1>(a, st, unsupported) : launch_tt<64, tc::kbs_for(64)>(a, st, unsupported);
-    case 128:
-      return ragged ? launch_tt<128, 1>(a, st, unsupported) : launch_tt<128, tc::kbs_for(128)>(a, st, unsupported);
-    default: *unsupported = 1; return cudaSuccess;
+  // two weight blocks per unit need whole 256-row block pairs and whole K blocks
+  if (a.wblocks == 2 || a.silu) {
+    if (!tc_gemm_pairs_ok(a.n, a.k)) {
+      *unsupported = 1;
+      return cudaSuccess;
+    }
+    return a.silu ? launch_mode<tc::kGateUpSilu>(a, st, unsupported) : launch_mode<tc::kPair>(a, st, unsupported);
   }
+  if (a.k % 128 != 0) {  // a partial last K block: one K block per stage
+    switch (a.tok_tile) {
+      case 16: return launch_tt<16, 1, tc::kSingle>(a, st, unsupported);
+      case 32: return launch_tt<32, 1, tc::kSingle>(a, st, unsupported);
+      case 64: return launch_tt<64, 1, tc::kSingle>(a, st, unsupported);
+      case 128: return launch_tt<128, 1, tc::kSingle>(a, st, unsupported);
+      default: *unsupported = 1; return cudaSuccess;
+    }
+  }
+  return launch_mode<tc::kSingle>(a, st, unsupported);
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_tc_gemm)

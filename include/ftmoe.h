@@ -118,11 +118,15 @@ typedef struct ftmoe_routes {
 /* GEMM kernel choice. variant: 0 = automatic (SLOTS -> the HBM-streaming CUDA-core
  * kernel, GROUPED -> the tcgen05 tensor-core kernel), 1 = the streaming kernel,
  * 2 = the tcgen05 kernel. tok_tile: token columns per tensor-core tile, one of
- * 16/32/64/128; 0 = ftmoe_pick_tile's choice. */
+ * 16/32/64/128; 0 = ftmoe_pick_tile's choice. wblocks: 128-row weight blocks per
+ * tensor-core unit, sharing one token tile: 1, 2 (adjacent blocks; needs n % 256 == 0 and
+ * k % 128 == 0, else the request is treated as unsupported by the tcgen05 kernel), or 0 =
+ * automatic (2 from token tile 64 on where allowed, else 1). Results do not depend on it. */
 typedef struct ftmoe_tile {
   int32_t tok_tile;
   int32_t variant;
-  int32_t reserved[2];
+  int32_t wblocks;
+  int32_t reserved;
 } ftmoe_tile;
 
 const char* ftmoe_status_string(int status);
@@ -186,6 +190,22 @@ ftmoe_status ftmoe_grouped_gemm_gateup(const ftmoe_act* a, const ftmoe_routes* r
                                        const ftmoe_expert_bank* w, float* out, int64_t ld_out,
                                        const ftmoe_tile* tile, void* stream);
 
+/* Grouped gate/up GEMM with SiLU-and-mul and FP8 re-quantization in its epilogue: the
+ * composition ftmoe_grouped_gemm_gateup -> ftmoe_silu_mul (FP8) without the fp32 gate/up
+ * rows in between. Each tensor-core unit multiplies one token tile by gate block j (rows
+ * [128 j, 128 j + 128)) and up block j (rows [I + 128 j, ...)) of the expert, so it holds
+ * g and u of intermediate columns [128 j, 128 j + 128) -- one whole 1x128 group -- and
+ * writes a = silu(g) * u as e4m3 codes with the group scale amax / 448. The arithmetic
+ * (fp32 promotion per K block, silu, division, rounding) is that of the two separate calls,
+ * so codes and scales are bit-identical to theirs.
+ * FP8 only; routes must be FTMOE_ROUTES_GROUPED; w->n = 2I with I % 128 == 0 and
+ * w->k % 128 == 0 (else FTMOE_UNSUPPORTED). q_out uint8 [a->rows][I], scales_out float
+ * [a->rows][I / 128], dense; rows at or beyond offsets[E] are not touched. tile->variant
+ * and tile->wblocks are ignored. */
+ftmoe_status ftmoe_grouped_gemm_gateup_silu(const ftmoe_act* a, const ftmoe_routes* routes,
+                                            const ftmoe_expert_bank* w, uint8_t* q_out,
+                                            float* scales_out, const ftmoe_tile* tile, void* stream);
+
 /* SiLU-and-mul with re-quantization: for each row, a[i] = silu(g[i]) * u[i] with
  * g = gu[row, 0:inter], u = gu[row, inter:2*inter], silu(g) = g / (1 + exp(-g)) in fp32;
  * then a is quantized like ftmoe_quantize_act (FP8: q [rows][inter], scales float
@@ -218,8 +238,12 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
 /* ------------------------------------------------------------------------------------
  * Fused forward. Launch shapes depend only on the shape below, never on route content,
  * so one captured CUDA graph can be replayed while routes and inputs change in place.
- * path: 0 = automatic (the grouped tensor-core path at every batch size), 1 = route-slot
- * streaming path (FP8 only), 2 = grouped path.
+ * path: 0 = automatic, 1 = route-slot streaming path (FP8 only), 2 = grouped path with
+ * the separate SiLU-and-mul kernel, 3 = grouped path with SiLU-and-mul fused into the
+ * gate/up GEMM (ftmoe_grouped_gemm_gateup_silu; FP8, I % 128 == 0, H % 128 == 0).
+ * Automatic: the grouped path at every batch size, fused where the routes can reach at
+ * least 2048 (expert, gate/up block pair) units (min(T*topk, E) * I/128 >= 2048), else with
+ * the separate kernel. Paths 2 and 3 give bit-identical outputs.
  * ------------------------------------------------------------------------------------ */
 typedef struct ftmoe_moe_shape {
   int64_t tokens;     /* T */
@@ -251,7 +275,7 @@ typedef struct ftmoe_workspace_layout {
   size_t x_q, x_scales, x_gscale;            /* quantized token rows */
   size_t counts, offsets, dst2src, route2dst; /* segmenter (grouped path) */
   size_t rows_q, rows_scales;                /* gathered rows (grouped path) */
-  size_t gateup, gateup_bytes;               /* float gate/up output [R][2I] */
+  size_t gateup, gateup_bytes;               /* float gate/up output [R][2I] (not in path 3) */
   size_t act_q, act_q_bytes, act_scales, act_scales_bytes, act_gscale;
   size_t down, down_bytes;                   /* float down output [R][H] */
   size_t total;

@@ -78,12 +78,16 @@ def test_invalid_arguments_rejected_on_host(ft):
 
 
 def test_forward_workspace_layout(ft):
-    s = ft.moe_shape(8, 4096, 1024, 8, 64)
+    s = ft.moe_shape(8, 4096, 1024, 8, 64, path=2)
     n = ft.ftmoe_forward_workspace_bytes(s)
     lay = ft.ftmoe_forward_workspace_layout(s)
     assert lay["total"] == n
     R = 64
     assert lay["gateup_bytes"] == R * 2 * 1024 * 4 and lay["down_bytes"] == R * 4096 * 4
+    assert lay["act_q_bytes"] == R * 1024 and lay["act_scales_bytes"] == R * 8 * 4
+    fused = ft.ftmoe_forward_workspace_layout(ft.moe_shape(8, 4096, 1024, 8, 64, path=3))
+    assert fused["gateup"] == 0 and fused["gateup_bytes"] == 0  # no fp32 gate/up rows
+    assert fused["total"] == n - R * 2 * 1024 * 4
     for key in ("x_q", "x_scales", "gateup", "act_q", "act_scales", "down"):
         assert lay[key] % 256 == 0
     assert lay["rows_q"] > 0  # eight tokens take the grouped path: gather buffers
@@ -111,3 +115,20 @@ def test_forward_rejects_inconsistent_banks(ft):
     assert ft.lib().ftmoe_moe_forward(ctypes.byref(args), ctypes.c_void_p(256), 1 << 30, None) == ft.FTMOE_INVALID_ARG
     args.w_down.num_experts = 4
     assert ft.lib().ftmoe_moe_forward(ctypes.byref(args), ctypes.c_void_p(256), 16, None) == ft.FTMOE_WORKSPACE_TOO_SMALL
+
+
+def test_automatic_forward_path_choice(ft):
+    # SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up buffer) where
+    # min(T * topk, E) * I / 128 >= 2048, the separate kernel below and for NVFP4
+    lay = ft.ftmoe_forward_workspace_layout
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256))["gateup_bytes"] == 0
+    assert lay(ft.moe_shape(256, 7168, 2048, 6, 256))["gateup_bytes"] == 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=3))["gateup_bytes"] == 0
+    assert lay(ft.moe_shape(1, 4096, 1024, 8, 64))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(1, 2048, 768, 8, 8))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, fmt=ft.FMT_NVFP4))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=2))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(1, 2048, 768, 8, 8, path=3))["gateup_bytes"] == 0
+    with pytest.raises(ft.FtmoeError):
+        lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4))

@@ -30,7 +30,7 @@ def _check(prob, out, ids=None, weights=None, x=None):
     return prob.check(out, ids=ids, weights=weights, x=x)
 
 
-@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("path", [0, 1, 2, 3])
 def test_decode_2048_768_two_of_eight_active(ft, path):
     # hidden 2048, intermediate 768, 8 resident experts, top-k 8, 6 of 8 slots -1
     p = Problem(1, 2048, 768, 8, 8, seed=0xF7E00001, active=2)
@@ -40,11 +40,12 @@ def test_decode_2048_768_two_of_eight_active(ft, path):
     _check(p, out)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 @pytest.mark.parametrize("T", [1, 8])
 @pytest.mark.parametrize("active", [8, 4, 2, 0])
 def test_decode_4096_1024_sweep(ft, T, active, path):
-    # path 1: route-slot streaming kernel; path 2: segment + gather + tcgen05 grouped GEMMs
+    # path 1: route-slot streaming kernel; path 2: segment + gather + tcgen05 grouped GEMMs;
+    # path 3: the same with SiLU-and-mul fused into the gate/up GEMM
     p = Problem(T, 4096, 1024, 64, 8, seed=0xF7E00002, active=active)
     out, ws, shape = p.forward(path=path)
     torch.cuda.synchronize()
@@ -66,7 +67,7 @@ def _poison(ws, lay):
             region.fill_(0xFF)
 
 
-@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (8, 2)])
+@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (8, 2), (8, 3)])
 def test_graph_replay_with_poisoned_intermediates(ft, T, path):
     H, I, E, k = 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=8)
@@ -103,8 +104,8 @@ def test_graph_replay_with_poisoned_intermediates(ft, T, path):
         torch.cuda.synchronize()
         _check(p, out, ids=ids, weights=w, x=x)
         assert not torch.any(torch.isnan(out.float()))
-        if path == 2:
-            continue  # grouped path: inactive routes have no rows at all
+        if path != 1:
+            continue  # grouped paths: inactive routes have no rows at all
         # route-slot path: exact zeros in the gate/up, activation and down rows of inactive routes
         R = T * k
         gu = ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(R, 2 * I)
@@ -120,7 +121,7 @@ def test_graph_replay_with_poisoned_intermediates(ft, T, path):
         assert not torch.any(torch.isnan(out.float()))
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_negative_slots_equal_clamped_zero_weight_path(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=2)
@@ -134,7 +135,7 @@ def test_negative_slots_equal_clamped_zero_weight_path(ft, path):
     assert torch.equal(out_new.view(torch.int16), out_old.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_all_inactive_and_empty_bank_use(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=0)

@@ -106,10 +106,11 @@ def test_prefill_forward_medium(ft):
     p = Problem(T, H, I, E, k, seed=0xF7E00004)
     ids = synth.routes(T, k, E, 3, active_per_token=[6, 5, 4, 6] * 24, device=DEV)
     w = torch.where(ids >= 0, p.w, torch.full_like(p.w, float("nan")))
-    for tok_tile in (0, 16, 128):
-        out, _, _ = p.forward(path=2, tok_tile=tok_tile, ids=ids, weights=w)
-        torch.cuda.synchronize()
-        p.check(out, ids=ids, weights=w)
+    for path in (2, 3):
+        for tok_tile in (0, 16, 128):
+            out, _, _ = p.forward(path=path, tok_tile=tok_tile, ids=ids, weights=w)
+            torch.cuda.synchronize()
+            p.check(out, ids=ids, weights=w)
     # the route-slot streaming path gives the same answer within tolerance
     out_d, _, _ = p.forward(path=1, ids=ids, weights=w)
     torch.cuda.synchronize()
