@@ -234,12 +234,15 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
 // 86 us); the route-slot path stays available as path 1.
 bool use_grouped(const ftmoe_moe_shape* s) { return s->path != 1; }
 
-// Minimum number of (expert, gate/up block pair) units, counted for the most distinct
-// experts the routes can reach, for the automatic path to fuse SiLU-and-mul into the
-// gate/up GEMM. A fused unit is twice as large as a one-block unit, so with few units per
-// SM the CTAs finish unevenly: measured on GB300, eight decode tokens (64 experts x 8
-// pairs) ran 126.9 us fused against 122.9 us separate, while the 256-expert prefill
-// (4096 pairs) gained 2-4% at 1,536 and 6,144 routes and broke even at 24,576.
+// When the automatic path fuses SiLU-and-mul into the gate/up GEMM. Measured on GB300:
+//  - A fused unit is twice as large as a one-block unit, so with few units per SM the CTAs
+//    finish unevenly: eight decode tokens (64 experts x 8 gate/up block pairs) ran 126.9 us
+//    fused against 122.9 us separate. Hence a minimum of kFusedMinUnits units, counted for
+//    the most distinct experts the routes can reach.
+//  - At token tile 128 only two accumulator pairs fit in TMEM, so the MMA waits while the
+//    epilogue forms and re-quantizes a unit's SiLU outputs: at 24,576 routes (256 experts)
+//    fused ran 3193 us, separate 3136 us. At tiles 16 and 32 (1,536 and 6,144 routes) fused
+//    won, 1667 vs 1698 us and 1932 vs 2031 us.
 constexpr int64_t kFusedMinUnits = 2048;
 
 bool use_fused(const ftmoe_moe_shape* s) {
@@ -247,6 +250,8 @@ bool use_fused(const ftmoe_moe_shape* s) {
   if (s->path != 0 || s->format != FTMOE_FMT_FP8) return false;
   if (!tc_gemm_pairs_ok(2 * s->inter, s->hidden)) return false;
   const int64_t R = s->tokens * s->topk;
+  const int tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, s->num_experts);
+  if (tile > 64) return false;
   const int64_t experts = R < s->num_experts ? R : s->num_experts;
   return experts * (s->inter / 128) >= kFusedMinUnits;
 }

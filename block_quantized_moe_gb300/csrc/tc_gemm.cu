@@ -103,15 +103,15 @@ __host__ __device__ constexpr int kbs_for(int tt, int mode) {
 }
 
 // Warp roles. Warp 0 issues TMA, warp 1 issues MMAs, the last kEpiWarps warps promote.
-// Units with two weight blocks at token tile 128 hold 64 fp32 accumulators per epilogue
-// thread; those kernels add two idle warps so that warps 0-3 form a warpgroup that gives
+// Units with two weight blocks from token tile 64 on hold 2 x TT/4 fp32 accumulators (32
+// or 64) per epilogue thread; those kernels add two idle warps so that warps 0-3 form a warpgroup that gives
 // registers back (setmaxnreg.dec to kCtlRegs) to the four epilogue warpgroups
 // (setmaxnreg.inc to kEpiRegs). The launch pool is threads x the kernel's register count;
 // the host checks kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps against it before launching,
 // since an increase the pool cannot cover would never complete.
 template <int TT, int MODE>
 struct Warps {
-  static constexpr bool kSplitRegs = TT == 128 && wb_of(MODE) == 2;
+  static constexpr bool kSplitRegs = TT >= 64 && wb_of(MODE) == 2;
   static constexpr int kCtl = kSplitRegs ? 4 : 2;
   static constexpr int kThreads = 32 * (kCtl + kEpiWarps);
   static constexpr int kCtlRegs = 56, kEpiRegs = 104;
@@ -132,11 +132,15 @@ struct Smem {
   static __device__ __forceinline__ uint32_t w_off(int b, int h) {
     return (uint32_t)((MODE == kPair ? h * kWB + b : b * KBS + h) * kSubW);
   }
-  // epilogue tables (bytes): activation scales [kGroups][2][kSaChunk][TT / kGroups],
-  // weight-block scales [kGroups][kWB][kMaxKB], SiLU group maxima [kGroups][4][TT / kGroups]
+  // epilogue tables (bytes): activation scales [kGroups][2][kSaChunk][TT / kGroups], their
+  // products with the weight-block scales [kGroups][2][kSaChunk][kWB][TT / kGroups], SiLU
+  // group maxima per lane quarter and group scales [kGroups][5][TT / kGroups], then the
+  // weight-block scales of the unit
+  // [kGroups][kWB][K blocks] (sw_bytes: sized by the launch's K)
   static constexpr int kSaBytes = 2 * kSaChunk * TT * 4;
-  static constexpr int kSwBytes = kGroups * kWB * kMaxKB * 4;
-  static constexpr int kRedBytes = MODE == kGateUpSilu ? 4 * TT * 4 : 0;
+  static constexpr int kProdBytes = 2 * kSaChunk * kWB * TT * 4;
+  static __host__ __device__ int sw_bytes(int kb_count) { return ((kGroups * kWB * kb_count + 3) & ~3) * 4; }
+  static constexpr int kRedBytes = MODE == kGateUpSilu ? 5 * TT * 4 : 0;
 };
 
 // Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the epilogue tables,
@@ -152,9 +156,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   const int S = p.stages;
   uint8_t* tiles = smem;
   float* sa = reinterpret_cast<float*>(smem + (size_t)S * SM::kStage);
-  float* swt = sa + SM::kSaBytes / 4;
-  float* red = swt + SM::kSwBytes / 4;
-  int* cum = reinterpret_cast<int*>(red + SM::kRedBytes / 4);  // [E+2] unit prefix
+  float* prod = sa + SM::kSaBytes / 4;
+  float* red = prod + SM::kProdBytes / 4;
+  float* swt = red + SM::kRedBytes / 4;
+  int* cum = reinterpret_cast<int*>(swt + SM::sw_bytes(p.kb_count) / 4);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
   int* seg_hi = seg_lo + p.E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
@@ -386,14 +391,15 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     // of the unit, and the group leaves together at the next unit boundary.
     constexpr int HC = TT / kGroups;          // token columns of this warp's group
     // TMEM columns read per tcgen05.ld round trip and block (keeps the registers in bounds)
-    constexpr int CH = WB * HC <= 16 ? HC : (W::kSplitRegs ? 4 : 16 / WB);
+    constexpr int CH = WB * HC <= 16 ? HC : (W::kSplitRegs ? (TT == 128 ? 4 : 8) : 16 / WB);
     const int ew = warp - W::kCtl;            // 0 .. kEpiWarps-1
     const int grp = ew >> 2;                  // column group
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int tid_g = (ew & 3) * 32 + lane;   // 0..127 within the group
-    float* my_sw = swt + grp * WB * kMaxKB;   // [WB][kMaxKB]
+    float* my_sw = swt + grp * WB * KB;       // [WB][KB]
     float* my_sa = sa + grp * 2 * kSaChunk * HC;  // [2][kSaChunk][HC]
-    float* my_red = red + grp * 4 * HC;       // [4][HC] (kGateUpSilu)
+    float* my_prod = prod + grp * 2 * kSaChunk * WB * HC;  // [2][kSaChunk][WB][HC]
+    float* my_red = red + grp * 5 * HC;       // [4][HC] maxima, [HC] scales (kGateUpSilu)
     uint32_t kc = 0;
     float sw_next[WB];
     bool have_next = false;
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       if (tid_g < KB) {
 #pragma unroll
         for (int b = 0; b < WB; ++b)
-          my_sw[b * kMaxKB + tid_g] =
+          my_sw[b * KB + tid_g] =
               have_next ? sw_next[b] : __ldg(p.w_s + ((int64_t)e * NB + wblock(nb, b)) * KB + tid_g);
       }
       have_next = false;
@@ -433,6 +439,18 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         }
         cp_async_commit();
       };
+      // products s_a * s_w of chunk ch (buffer ch & 1), one per (K block, weight block,
+      // column): the same for all 128 rows, so computed once here instead of per element
+      auto prod_fill = [&](int ch) {
+        const float* src = my_sa + (ch & 1) * kSaChunk * HC;
+        float* dst = my_prod + (ch & 1) * kSaChunk * WB * HC;
+        for (int i = tid_g; i < kSaChunk * WB * HC; i += 128) {
+          const int kbl = i / (WB * HC), rem = i - kbl * (WB * HC);
+          const int b = rem / HC, c = rem - b * HC;
+          const int kb = ch * kSaChunk + kbl;
+          dst[i] = kb < KB ? src[kbl * HC + c] * my_sw[b * KB + kb] : 0.0f;
+        }
+      };
       sa_issue(0);
       if (nchunks > 1) {
         sa_issue(1);
@@ -440,6 +458,8 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       } else {
         cp_async_wait<0>();
       }
+      named_bar(1 + grp, 128);
+      prod_fill(0);
       named_bar(1 + grp, 128);
 #pragma unroll
       for (int b = 0; b < WB; ++b)
@@ -449,10 +469,12 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       for (int kb = 0; kb < KB; ++kb, ++kc) {
         const int ch = kb / kSaChunk, kbl = kb - ch * kSaChunk;
         if (kbl == 0 && ch > 0) {
-          // chunk ch landed in buffer ch & 1; the barrier publishes it to the group and
-          // shows that chunk ch - 1 (buffer (ch + 1) & 1) is no longer read, so chunk
-          // ch + 1 may be copied there
+          // chunk ch landed in scale buffer ch & 1; the first barrier publishes it and shows
+          // that chunk ch - 2 (product buffer ch & 1) is no longer read, the second publishes
+          // the products and shows that scale buffer (ch + 1) & 1 (chunk ch - 1) was used
           cp_async_wait<0>();
+          named_bar(1 + grp, 128);
+          prod_fill(ch);
           named_bar(1 + grp, 128);
           if (ch + 1 < nchunks) sa_issue(ch + 1);
         }
@@ -464,10 +486,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         if (!ok) continue;
         fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + ab * (WB * TT) + grp * HC;
-        float sw[WB];
-#pragma unroll
-        for (int b = 0; b < WB; ++b) sw[b] = my_sw[b * kMaxKB + kb];
-        const float* sap = my_sa + (ch & 1) * kSaChunk * HC + kbl * HC;
+        const float* pp = my_prod + ((ch & 1) * kSaChunk + kbl) * WB * HC;
 #pragma unroll
         for (int c0 = 0; c0 < HC; c0 += CH) {
           float d[WB][CH];
@@ -480,16 +499,16 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
           }
-          const float4* s4p = reinterpret_cast<const float4*>(sap + c0);
 #pragma unroll
-          for (int c4 = 0; c4 < CH / 4; ++c4) {
-            const float4 s4 = s4p[c4];
+          for (int b = 0; b < WB; ++b) {
+            const float4* p4 = reinterpret_cast<const float4*>(pp + b * HC + c0);
 #pragma unroll
-            for (int b = 0; b < WB; ++b) {
-              acc[b][c0 + 4 * c4 + 0] = fmaf(d[b][4 * c4 + 0], s4.x * sw[b], acc[b][c0 + 4 * c4 + 0]);
-              acc[b][c0 + 4 * c4 + 1] = fmaf(d[b][4 * c4 + 1], s4.y * sw[b], acc[b][c0 + 4 * c4 + 1]);
-              acc[b][c0 + 4 * c4 + 2] = fmaf(d[b][4 * c4 + 2], s4.z * sw[b], acc[b][c0 + 4 * c4 + 2]);
-              acc[b][c0 + 4 * c4 + 3] = fmaf(d[b][4 * c4 + 3], s4.w * sw[b], acc[b][c0 + 4 * c4 + 3]);
+            for (int c4 = 0; c4 < CH / 4; ++c4) {
+              const float4 s4 = p4[c4];
+              acc[b][c0 + 4 * c4 + 0] = fmaf(d[b][4 * c4 + 0], s4.x, acc[b][c0 + 4 * c4 + 0]);
+              acc[b][c0 + 4 * c4 + 1] = fmaf(d[b][4 * c4 + 1], s4.y, acc[b][c0 + 4 * c4 + 1]);
+              acc[b][c0 + 4 * c4 + 2] = fmaf(d[b][4 * c4 + 2], s4.z, acc[b][c0 + 4 * c4 + 2]);
+              acc[b][c0 + 4 * c4 + 3] = fmaf(d[b][4 * c4 + 3], s4.w, acc[b][c0 + 4 * c4 + 3]);
             }
           }
         }
@@ -500,10 +519,38 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         // 128 rows, so the group maximum is a reduction over the four lane quarters
 #pragma unroll
         for (int c = 0; c < HC; ++c) acc[0][c] = silu_mul_1(acc[0][c], acc[1][c]);
+        {
+          // column maxima of |a| over the warp's 32 rows by a butterfly transpose-reduce:
+          // each exchange halves the columns a lane keeps, until lane l holds the maximum of
+          // column l / (32 / HC) (HC - 1 + 5 - log2(HC) shuffles instead of 5 per column)
+          float v[HC];
 #pragma unroll
-        for (int c = 0; c < HC; ++c) {
-          const float mx = warp_max(fabsf(acc[0][c]));
-          if (lane == 0) my_red[quarter * HC + c] = mx;
+          for (int c = 0; c < HC; ++c) v[c] = fabsf(acc[0][c]);
+#pragma unroll
+          for (int st = 0; st < 5; ++st) {
+            const int o = 16 >> st;
+            constexpr int kLog = HC >= 32 ? 5 : HC >= 16 ? 4 : HC >= 8 ? 3 : HC >= 4 ? 2 : HC >= 2 ? 1 : 0;
+            if (st < kLog) {
+              const int half = HC >> (st + 1);
+              const bool upper = (lane & o) != 0;
+#pragma unroll
+              for (int i = 0; i < half; ++i) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+              }
+            } else {
+              v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+            }
+          }
+          if ((lane & (32 / HC - 1)) == 0) my_red[quarter * HC + lane / (32 / HC)] = v[0];
+        }
+        named_bar(1 + grp, 128);
+        // one thread per column: the group scale amax / 448
+        if (tid_g < HC) {
+          const int c = tid_g;
+          const float amax = fmaxf(fmaxf(my_red[c], my_red[HC + c]), fmaxf(my_red[2 * HC + c], my_red[3 * HC + c]));
+          my_red[4 * HC + c] = div_rn(amax, kE4M3Max);
         }
         named_bar(1 + grp, 128);
         const int ld_q = p.n >> 1, ld_s = NBU;
@@ -511,7 +558,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         for (int c = 0; c < HC; ++c) {
           const int r = grp * HC + c;
           const float amax = fmaxf(fmaxf(my_red[c], my_red[HC + c]), fmaxf(my_red[2 * HC + c], my_red[3 * HC + c]));
-          const float sc = div_rn(amax, kE4M3Max);
+          const float sc = my_red[4 * HC + c];
           const uint8_t code = amax > 0.0f ? (uint8_t)(f2_to_e4m3x2(div_rn(acc[0][c], sc), 0.0f) & 0xFF) : (uint8_t)0;
           if (ok && r < rows) {
             p.q_out[(int64_t)(row0 + r) * ld_q + nb * kBM + m] = code;
@@ -608,7 +655,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     *unsupported = 1;
     return cudaSuccess;
   }
-  const size_t fixed = 1024 /*align*/ + SM::kSaBytes + SM::kSwBytes + SM::kRedBytes + (size_t)(3 * a.E + 2) * 4 + 8;
+  const size_t fixed = 1024 /*align*/ + SM::kSaBytes + SM::kProdBytes + SM::kRedBytes + SM::sw_bytes(KB) +
+                       (size_t)(3 * a.E + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
   int dev = 0;

@@ -118,11 +118,14 @@ def test_forward_rejects_inconsistent_banks(ft):
 
 
 def test_automatic_forward_path_choice(ft):
-    # SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up buffer) where
-    # min(T * topk, E) * I / 128 >= 2048, the separate kernel below and for NVFP4
+    # SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up buffer) where the token
+    # tile is at most 64 and min(T * topk, E) * I / 128 >= 2048; the separate kernel
+    # otherwise and for NVFP4
     lay = ft.ftmoe_forward_workspace_layout
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64))["gateup_bytes"] > 0
-    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256))["gateup_bytes"] == 0
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256))["gateup_bytes"] > 0       # tile 128
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, tok_tile=32))["gateup_bytes"] == 0
+    assert lay(ft.moe_shape(1024, 7168, 2048, 6, 256))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(256, 7168, 2048, 6, 256))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=3))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(1, 4096, 1024, 8, 64))["gateup_bytes"] > 0
