@@ -15,8 +15,11 @@ __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
     const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
     const int32_t* __restrict__ rows_dev, uint8_t* __restrict__ q, float* __restrict__ s,
     int64_t ng) {
-  pdl_wait();  // the predecessor's outputs are complete from here on
+  // The down GEMM that follows reads nothing before its own wait that the gate/up GEMM
+  // writes (only the segment offsets, complete long before), so it may start -- and begin
+  // streaming its weights -- while this kernel still waits for the gate/up GEMM to finish.
   pdl_trigger();
+  pdl_wait();  // the predecessor's outputs are complete from here on
   int64_t limit = rows;
   if (rows_dev != nullptr) {
     const int64_t d = *rows_dev;

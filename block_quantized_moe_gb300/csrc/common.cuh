@@ -25,8 +25,10 @@ __device__ __forceinline__ void raise_error(unsigned int bit) { atomicOr(&g_err_
 // Programmatic dependent launch. Inside the fused forward a kernel may start while its
 // predecessor is still running; it waits here before it reads anything the predecessor
 // writes (or writes anything it reads), and only then lets its own dependent start. So when
-// a kernel starts, every kernel two or more launches earlier has completed. Outside such a
-// launch both are no-ops.
+// a kernel starts, every kernel two or more launches earlier has completed -- with one
+// exception: the FP8 SiLU-and-mul kernel lets the down GEMM start first, and the down GEMM
+// reads nothing the gate/up GEMM writes before its own wait. Outside such a launch both are
+// no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -405,11 +405,44 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     bool have_next = false;
     float acc[WB][HC];
     const int nchunks = (KB + kSaChunk - 1) / kSaChunk;
+    // Activation scales travel in chunks of kSaChunk K blocks, copied global -> shared by
+    // cp.async (no registers held) into two buffers that alternate along the whole sequence
+    // of (unit, chunk) pairs of this CTA: entry (kbl, c) of a chunk is
+    // s_a[row0 + grp * HC + c][ch * kSaChunk + kbl], 0 for columns past the tile's rows.
+    // While a chunk is in use the next one is in flight, the next unit's first chunk included.
+    auto sa_issue = [&](int r0, int nrows, int ch, int buf) {
+      for (int i = tid_g; i < kSaChunk * HC; i += 128) {
+        const int kbl = i / HC, c = i - kbl * HC;
+        const int kb = ch * kSaChunk + kbl, r = grp * HC + c;
+        const bool valid = kb < KB && r < nrows;
+        cp_async_4(smem_u32(my_sa + buf * kSaChunk * HC + i), valid ? p.a_s + (int64_t)(r0 + r) * KB + kb : p.a_s,
+                   valid);
+      }
+      cp_async_commit();
+    };
+    // products s_a * s_w of the chunk in buffer buf, one per (K block, weight block,
+    // column): the same for all 128 rows, so formed once here instead of per element
+    auto prod_fill = [&](int ch, int buf) {
+      const float* src = my_sa + buf * kSaChunk * HC;
+      float* dst = my_prod + buf * kSaChunk * WB * HC;
+      for (int i = tid_g; i < kSaChunk * WB * HC; i += 128) {
+        const int kbl = i / (WB * HC), rem = i - kbl * (WB * HC);
+        const int b = rem / HC, c = rem - b * HC;
+        const int kb = ch * kSaChunk + kbl;
+        dst[i] = kb < KB ? src[kbl * HC + c] * my_sw[b * KB + kb] : 0.0f;
+      }
+    };
+    uint32_t gch = 0;  // chunks begun so far; chunk gch uses buffer gch & 1
+    if (u_begin < u_end) {
+      int e0, nb0, tt0, r00, rows0;
+      decode(u_begin, e0, nb0, tt0, r00, rows0);
+      sa_issue(r00, rows0, 0, 0);
+    }
     for (int u = u_begin; u < u_end; ++u) {
       int e, nb, tt, row0, rows;
       decode(u, e, nb, tt, row0, rows);
       // all warps of the group leave together on an abort; the barrier also orders the
-      // previous unit's reads of the scale tables before they are rewritten
+      // previous unit's reads of the weight-scale table before it is rewritten
       if (named_bar_or(1 + grp, 128, s_abort)) break;
       // weight-block scales of this unit (prefetched during the previous unit)
       if (tid_g < KB) {
@@ -426,41 +459,6 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         for (int b = 0; b < WB; ++b) sw_next[b] = __ldg(p.w_s + ((int64_t)e2 * NB + wblock(nb2, b)) * KB + tid_g);
         have_next = true;
       }
-      // activation scales of the token tile, kSaChunk K blocks at a time in two buffers,
-      // copied global -> shared by cp.async (no registers held): entry (kbl, c) of chunk ch
-      // is s_a[row0 + grp * HC + c][ch * kSaChunk + kbl], 0 for columns past the rows
-      auto sa_issue = [&](int ch) {
-        for (int i = tid_g; i < kSaChunk * HC; i += 128) {
-          const int kbl = i / HC, c = i - kbl * HC;
-          const int kb = ch * kSaChunk + kbl, r = grp * HC + c;
-          const bool valid = kb < KB && r < rows;
-          cp_async_4(smem_u32(my_sa + (ch & 1) * kSaChunk * HC + i),
-                     valid ? p.a_s + (int64_t)(row0 + r) * KB + kb : p.a_s, valid);
-        }
-        cp_async_commit();
-      };
-      // products s_a * s_w of chunk ch (buffer ch & 1), one per (K block, weight block,
-      // column): the same for all 128 rows, so computed once here instead of per element
-      auto prod_fill = [&](int ch) {
-        const float* src = my_sa + (ch & 1) * kSaChunk * HC;
-        float* dst = my_prod + (ch & 1) * kSaChunk * WB * HC;
-        for (int i = tid_g; i < kSaChunk * WB * HC; i += 128) {
-          const int kbl = i / (WB * HC), rem = i - kbl * (WB * HC);
-          const int b = rem / HC, c = rem - b * HC;
-          const int kb = ch * kSaChunk + kbl;
-          dst[i] = kb < KB ? src[kbl * HC + c] * my_sw[b * KB + kb] : 0.0f;
-        }
-      };
-      sa_issue(0);
-      if (nchunks > 1) {
-        sa_issue(1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      named_bar(1 + grp, 128);
-      prod_fill(0);
-      named_bar(1 + grp, 128);
 #pragma unroll
       for (int b = 0; b < WB; ++b)
 #pragma unroll
@@ -468,16 +466,25 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
         const int ch = kb / kSaChunk, kbl = kb - ch * kSaChunk;
-        if (kbl == 0 && ch > 0) {
-          // chunk ch landed in scale buffer ch & 1; the first barrier publishes it and shows
-          // that chunk ch - 2 (product buffer ch & 1) is no longer read, the second publishes
-          // the products and shows that scale buffer (ch + 1) & 1 (chunk ch - 1) was used
+        if (kbl == 0) {
+          // Chunk gch has landed once this thread's copies are done; the first barrier
+          // publishes it and shows that the products of chunk gch - 2 (same buffer) and the
+          // scales of chunk gch - 1 are no longer read, and that this unit's weight scales are
+          // in place; the second publishes the products. Then chunk gch + 1 goes in flight.
           cp_async_wait<0>();
           named_bar(1 + grp, 128);
-          prod_fill(ch);
+          prod_fill(ch, gch & 1);
           named_bar(1 + grp, 128);
-          if (ch + 1 < nchunks) sa_issue(ch + 1);
+          if (ch + 1 < nchunks) {
+            sa_issue(row0, rows, ch + 1, (gch + 1) & 1);
+          } else if (u + 1 < u_end) {
+            int e2, nb2, tt2, r02, rows2;
+            decode(u + 1, e2, nb2, tt2, r02, rows2);
+            sa_issue(r02, rows2, 0, (gch + 1) & 1);
+          }
+          ++gch;
         }
+        const int buf = (gch - 1) & 1;
         const uint32_t ab = kc % kAcc;
         if (ok) {
           const int got = mbar_wait(smem_u32(&tfull[ab]), (kc / kAcc) & 1, &s_abort) ? 1 : 0;
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         if (!ok) continue;
         fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + ab * (WB * TT) + grp * HC;
-        const float* pp = my_prod + ((ch & 1) * kSaChunk + kbl) * WB * HC;
+        const float* pp = my_prod + (buf * kSaChunk + kbl) * WB * HC;
 #pragma unroll
         for (int c0 = 0; c0 < HC; c0 += CH) {
           float d[WB][CH];
@@ -579,6 +586,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         }
       }
     }
+    cp_async_wait<0>();  // a copy left in flight by an abort lands before the CTA exits
   }
 
   fence_before();
