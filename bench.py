@@ -328,8 +328,11 @@ class MoeWorkload:
         self.w_in = torch.empty(T, k, dtype=torch.float32, device=device)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         # kernels per forward: quantize, [segment, gather,] gate/up, SiLU-and-mul, down, combine;
-        # each NVFP4 quantizer adds an amax pass and the tensor-scale conversion
-        self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) +
+        # FP8 on the grouped path quantizes and segments in one launch, and the fused path has
+        # no SiLU-and-mul launch; each NVFP4 quantizer adds an amax pass and the tensor-scale
+        # conversion
+        self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) -
+                                  (1 if self.grouped and self.fmt == "fp8" else 0) +
                                   (4 if self.fmt == "nvfp4" else 0))
 
     # algorithmic bytes/flops of one forward on route set i
@@ -763,23 +766,26 @@ def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
         M.moe_forward(x[t:t + 1], ids[t:t + 1], w[t:t + 1], bg, bd, fmt="nvfp4")
 
 
-def cpu_baseline(name, budget_s=20.0, repeats=None):
-    """Time the oracle's forward on a bounded sample of tokens; scale to one full call."""
+def cpu_baseline(name, budget_s=20.0, min_s=10.0):
+    """Time the oracle's forward token by token on the first (at most 8) tokens of a call,
+    in repeated passes until at least min_s of CPU work (stopping at budget_s); scale the
+    time per token to one full call."""
     T_full = WORKLOADS[name][0]
-    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(name, max_tokens=min(T_full, 4))
+    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(name, max_tokens=min(T_full, 8))
+    n = ids.shape[0]
     T = T_full
     t0 = time.perf_counter()
     done = 0
-    toks = []
-    while done < ids.shape[0] and (time.perf_counter() - t0) < budget_s:
-        _oracle_token(M, x, ids, w, bg, bd, fmt, done)
-        toks.append(done)
+    while True:
+        _oracle_token(M, x, ids, w, bg, bd, fmt, done % n)
         done += 1
-    el = time.perf_counter() - t0
-    per_call = el / len(toks) * T
+        el = time.perf_counter() - t0
+        if el >= budget_s or (el >= min_s and done % n == 0):
+            break
+    per_call = el / done * T
     return {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
-            "sample": f"{len(toks)} of {T} tokens of one call (numpy float64, single thread), "
-                      f"{el:.1f} s of CPU work, scaled to the full call"}
+            "sample": f"{done} token forwards over the first {n} of {T} tokens of one call (numpy float64, "
+                      f"single thread), {el:.1f} s of CPU work, scaled to the full call"}
 
 
 def _gather_oracle_problem(name, seed=0xF7E00003):

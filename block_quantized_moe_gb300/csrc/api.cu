@@ -468,8 +468,20 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   memset(&tile, 0, sizeof(tile));
   tile.tok_tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, (int32_t)E);
 
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.l.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.l.offsets);
+  int32_t* dst2src = reinterpret_cast<int32_t*>(ws + L.l.dst2src);
+  int32_t* route2dst = reinterpret_cast<int32_t*>(ws + L.l.route2dst);
+  // FP8 on the grouped path: quantization and the segmenter share the first launch
+  const bool prep = L.grouped && f == FTMOE_FMT_FP8;
+  if (prep && R > 0x7fffffff) return FTMOE_UNSUPPORTED;
+
   OverlapScope overlap;
-  st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, xg, stream);
+  if (prep)
+    st = from_cuda(launch_prep_fp8(args->x, T, H, args->ld_x, xq, static_cast<float*>(xs), args->expert_ids, R,
+                                   s->topk, (int32_t)E, counts, offsets, dst2src, route2dst, strm));
+  else
+    st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, xg, stream);
   if (st != FTMOE_OK) return st;
   overlap.enable();
   if (!L.grouped) {
@@ -490,15 +502,13 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
     return ftmoe_combine(y, H, nullptr, args->expert_ids, args->route_weights, T, s->topk, H,
                          args->out, args->ld_out, stream);
   }
-  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.l.counts);
-  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.l.offsets);
-  int32_t* dst2src = reinterpret_cast<int32_t*>(ws + L.l.dst2src);
-  int32_t* route2dst = reinterpret_cast<int32_t*>(ws + L.l.route2dst);
   uint8_t* rq = ws + L.l.rows_q;
   void* rs = ws + L.l.rows_scales;
-  st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src,
-                            route2dst, stream);
-  if (st != FTMOE_OK) return st;
+  if (!prep) {
+    st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src,
+                              route2dst, stream);
+    if (st != FTMOE_OK) return st;
+  }
   st = ftmoe_gather_rows_scales(xq, xs, T, (int64_t)code_row_bytes(f, H), (int64_t)scale_row_bytes(f, H), dst2src, R,
                                 offsets + E, rq, rs, stream);
   if (st != FTMOE_OK) return st;

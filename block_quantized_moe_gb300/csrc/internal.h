@@ -64,6 +64,10 @@ uint32_t read_err_quant();
 cudaError_t launch_segment(const int32_t* ids, int64_t routes, int32_t topk, int32_t E,
                            int32_t* counts, int32_t* offsets, int32_t* dst2src,
                            int32_t* route2dst, cudaStream_t s);
+// the fused forward's first kernel: FP8 quantization of x and the segmenter in one grid
+cudaError_t launch_prep_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* q, float* scales,
+                            const int32_t* ids, int64_t routes, int32_t topk, int32_t E, int32_t* counts,
+                            int32_t* offsets, int32_t* dst2src, int32_t* route2dst, cudaStream_t s);
 uint32_t read_err_segment();
 
 // gather.cu

@@ -8,6 +8,7 @@
 // sb = e4m3(amax_block / (6 g)), code = e2m1_rne(x / (sb * g)).
 #include "common.cuh"
 #include "internal.h"
+#include "rowquant.cuh"
 
 namespace ftmoe {
 
@@ -23,37 +24,7 @@ __global__ void __launch_bounds__(256) quantize_act_fp8_kernel(
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows * ng;
        w += nwarps) {
     const int64_t row = w / ng, g = w - row * ng;
-    const int64_t c0 = g * kGroup + lane * 4;
-    const uint16_t* xr = x + row * ld_x;
-    float v[4];
-    const bool full = c0 + 4 <= k;
-    if (kVec && full) {
-      const uint2 p = *reinterpret_cast<const uint2*>(xr + c0);
-      v[0] = bf16_bits_to_f(p.x & 0xffffu);
-      v[1] = bf16_bits_to_f(p.x >> 16);
-      v[2] = bf16_bits_to_f(p.y & 0xffffu);
-      v[3] = bf16_bits_to_f(p.y >> 16);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = (c0 + i < k) ? bf16_bits_to_f(xr[c0 + i]) : 0.0f;
-    }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    amax = warp_max(amax);
-    const float sc = div_rn(amax, kE4M3Max);
-    uint32_t codes = 0;
-    if (amax > 0.0f) {
-      codes = (uint32_t)f2_to_e4m3x2(div_rn(v[0], sc), div_rn(v[1], sc)) |
-              ((uint32_t)f2_to_e4m3x2(div_rn(v[2], sc), div_rn(v[3], sc)) << 16);
-    }
-    uint8_t* qr = q + row * k;
-    if (kVec && full) {
-      *reinterpret_cast<uint32_t*>(qr + c0) = codes;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + i < k) qr[c0 + i] = (uint8_t)(codes >> (8 * i));
-    }
-    if (lane == 0) s[row * ng + g] = sc;
+    quantize_fp8_group<kVec>(x, k, ld_x, q, s, ng, row, g, lane);
   }
 }
 
@@ -67,7 +38,7 @@ static int grid_for(int64_t work_items, int per_block) {
 cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
                                     uint8_t* q, float* scales, cudaStream_t st) {
   const int64_t ng = cdiv(k, kGroup);
-  const bool vec = ((uintptr_t)x % 8 == 0) && (ld_x % 4 == 0) && ((uintptr_t)q % 4 == 0) && (k % 4 == 0);
+  const bool vec = quantize_fp8_vec_ok(x, ld_x, q, k);
   const int grid = grid_for(rows * ng, 8);
   return launch_kernel(vec ? quantize_act_fp8_kernel<true> : quantize_act_fp8_kernel<false>, dim3(grid), dim3(256), 0,
                        st, true, x, rows, k, ld_x, q, scales, ng);

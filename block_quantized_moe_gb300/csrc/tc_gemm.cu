@@ -12,19 +12,22 @@
 // weight-scale block row), the MMA's N is the token tile (16/32/64/128 rows of one
 // expert, picked from rows per expert because padding is not free -- FreeToken
 // "perf(dsfp4): pick the grouped-prefill tile from route density on sm_89").
-// Per 128-wide K block: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM
-// accumulator; the epilogue warps tcgen05.ld it, multiply by s_w * s_a[column] and add
-// into fp32 registers. Up to sixteen TMEM accumulators rotate (512 columns / token tile)
-// so the MMA runs ahead of the promotion.
+// A unit is (expert, token tile, one or two weight blocks); with two blocks the token tile
+// is shared (see Mode), and the gate/up pairing lets the epilogue apply SiLU-and-mul and the
+// FP8 re-quantization of the intermediate. Per 128-wide K block and weight block:
+// 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM accumulator; the epilogue
+// warps tcgen05.ld it and add d * (s_a[column] * s_w) into fp32 registers, the scale
+// products formed once per chunk of K blocks. Up to sixteen TMEM accumulators (512 columns
+// at most) rotate so the MMA runs ahead of the promotion.
 //
-// One persistent CTA per SM takes a contiguous range of units (expert, token tile,
-// 128-row weight block), weight block innermost: every weight tile is read once, and a
-// CTA's token tile and its activation scales stay in place across its units; the weight
-// block scale row of the next unit is prefetched while the current one runs. Roles: warp 0 = TMA producer, warp 1 = MMA
-// issuer (and TMEM owner), warps 2..17 = epilogue (four groups of four warps, one group
-// per quarter of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is
-// bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all roles, waits
-// for its own TMA loads still in flight, frees its TMEM and returns.
+// One persistent CTA per SM takes a contiguous range of units, weight blocks innermost:
+// every weight tile is read once and a token tile is read again from L2 by the units that
+// share it; the weight-scale rows of the next unit and the next chunk of activation scales
+// are fetched while the current ones are in use. Roles: warp 0 = TMA producer, warp 1 = MMA
+// issuer (and TMEM owner), the last 16 warps = epilogue (four groups of four warps, one
+// group per quarter of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every
+// mbarrier wait is bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all
+// roles, waits for its own TMA loads still in flight, frees its TMEM and returns.
 #include <cuda.h>
 
 #include <mutex>
