@@ -135,3 +135,41 @@ def test_automatic_forward_path_choice(ft):
     assert lay(ft.moe_shape(1, 2048, 768, 8, 8, path=3))["gateup_bytes"] == 0
     with pytest.raises(ft.FtmoeError):
         lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4))
+
+
+def test_two_block_and_fused_gemm_host_checks(ft):
+    # Every call here must be refused (or finish without a launch) on the host: the
+    # pointers are fake, so a call that reached a kernel would fault on a GPU.
+    L = ft.lib()
+    fake = ctypes.c_void_p(256)
+    bank = ft.ExpertBank(ft.FMT_FP8, 4, 384, 256, fake, fake, None)      # 2I = 384: not whole 256-row pairs
+    act = ft.Act(ft.FMT_FP8, 0, 8, 256, fake, fake, None)
+    rt = ft.Routes(ft.ROUTES_GROUPED, 0, 0, fake, None)
+    t = ft.Tile(16, 0, 0, 0)
+    silu = L.ftmoe_grouped_gemm_gateup_silu
+    assert silu(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, fake, ctypes.byref(t),
+                None) == ft.FTMOE_UNSUPPORTED
+    bank.n = 512
+    bank.k = 200  # K not a whole number of 128-wide blocks
+    act.k = 200
+    assert silu(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, fake, ctypes.byref(t),
+                None) == ft.FTMOE_UNSUPPORTED
+    bank.k = act.k = 256
+    assert silu(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), None, fake, ctypes.byref(t),
+                None) == ft.FTMOE_INVALID_ARG
+    slots = ft.Routes(ft.ROUTES_SLOTS, 8, 1, None, fake)  # the fused GEMM takes grouped rows only
+    assert silu(ctypes.byref(act), ctypes.byref(slots), ctypes.byref(bank), fake, fake, ctypes.byref(t),
+                None) == ft.FTMOE_INVALID_ARG
+    nv = ft.ExpertBank(ft.FMT_NVFP4, 4, 512, 256, fake, fake, fake)
+    act_nv = ft.Act(ft.FMT_NVFP4, 0, 8, 256, fake, fake, fake)
+    assert silu(ctypes.byref(act_nv), ctypes.byref(rt), ctypes.byref(nv), fake, fake, ctypes.byref(t),
+                None) == ft.FTMOE_UNSUPPORTED
+    act.rows = 0  # zero rows: OK without a launch
+    assert silu(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, fake, ctypes.byref(t),
+                None) == ft.FTMOE_OK
+    # ftmoe_tile.wblocks outside {0, 1, 2} is refused by the GEMM entry points
+    act.rows = 8
+    bad = ft.Tile(16, 2, 3, 0)
+    for fn in (L.ftmoe_grouped_gemm_gateup, L.ftmoe_grouped_gemm_down):
+        assert fn(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, 512, ctypes.byref(bad),
+                  None) == ft.FTMOE_INVALID_ARG
