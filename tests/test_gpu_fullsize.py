@@ -64,3 +64,20 @@ def test_prefill_24576_routes_on_1024_token_subsample(ft, fmt):
     ref, extra = forward_subsample(x.float().numpy(), ids.numpy(), w.numpy(), sub, H, I, E, seed, fmt,
                                    workers=max(2, (os.cpu_count() or 4)))
     assert_within_tolerance(got[sub], ref[sub], what=f"{fmt} forward, 24,576 routes", extra=extra[sub])
+
+
+def test_prefill_6144_routes_fused_equals_separate_and_oracle_sample(ft):
+    # 1,024 tokens x top-6 of 256 experts (24 rows per expert, token tile 32): the automatic
+    # forward fuses SiLU-and-mul into the gate/up GEMM here. Its whole output must equal the
+    # separate-kernel forward bit for bit, and a seeded 2-token sample must match the oracle.
+    from common import Problem
+    T, H, I, E, k, seed = 1024, 7168, 2048, 256, 6, 0xF7E00006
+    ids = synth.routes_fast(T, k, E, seed, DEV)
+    p = Problem(T, H, I, E, k, seed=seed, ids=ids)
+    assert ft.ftmoe_forward_workspace_layout(ft.moe_shape(T, H, I, k, E))["gateup_bytes"] == 0  # fused
+    out_auto, _, _ = p.forward(path=0)
+    out_sep, _, _ = p.forward(path=2)
+    torch.cuda.synchronize()
+    assert ft.ftmoe_read_error_flags() == 0
+    assert torch.equal(out_auto.view(torch.int16), out_sep.view(torch.int16))
+    p.check(out_auto, tokens_subset=synth.subsample(T, 2, seed))
