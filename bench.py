@@ -766,26 +766,73 @@ def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
         M.moe_forward(x[t:t + 1], ids[t:t + 1], w[t:t + 1], bg, bd, fmt="nvfp4")
 
 
+def _cpp_oracle_call(M, x, ids, w, bg, bd, fmt):
+    """The C++ oracle's inputs for a call of these tokens: the bank compacted to the experts
+    they use (expert ids renumbered; the arithmetic does not depend on the numbering).
+    Returns a function running the whole call on `threads` host threads."""
+    from oracle import cpu as C
+    C.lib()  # raises if the C++ oracle cannot be built or loaded
+    used = sorted(set(int(e) for e in ids.reshape(-1).tolist() if e >= 0))
+    remap = np.full(max(used) + 1 if used else 1, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    ids_c = np.where(ids >= 0, remap[np.maximum(ids, 0)], -1).astype(np.int32)
+
+    def stack(bank, n, k):
+        parts = [bank.parts(e) for e in used]
+        if fmt == "fp8":
+            if not parts:
+                return np.zeros((0, n, k), np.uint8), np.zeros((0, -(-n // 128), -(-k // 128)), np.float32)
+            return np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts])
+        if not parts:
+            return (np.zeros((0, n, k), np.uint8), np.zeros((0, n, -(-k // 16)), np.uint8),
+                    np.zeros(0, np.float32))
+        return (np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]),
+                np.array([p[2] for p in parts], np.float32))
+
+    H = x.shape[1]
+    I = bg.n // 2
+    bank_g, bank_d = stack(bg, 2 * I, H), stack(bd, H, I)
+    return lambda threads: C.moe_forward(x, ids_c, w, bank_g, bank_d, fmt=fmt, threads=threads)
+
+
 def cpu_baseline(name, budget_s=20.0, min_s=10.0):
-    """Time the oracle's forward token by token on the first (at most 8) tokens of a call,
-    in repeated passes until at least min_s of CPU work (stopping at budget_s); scale the
-    time per token to one full call."""
+    """Time the oracle on the first (at most 8) tokens of a call, taken as a call of their
+    own, in repeated calls until at least min_s (stopping at budget_s); scale the time per
+    token to one full call. The C++ oracle runs on every host thread; where it cannot be
+    built or loaded, the numpy oracle runs on one thread, token by token. FP8 quantizes per
+    token, so the sample's rows equal the full call's; NVFP4's tensor scales span the
+    sample instead (the same work per token)."""
     T_full = WORKLOADS[name][0]
     M, x, ids, w, bg, bd, T, fmt = _oracle_problem(name, max_tokens=min(T_full, 8))
     n = ids.shape[0]
     T = T_full
+    try:
+        from oracle import cpu as C
+        run = _cpp_oracle_call(M, x, ids, w, bg, bd, fmt)
+        threads = C.hardware_threads()
+    except Exception as exc:  # noqa: BLE001 - the baseline leg only
+        run, threads, why = None, 1, str(exc).splitlines()[0] if str(exc) else type(exc).__name__
     t0 = time.perf_counter()
     done = 0
     while True:
-        _oracle_token(M, x, ids, w, bg, bd, fmt, done % n)
-        done += 1
+        if run is not None:
+            run(threads)
+            done += n
+        else:
+            _oracle_token(M, x, ids, w, bg, bd, fmt, done % n)
+            done += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (el >= min_s and done % n == 0):
             break
     per_call = el / done * T
-    return {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
-            "sample": f"{done} token forwards over the first {n} of {T} tokens of one call (numpy float64, "
-                      f"single thread), {el:.1f} s of CPU work, scaled to the full call"}
+    if run is not None:
+        sample = (f"{done // n} calls of the first {n} of {T} tokens (C++ oracle, float64, "
+                  f"{threads} threads), {el:.1f} s, scaled to the full call")
+    else:
+        sample = (f"{done} token forwards over the first {n} of {T} tokens of one call (numpy float64, "
+                  f"single thread; C++ oracle unavailable: {why}), {el:.1f} s, scaled to the full call")
+    return {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
+            "sample": sample}
 
 
 def _gather_oracle_problem(name, seed=0xF7E00003):
@@ -835,19 +882,35 @@ def run_reference(args, rank, world):
     M, x, ids, w, bg, bd, T, fmt = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
     T = T_full
     ns = ids.shape[0]
+    try:
+        from oracle import cpu as C
+        run = _cpp_oracle_call(M, x, ids, w, bg, bd, fmt)
+        threads = C.hardware_threads()
+        per_step = ns
+        what = f"each step: a call of the first {ns} of {T} tokens (C++ oracle, {threads} threads)"
+    except Exception:  # noqa: BLE001 - the reference leg only
+        run, threads, per_step = None, 1, 1
+        what = f"each step: 1 of {T} tokens of one call (numpy oracle, one thread)"
+
+    def step(i):
+        if run is not None:
+            run(threads)
+        else:
+            _oracle_token(M, x, ids, w, bg, bd, fmt, i % ns)
+
     for i in range(args.warmup):
-        _oracle_token(M, x, ids, w, bg, bd, fmt, i % ns)
+        step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        _oracle_token(M, x, ids, w, bg, bd, fmt, i % ns)
+        step(i)
     el = time.perf_counter() - t0
-    us = el / args.steps * T * 1e6
+    us = el / (args.steps * per_step) * T * 1e6
     return {"impl": "reference", "metric": "MoE FFN us/call", "value": round(us, 1), "unit": "us/call",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload},
-            "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: 1 of {T} tokens of one call, scaled to the full call"},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
+                             "sample": what + ", scaled to the full call"},
             "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

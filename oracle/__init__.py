@@ -1,4 +1,4 @@
-"""CPU oracle of the routed-expert block-quantized MoE FFN (numpy, float64).
+"""CPU oracles of the routed-expert block-quantized MoE FFN: numpy (float64) and C++.
 
 TEST INFRASTRUCTURE. Only the test suite, `__graft_entry__.smoke()` and the
 benchmark's `cpu_baseline` / `--impl reference` legs may import or call anything
@@ -19,5 +19,9 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   moe.silu_mul                        pinned: scipy.special.expit, closed-form points
   moe.combine                         pinned: single route of weight 1, all inactive
   moe.pick_tile                       pinned: the dsfp4 page's table (tests/golden)
+  cpu (cpu_oracle.cpp)                the same definitions written again in plain C++17 with
+                                      std::thread; pinned to the numpy oracle above (codes,
+                                      scales, indices and bytes bit for bit; FFN outputs to
+                                      float64 rounding) and to the same closed forms
 """
 from . import formats, moe  # noqa: F401
