@@ -831,8 +831,17 @@ def cpu_baseline(name, budget_s=20.0, min_s=10.0):
     else:
         sample = (f"{done} token forwards over the first {n} of {T} tokens of one call (numpy float64, "
                   f"single thread; C++ oracle unavailable: {why}), {el:.1f} s, scaled to the full call")
-    return {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
-            "sample": sample}
+    res = {"value": round(per_call * 1e6, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
+           "sample": sample}
+    if run is not None and threads > 1:
+        # the same sampled call on one thread, once
+        t1 = time.perf_counter()
+        run(1)
+        el1 = time.perf_counter() - t1
+        res["single_thread"] = {"value": round(el1 / n * T * 1e6, 1), "unit": "us/call", "cores": 1,
+                                "sample": f"1 call of the first {n} of {T} tokens (C++ oracle, one thread), "
+                                          f"{el1:.1f} s, scaled to the full call"}
+    return res
 
 
 def _gather_oracle_problem(name, seed=0xF7E00003):
