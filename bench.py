@@ -232,9 +232,9 @@ class ClockSampler:
             self.thread.start()
             return
         try:
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{self.device.index or 0}.csv")
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix=f"clocks_dev{self.device.index or 0}_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device.index or 0),
                                           f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -256,7 +256,10 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in open(self.path):
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        os.unlink(self.path)
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
