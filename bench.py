@@ -103,10 +103,44 @@ def weight_bytes(fmt, n, k):
     return n * k // 2 + n * k // 16 + 4
 
 
+def code_hash(path):
+    """First 12 hex digits of the sha1 of a C/C++/CUDA source's code: // and /* */ comments,
+    trailing blanks and blank lines removed. Editing a comment keeps a recorded capture
+    valid; any change to the code voids it."""
+    import hashlib
+    text = open(path).read()
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return hashlib.sha1("\n".join(ln for ln in lines if ln).encode()).hexdigest()[:12]
+
+
 def recorded_traffic(workload):
     """DRAM bytes per launch of the dominant kernel from profiles/traffic.txt, or None when
-    no capture is recorded or the kernel source changed since it was taken."""
-    import hashlib
+    no capture is recorded or the kernel's code changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -117,8 +151,7 @@ def recorded_traffic(workload):
         src = os.path.join(ROOT, "block_quantized_moe_gb300", parts[1])
         if not os.path.exists(src):
             return None
-        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
-        return int(parts[3]) if sha == parts[2] else None
+        return int(parts[3]) if code_hash(src) == parts[2] else None
     return None
 
 

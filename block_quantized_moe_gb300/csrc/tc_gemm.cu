@@ -107,11 +107,11 @@ __host__ __device__ constexpr int kbs_for(int tt, int mode) {
 
 // Warp roles. Warp 0 issues TMA, warp 1 issues MMAs, the last kEpiWarps warps promote.
 // Units with two weight blocks from token tile 64 on hold 2 x TT/4 fp32 accumulators (32
-// or 64) per epilogue thread; those kernels add two idle warps so that warps 0-3 form a warpgroup that gives
-// registers back (setmaxnreg.dec to kCtlRegs) to the four epilogue warpgroups
-// (setmaxnreg.inc to kEpiRegs). The launch pool is threads x the kernel's register count;
-// the host checks kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps against it before launching,
-// since an increase the pool cannot cover would never complete.
+// or 64) per epilogue thread. Those kernels add two idle warps, so that warps 0-3 form a
+// warpgroup that gives registers back (setmaxnreg.dec to kCtlRegs) to the four epilogue
+// warpgroups (setmaxnreg.inc to kEpiRegs). The launch pool is threads x the kernel's
+// register count; the host checks kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps against it
+// before launching, since an increase the pool cannot cover would never complete.
 template <int TT, int MODE>
 struct Warps {
   static constexpr bool kSplitRegs = TT >= 64 && wb_of(MODE) == 2;
