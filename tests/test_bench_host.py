@@ -1,0 +1,33 @@
+"""Host-side helpers of bench.py that need no GPU."""
+import os
+
+import bench
+
+
+def _write(tmp_path, name, text):
+    p = os.path.join(tmp_path, name)
+    with open(p, "w") as f:
+        f.write(text)
+    return p
+
+
+def test_code_hash_ignores_comments_and_blank_lines_only(tmp_path):
+    base = _write(tmp_path, "a.cu", 'int a = 1;  // one\n/* two */\nconst char* s = "// kept";\n')
+    comments = _write(tmp_path, "b.cu", '// header\nint a = 1;  // changed\n\n/* two\n lines */\nconst char* s = "// kept";\n')
+    code = _write(tmp_path, "c.cu", 'int a = 2;  // one\n/* two */\nconst char* s = "// kept";\n')
+    string = _write(tmp_path, "d.cu", 'int a = 1;  // one\n/* two */\nconst char* s = "// other";\n')
+    assert bench.code_hash(base) == bench.code_hash(comments)
+    assert bench.code_hash(base) != bench.code_hash(code)
+    assert bench.code_hash(base) != bench.code_hash(string)  # text inside a string literal is code
+
+
+def test_recorded_traffic_entries_are_well_formed():
+    path = os.path.join(bench.ROOT, "profiles", "traffic.txt")
+    for ln in open(path):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        workload, src, h, nbytes = ln.split()
+        assert workload in bench.WORKLOADS or workload in bench.GATHER_WORKLOADS
+        assert os.path.exists(os.path.join(bench.ROOT, "block_quantized_moe_gb300", src))
+        assert len(h) == 12 and int(h, 16) >= 0 and int(nbytes) > 0
+    assert bench.recorded_traffic("no-such-workload") is None
