@@ -248,7 +248,7 @@ constexpr int64_t kFusedMinUnits = 2048;
 bool use_fused(const ftmoe_moe_shape* s) {
   if (s->path == 3) return true;
   if (s->path != 0 || s->format != FTMOE_FMT_FP8) return false;
-  if (!tc_gemm_pairs_ok(2 * s->inter, s->hidden)) return false;
+  if (!tc_gemm_pairs_ok(2 * s->inter, s->hidden) || s->num_experts > kTcGemmMaxExperts) return false;
   const int64_t R = s->tokens * s->topk;
   const int tile = s->tok_tile ? s->tok_tile : pick_tile_value(R, s->num_experts);
   if (tile > 64) return false;

@@ -120,6 +120,9 @@ struct TcGemmArgs {
 };
 // whether an n x k weight matrix can run two weight blocks per unit (n % 256, k % 128)
 bool tc_gemm_pairs_ok(int64_t n, int64_t k);
+// largest expert count the tensor-core GEMM's unit table holds (tc::kMaxExperts in
+// tc_gemm.cu, which refuses larger banks as unsupported)
+constexpr int32_t kTcGemmMaxExperts = 1024;
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s, int* unsupported);
 uint32_t read_err_tc_gemm();
 

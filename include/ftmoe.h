@@ -242,7 +242,8 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * the separate SiLU-and-mul kernel, 3 = grouped path with SiLU-and-mul fused into the
  * gate/up GEMM (ftmoe_grouped_gemm_gateup_silu; FP8, I % 128 == 0, H % 128 == 0).
  * Automatic: the grouped path at every batch size, fused where the token tile is at most
- * 64 and the routes can reach at least 2048 (expert, gate/up block pair) units
+ * 64, the bank has at most 1024 experts and the routes can reach at least 2048 (expert,
+ * gate/up block pair) units
  * (min(T*topk, E) * I/128 >= 2048), else with the separate kernel. Paths 2 and 3 give
  * bit-identical outputs.
  * ------------------------------------------------------------------------------------ */

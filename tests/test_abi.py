@@ -132,6 +132,7 @@ def test_automatic_forward_path_choice(ft):
     assert lay(ft.moe_shape(1, 2048, 768, 8, 8))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, fmt=ft.FMT_NVFP4))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=2))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(2048, 7168, 2048, 6, 2048))["gateup_bytes"] > 0  # beyond the GEMM's 1024 experts
     assert lay(ft.moe_shape(1, 2048, 768, 8, 8, path=3))["gateup_bytes"] == 0
     with pytest.raises(ft.FtmoeError):
         lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4))
