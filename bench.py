@@ -82,6 +82,31 @@ DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
 GATHER_WORKLOADS = {f"gather-k{k}-t{t}": (k, t, 8) for k in (7168, 2048, 896) for t in (1, 8, 64, 1024)}
 
 
+# The pages' own per-call times for exactly these workloads (other GPUs: context, not a
+# target), so that vs_baseline = value / page value (below 1 = faster):
+# - FreeToken "perf(moe): skip inactive block-fp8 decode routes", GPU decode A/B table:
+#   RTX A1000 (sm_86, its FP8 compatibility path), batch 1, top-k 8, CUDA graphs;
+# - SGLang "Gather the cutlass MoE activation and its scales in one launch", Speed Tests:
+#   the fused gather on B200, top-k 8.
+PAGES_US = {
+    "decode-h2048-i768-e8-t1-a2": 60.589,
+    "decode-h4096-i1024-e64-t1-a8": 472.730,
+    "decode-h4096-i1024-e64-t1-a4": 255.034,
+    "decode-h4096-i1024-e64-t1-a2": 148.278,
+    "decode-h4096-i1024-e64-t1-a0": 8.819,
+    "gather-k7168-t1": 1.31,
+    "gather-k2048-t1": 1.42,
+    "gather-k7168-t8": 1.60,
+    "gather-k7168-t64": 2.10,
+    "gather-k7168-t1024": 11.14,
+}
+
+
+def vs_pages(workload, value_us):
+    ref = PAGES_US.get(workload)
+    return None if ref is None else round(value_us / ref, 4)
+
+
 def workload_format(name):
     return "nvfp4" if "-nvfp4-" in name else "fp8"
 
@@ -628,7 +653,7 @@ def run_gpu(args, rank, world, local):
         "ms_per_step": round(ms_max / args.steps, 5),
         "higher_is_better": False,
         "scaling": "weak",
-        "vs_baseline": None,
+        "vs_baseline": vs_pages(wl.name, value),
         "dtype": ("fp8-e4m3 (fp32 accumulate)" if wl.fmt == "fp8" else
                   "nvfp4-e2m1 with e4m3 block scales (fp32 accumulate)"),
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
@@ -750,7 +775,8 @@ def run_gather(args, rank, world, local):
     result = {
         "metric": "gather us/call", "value": round(value, 3), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8 (FP8 bytes) + fp32 scales",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": vs_pages(args.workload, value),
+        "dtype": "u8 (FP8 bytes) + fp32 scales",
         "data": "synthetic (seeded random FP8 bytes, U(1e-3, 1) scales, randint maps with duplicates)",
         "config": {"workload": args.workload, "k": k, "tokens": T, "topk": topk, "rows": n_dst,
                    "maps_rotated": nsets, "l2": L2Flush.DESC,

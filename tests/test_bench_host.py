@@ -31,3 +31,11 @@ def test_recorded_traffic_entries_are_well_formed():
         assert os.path.exists(os.path.join(bench.ROOT, "block_quantized_moe_gb300", src))
         assert len(h) == 12 and int(h, 16) >= 0 and int(nbytes) > 0
     assert bench.recorded_traffic("no-such-workload") is None
+
+
+def test_vs_baseline_only_for_workloads_the_pages_time():
+    assert bench.vs_pages("decode-h4096-i1024-e64-t8-a8", 118.0) is None  # no page number
+    assert bench.vs_pages("decode-h2048-i768-e8-t1-a2", 60.589) == 1.0
+    assert bench.vs_pages("gather-k7168-t1024", 5.57) == 0.5
+    for name in bench.PAGES_US:
+        assert name in bench.WORKLOADS or name in bench.GATHER_WORKLOADS
