@@ -39,3 +39,24 @@ def test_vs_baseline_only_for_workloads_the_pages_time():
     assert bench.vs_pages("gather-k7168-t1024", 5.57) == 0.5
     for name in bench.PAGES_US:
         assert name in bench.WORKLOADS or name in bench.GATHER_WORKLOADS
+
+
+def test_cpu_baseline_oracle_call_equals_the_numpy_oracle():
+    # the bench's CPU-baseline call (C++ oracle over a bank compacted to the used experts)
+    # computes the numpy oracle's forward, in both formats and with no active route
+    import numpy as np
+
+    import synth
+    from oracle import moe as M
+    T, H, I, E, k, seed = 4, 256, 128, 6, 3, 5
+    x = synth.activations_bf16(T, H, seed, "cpu").float().numpy()
+    ids = synth.routes(T, k, E, seed, active_per_token=[3, 2, 0, 3], device="cpu").numpy()
+    w = synth.routing_weights(T, k, seed, "cpu").numpy()
+    for fmt in ("fp8", "nvfp4"):
+        bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
+        bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
+        got = bench._cpp_oracle_call(M, x, ids, w, bg, bd, fmt)(4)
+        ref = M.moe_forward(x, ids, w, bg, bd, fmt=fmt)["out"]
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-14 * np.abs(ref).max())
+        none = np.full_like(ids, -1)
+        assert not bench._cpp_oracle_call(M, x, none, w, bg, bd, fmt)(2).any()
