@@ -60,3 +60,15 @@ def test_cpu_baseline_oracle_call_equals_the_numpy_oracle():
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-14 * np.abs(ref).max())
         none = np.full_like(ids, -1)
         assert not bench._cpp_oracle_call(M, x, none, w, bg, bd, fmt)(2).any()
+
+
+def test_cpu_baseline_uses_the_cpp_oracle_and_falls_back_to_numpy(monkeypatch):
+    res = bench.cpu_baseline("decode-h2048-i768-e8-t1-a2", budget_s=1.0, min_s=0.2)
+    assert res["kind"] == "oracle" and res["value"] > 0 and "C++ oracle" in res["sample"]
+    from oracle import cpu as C
+
+    def unavailable():
+        raise RuntimeError("no compiler")
+    monkeypatch.setattr(C, "lib", unavailable)
+    res = bench.cpu_baseline("decode-h2048-i768-e8-t1-a2", budget_s=1.0, min_s=0.2)
+    assert res["cores"] == 1 and "numpy" in res["sample"] and "no compiler" in res["sample"]
