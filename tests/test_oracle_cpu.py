@@ -148,3 +148,29 @@ def test_forward_inactive_invariants():
     a = C.moe_forward(x, ids2, w_new, _bank(bg, "fp8"), _bank(bd, "fp8"))
     b = C.moe_forward(x, clamped, w_old, _bank(bg, "fp8"), _bank(bd, "fp8"))
     assert np.array_equal(a, b) and not np.any(np.isnan(a))
+
+
+def test_forward_at_the_decode_2048_768_workload_matches_the_numpy_oracle():
+    # one token, hidden 2048, intermediate 768, 8 experts, top-8 with 2 of 8 slots active
+    import synth
+    T, H, I, E, k, seed = 1, 2048, 768, 8, 8, 0xF7E00001
+    x = synth.activations_bf16(T, H, seed, "cpu").float().numpy()
+    ids = synth.routes(T, k, E, seed, active_per_token=2, device="cpu").numpy()
+    w = synth.routing_weights(T, k, seed, "cpu").numpy()
+    used = sorted(int(e) for e in ids.reshape(-1) if e >= 0)
+    raw_g = {e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy() for e in used}
+    raw_d = {e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy() for e in used}
+    bg = M.LazyBank(lambda e: raw_g[e], 2 * I)
+    bd = M.LazyBank(lambda e: raw_d[e], H)
+    ref = M.moe_forward(x, ids, w, bg, bd)["out"]
+    # the C++ oracle quantizes the same raw weights itself
+    gq = np.zeros((E, 2 * I, H), np.uint8)
+    gs = np.zeros((E, 2 * I // 128, H // 128), np.float32)
+    dq = np.zeros((E, H, I), np.uint8)
+    ds = np.zeros((E, H // 128, I // 128), np.float32)
+    for e in used:
+        gq[e], gs[e] = C.quantize_weight_fp8(raw_g[e])
+        dq[e], ds[e] = C.quantize_weight_fp8(raw_d[e])
+        assert np.array_equal(gq[e], bg.parts(e)[0]) and np.array_equal(_bits(gs[e]), _bits(bg.parts(e)[1]))
+    got = C.moe_forward(x, ids, w, (gq, gs), (dq, ds), threads=4)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-14 * np.max(np.abs(ref)))
