@@ -1,6 +1,7 @@
 // C ABI of libftmoe: argument validation on the host, then kernel launches on the
 // caller's stream. Nothing here allocates, frees or synchronises (except
-// ftmoe_read_error_flags), so every entry point can be captured in a CUDA graph.
+// ftmoe_read_error_flags), so every entry point defined in this file can be captured in a
+// CUDA graph.
 #include <string.h>
 
 #include "common.cuh"

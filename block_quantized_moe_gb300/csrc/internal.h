@@ -14,6 +14,15 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Whether launches from this host thread may overlap the previous kernel on the stream
 // (programmatic dependent launch). Set by the fused forward for its kernels after the
 // first; every kernel waits for its predecessor's data (pdl_wait) before touching it.
+//
+// Ordering invariant the tensor-core GEMMs rely on: they read the segment offsets before
+// their own pdl_wait, so the segmenter (or the prep kernel) must have completed by the time
+// a GEMM starts. That holds as long as every kernel launched between the segmenter and a
+// GEMM either waits before it triggers its dependents (the gather and the GEMMs do), or
+// is itself launched only after a kernel that did (the FP8 SiLU-and-mul kernel triggers
+// first, but it follows the gate/up GEMM, which has waited for the gather, which waited
+// for the segmenter). A new kernel placed between the segmenter and a GEMM must wait
+// before it triggers.
 bool& pdl_enabled();
 
 template <typename... KArgs, typename... Args>

@@ -4,7 +4,9 @@
 // caller-provided workspace. Every GPU that loads the library holds this array until the
 // process exits. The array's host-side name is only a stand-in for the symbol, never a
 // device address, so the address is fetched with cudaGetSymbolAddress once per device
-// (the first call on that device, with it current) and cached.
+// (the first call on that device, with it current) and cached. The cached address is that
+// of the device's primary context; a context destroyed and recreated (cudaDeviceReset)
+// places the array elsewhere, and the library has to be reloaded after it.
 #include <mutex>
 
 #include "common.cuh"

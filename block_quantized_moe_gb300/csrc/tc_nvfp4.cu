@@ -3,8 +3,10 @@
 // out[row, n] = g_a * g_w[e] * sum_k (a[row,k] * sa[row, k/16]) * (w[e,n,k] * sw[e,n,k/16])
 // with e2m1 codes a, w (two per byte, even element in the low nibble), e4m3 block scales
 // sa, sw (one per 16 elements) and fp32 tensor scales g_a, g_w[e] -- the NVFP4 variant of
-// the prefill GEMM (the dsfp4 page names the format; the two-level recipe is fixed in the
-// design notes). Unlike the FP8 path, the block scales are native to the MMA
+// the prefill GEMM. The dsfp4 page names the format only; the two-level recipe used here is
+// g = amax_tensor / (448 * 6) per tensor, one e4m3 scale sb = e4m3(amax_16 / (6 g)) per 16
+// consecutive elements of a row, and e2m1 codes of x / (sb * g), rounded to nearest even.
+// Unlike the FP8 path, the block scales are native to the MMA
 // (tcgen05.mma ... kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per instruction, one
 // ue4m3 scale per 16 elements of each row), so a unit accumulates all of K in TMEM and the
 // epilogue only applies g_a * g_w once.

@@ -18,8 +18,9 @@
  *
  * Conventions for every entry point:
  *   - Pointers named in the argument lists are DEVICE pointers unless stated; the caller
- *     allocates and owns all memory. No entry point allocates, frees or synchronises,
- *     so every call may be captured into a CUDA graph (ftmoe_read_error_flags excepted).
+ *     allocates and owns all memory. No entry point allocates, frees or synchronises
+ *     (ftmoe_read_error_flags excepted), so the stream-ordered calls declared before
+ *     ftmoe_moe_forward_noalloc may be captured into a CUDA graph.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *     Errors of the asynchronous work surface at the caller's next synchronisation.
  *   - Argument checks run on the host before anything is enqueued and touch no device
@@ -161,7 +162,11 @@ ftmoe_status ftmoe_quantize_weights(const float* w, int32_t num_experts, int64_t
  * Outputs: counts int32 [E]; offsets int32 [E+1] (exclusive prefix, offsets[E] = active
  * routes); dst2src int32 [tokens*topk] capacity, entry d < offsets[E] is the token of
  * grouped row d; route2dst int32 [tokens*topk], the grouped row of route r or -1.
- * Within an expert rows keep route order. All outputs are deterministic. */
+ * Within an expert rows keep route order. All outputs are deterministic.
+ * Passages: SGLang gather page, Motivation (the quantized activation is replicated once per
+ * routed expert through a dst2src map of m * topk entries, one source token per grouped
+ * row); FreeToken "perf(dsfp4): pick the grouped-prefill tile from route density on sm_89",
+ * Measurements (the grouped GEMM's rows per expert, which counts[e] holds). */
 ftmoe_status ftmoe_segment_routes(const int32_t* expert_ids, int64_t tokens, int32_t topk,
                                   int32_t num_experts, int32_t* counts, int32_t* offsets,
                                   int32_t* dst2src, int32_t* route2dst, void* stream);
@@ -206,7 +211,10 @@ ftmoe_status ftmoe_grouped_gemm_gateup_silu(const ftmoe_act* a, const ftmoe_rout
                                             const ftmoe_expert_bank* w, uint8_t* q_out,
                                             float* scales_out, const ftmoe_tile* tile, void* stream);
 
-/* SiLU-and-mul with re-quantization: for each row, a[i] = silu(g[i]) * u[i] with
+/* SiLU-and-mul with re-quantization (FreeToken "perf(moe): skip inactive block-fp8 decode
+ * routes", first section: the activation reads the whole gate/up buffer, zero tiles of
+ * inactive routes included; its Validation names SiLU-and-mul among the activations):
+ * for each row, a[i] = silu(g[i]) * u[i] with
  * g = gu[row, 0:inter], u = gu[row, inter:2*inter], silu(g) = g / (1 + exp(-g)) in fp32;
  * then a is quantized like ftmoe_quantize_act (FP8: q [rows][inter], scales float
  * [rows][ceil(inter/128)]; NVFP4: q [rows][inter/2], scales [rows][inter/16],
@@ -217,7 +225,10 @@ ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_
                             const int32_t* rows_dev, int32_t format, uint8_t* q, void* scales,
                             float* global_scale, void* stream);
 
-/* Grouped down GEMM: the same contraction as ftmoe_grouped_gemm_gateup with
+/* Grouped down GEMM (FreeToken "perf(moe): skip inactive block-fp8 decode routes", first
+ * section: gate/up and down run the same block-FP8 kernel, and an inactive route's down
+ * output tile is written as zeros; SGLang gather page, Motivation: the second grouped GEMM
+ * of the blockwise-FP8 MoE): the same contraction as ftmoe_grouped_gemm_gateup with
  * w->n = hidden and w->k = a->k = inter. In FTMOE_ROUTES_SLOTS mode activation row r
  * belongs to route r. */
 ftmoe_status ftmoe_grouped_gemm_down(const ftmoe_act* a, const ftmoe_routes* routes,
@@ -236,8 +247,12 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
                            void* stream);
 
 /* ------------------------------------------------------------------------------------
- * Fused forward. Launch shapes depend only on the shape below, never on route content,
- * so one captured CUDA graph can be replayed while routes and inputs change in place.
+ * Fused forward (FreeToken "perf(moe): skip inactive block-fp8 decode routes": first
+ * section, the launch shapes stay fixed and the activation still processes the zeroed
+ * buffers; Validation, one CUDA graph replayed while the routes switch between all-active,
+ * mixed and all-inactive and the inputs change). Launch shapes depend only on the shape
+ * below, never on route content, so one captured CUDA graph can be replayed while routes
+ * and inputs change in place.
  * path: 0 = automatic, 1 = route-slot streaming path (FP8 only), 2 = grouped path with
  * the separate SiLU-and-mul kernel, 3 = grouped path with SiLU-and-mul fused into the
  * gate/up GEMM (ftmoe_grouped_gemm_gateup_silu; FP8, I % 128 == 0, H % 128 == 0).
@@ -291,20 +306,21 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
 
 /* Allocation-free variant of ftmoe_moe_forward (no counterpart in the pages; a service of
  * this library). For callers that cannot allocate device memory themselves: a plugin
- * hosted by a runtime that owns all device memory and exposes no allocator, code that
- * records a CUDA graph in a capture mode where cudaMalloc is not allowed, or a latency
+ * hosted by a runtime that owns all device memory and exposes no allocator, or a latency
  * path that cannot afford an allocation's implicit synchronisation. The intermediates
  * live in a file-scope device array of 8 MiB that every GPU loading the library keeps
  * until the process exits; shapes whose workspace (ftmoe_forward_workspace_bytes)
  * exceeds it return FTMOE_WORKSPACE_TOO_SMALL. Decode-size shapes fit (8 tokens, top-8,
  * hidden 4096, intermediate 1024 need about 1.7 MiB).
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture. Every call
- * on a device shares the one array: calls whose GPU work overlaps (other streams, other
- * threads) race on it and must be serialised by the caller. The forward writes every
- * region of the array before reading it, so a previous call's contents are never used.
- * No cudaMalloc, cudaFree or allocating library routine is called. Inputs, outputs and
- * their ownership are as for ftmoe_moe_forward. */
+ * with that device current and caches it; make that first call before any stream capture.
+ * The cached address belongs to the device's primary context: after the context is
+ * destroyed and recreated (cudaDeviceReset), the array lives at a new address and the
+ * library must be reloaded. Every call on a device shares the one array: calls whose GPU
+ * work overlaps (other streams, other threads) race on it and must be serialised by the
+ * caller. The forward writes every region of the array before reading it, so a previous
+ * call's contents are never used. No cudaMalloc, cudaFree or allocating library routine is
+ * called. Inputs, outputs and their ownership are as for ftmoe_moe_forward. */
 ftmoe_status ftmoe_moe_forward_noalloc(const ftmoe_moe_args* args, void* stream);
 
 /* Reads and clears the device error word of the current device (FTMOE_ERR_* bits) into
