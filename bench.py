@@ -1,10 +1,11 @@
 """Benchmark of the routed-expert block-quantized MoE FFN on GB300 (libftmoe).
 
-Default workload: the decode sweep geometry -- hidden 4096, intermediate 1024, 64-expert
-FP8 bank with 128x128 block scales, top-k 8, batch 8 tokens, all 8 routes active --
-replayed from one CUDA graph while the routes and inputs change between steps.
-A step is one ftmoe_moe_forward (quantize -> gate/up -> SiLU-and-mul -> down ->
-combine). Other workloads (--workload) are available for measurement runs.
+Default workload: the largest single-GPU configuration -- FP8 prefill, 4,096 tokens routed
+top-6 over 256 experts (24,576 routes, about 96 rows per expert), hidden 7168, per-expert
+intermediate 2048, FP8-e4m3 weights with 128x128 fp32 block scales -- replayed from one CUDA
+graph while the routes and inputs change between steps. A step is one ftmoe_moe_forward
+(quantize + segment -> gather -> gate/up -> SiLU-and-mul -> down -> combine). The decode,
+gather and NVFP4 workloads are selected with --workload.
 
 Timing: W warm-up steps, then K timed steps; before every step the inputs of the
 next route set are copied into the graph's input buffers and L2 is flushed (a 512 MiB
@@ -74,7 +75,7 @@ WORKLOADS = {
     "prefill-nvfp4-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
     "prefill-nvfp4-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
 }
-DEFAULT_WORKLOAD = "decode-h4096-i1024-e64-t8-a8"
+DEFAULT_WORKLOAD = "prefill-fp8-h7168-i2048-e256-r24576"
 
 # The fused FP8 row + scale gather alone: name -> (k, tokens, top-k). Source rows are random
 # FP8 bytes [tokens x k] with fp32 scales U(1e-3, 1) per 128 columns; the map has
@@ -800,7 +801,8 @@ def run_gather(args, rank, world, local):
 # ------------------------------------------------------------------------------------
 
 def _oracle_problem(name, seed=0xF7E00002, max_tokens=None):
-    from oracle import moe as M
+    """Inputs of the oracle's sampled call: x, ids, weights of the first max_tokens tokens,
+    the full call's token count, the format and the experts the sample uses."""
     T, H, I, E, k, active, _ = WORKLOADS[name]
     fmt = workload_format(name)
     x = synth.activations_bf16(T, H, seed + 17, "cpu")
@@ -810,17 +812,26 @@ def _oracle_problem(name, seed=0xF7E00002, max_tokens=None):
     if max_tokens is not None:  # the first tokens of the call
         ids, x, w = ids[:max_tokens], x[:max_tokens], w[:max_tokens]
     used = sorted(set(int(e) for e in ids.reshape(-1).tolist() if e >= 0))
+    return x.float().numpy(), ids.numpy(), w.numpy(), T, fmt, used
+
+
+def _numpy_banks(name, used, seed=0xF7E00002):
+    """The numpy oracle's lazily quantized banks, the sample's experts quantized up front
+    (the quantized bank is an input; it is built before timing)."""
+    from oracle import moe as M
+    _, H, I, _, _, _, _ = WORKLOADS[name]
+    fmt = workload_format(name)
     bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
     bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
-    for e in used:  # the quantized bank is an input; build it before timing
+    for e in used:
         bg.parts(e)
         bd.parts(e)
-    return M, x.float().numpy(), ids.numpy(), w.numpy(), bg, bd, T, fmt
+    return M, bg, bd
 
 
 def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
-    """The oracle's forward for token t alone. FP8 quantizes per token, so one token of the
-    call is exact; the NVFP4 tensor scales span the whole call, so there the token is run
+    """The numpy oracle's forward for token t alone. FP8 quantizes per token, so one token of
+    the call is exact; the NVFP4 tensor scales span the whole call, so there the token is run
     as a call of its own (the same work per token)."""
     if fmt == "fp8":
         M.moe_forward(x, ids, w, bg, bd, tokens_subset=[t])
@@ -828,32 +839,42 @@ def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
         M.moe_forward(x[t:t + 1], ids[t:t + 1], w[t:t + 1], bg, bd, fmt="nvfp4")
 
 
-def _cpp_oracle_call(M, x, ids, w, bg, bd, fmt):
-    """The C++ oracle's inputs for a call of these tokens: the bank compacted to the experts
-    they use (expert ids renumbered; the arithmetic does not depend on the numbering).
+def _cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=0xF7E00002):
+    """The C++ oracle's inputs for a call of these tokens, with the bank compacted to the
+    experts they use (expert ids renumbered; the arithmetic does not depend on the
+    numbering). The experts' raw weights are drawn and quantized by the C++ oracle's own
+    quantizers on all host threads (ctypes and torch release the GIL), before timing.
     Returns a function running the whole call on `threads` host threads."""
+    import concurrent.futures
     from oracle import cpu as C
     C.lib()  # raises if the C++ oracle cannot be built or loaded
-    used = sorted(set(int(e) for e in ids.reshape(-1).tolist() if e >= 0))
     remap = np.full(max(used) + 1 if used else 1, -1, np.int32)
     remap[used] = np.arange(len(used), dtype=np.int32)
     ids_c = np.where(ids >= 0, remap[np.maximum(ids, 0)], -1).astype(np.int32)
 
-    def stack(bank, n, k):
-        parts = [bank.parts(e) for e in used]
+    def quantized(job):
+        e, tag, n, k = job
+        raw = synth.expert_weight_fp32(n, k, seed, e, tag, "cpu").numpy()
+        return C.quantize_weight_fp8(raw) if fmt == "fp8" else C.quantize_nvfp4(raw)
+
+    jobs = [(e, tag, n, k) for e in used for tag, n, k in (("gateup", 2 * I, H), ("down", H, I))]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, C.hardware_threads())) as ex:
+        parts = list(ex.map(quantized, jobs))
+
+    def stack(which, n, k):
+        ps = parts[which::2]
         if fmt == "fp8":
-            if not parts:
+            if not ps:
                 return np.zeros((0, n, k), np.uint8), np.zeros((0, -(-n // 128), -(-k // 128)), np.float32)
-            return np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts])
-        if not parts:
+            return np.stack([p[0] for p in ps]), np.stack([p[1] for p in ps])
+        if not ps:
             return (np.zeros((0, n, k), np.uint8), np.zeros((0, n, -(-k // 16)), np.uint8),
                     np.zeros(0, np.float32))
-        return (np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]),
-                np.array([p[2] for p in parts], np.float32))
+        return (np.stack([p[0] for p in ps]), np.stack([p[1] for p in ps]),
+                np.array([p[2] for p in ps], np.float32))
 
-    H = x.shape[1]
-    I = bg.n // 2
-    bank_g, bank_d = stack(bg, 2 * I, H), stack(bd, H, I)
+    bank_g, bank_d = stack(0, 2 * I, H), stack(1, H, I)
+    del parts
     return lambda threads: C.moe_forward(x, ids_c, w, bank_g, bank_d, fmt=fmt, threads=threads)
 
 
@@ -865,15 +886,15 @@ def cpu_baseline(name, budget_s=20.0, min_s=10.0):
     token, so the sample's rows equal the full call's; NVFP4's tensor scales span the
     sample instead (the same work per token)."""
     T_full = WORKLOADS[name][0]
-    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(name, max_tokens=min(T_full, 8))
+    x, ids, w, T, fmt, used = _oracle_problem(name, max_tokens=min(T_full, 8))
     n = ids.shape[0]
-    T = T_full
     try:
         from oracle import cpu as C
-        run = _cpp_oracle_call(M, x, ids, w, bg, bd, fmt)
+        run = _cpp_oracle_call(x, ids, w, used, fmt, *WORKLOADS[name][1:3])
         threads = C.hardware_threads()
     except Exception as exc:  # noqa: BLE001 - the baseline leg only
         run, threads, why = None, 1, str(exc).splitlines()[0] if str(exc) else type(exc).__name__
+        M, bg, bd = _numpy_banks(name, used)
     t0 = time.perf_counter()
     done = 0
     while True:
@@ -950,18 +971,18 @@ def run_reference(args, rank, world):
                                  "sample": "whole calls (numpy, single thread)"},
                 "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     T_full = WORKLOADS[args.workload][0]
-    M, x, ids, w, bg, bd, T, fmt = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
-    T = T_full
+    x, ids, w, T, fmt, used = _oracle_problem(args.workload, max_tokens=min(T_full, 8))
     ns = ids.shape[0]
     try:
         from oracle import cpu as C
-        run = _cpp_oracle_call(M, x, ids, w, bg, bd, fmt)
+        run = _cpp_oracle_call(x, ids, w, used, fmt, *WORKLOADS[args.workload][1:3])
         threads = C.hardware_threads()
         per_step = ns
         what = f"each step: a call of the first {ns} of {T} tokens (C++ oracle, {threads} threads)"
     except Exception:  # noqa: BLE001 - the reference leg only
         run, threads, per_step = None, 1, 1
         what = f"each step: 1 of {T} tokens of one call (numpy oracle, one thread)"
+        M, bg, bd = _numpy_banks(args.workload, used)
 
     def step(i):
         if run is not None:

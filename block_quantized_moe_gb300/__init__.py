@@ -18,6 +18,8 @@ FTMOE_OK, FTMOE_INVALID_ARG, FTMOE_UNSUPPORTED, FTMOE_CUDA_ERROR, FTMOE_WORKSPAC
 FMT_FP8, FMT_NVFP4 = 0, 1
 ROUTES_GROUPED, ROUTES_SLOTS = 0, 1
 ERR_EXPERT_ID_RANGE, ERR_MAP_RANGE, ERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+OUT_BF16, OUT_FP16, OUT_FP32 = 0, 1, 2
+_OUT_DTYPES = {torch.bfloat16: OUT_BF16, torch.float16: OUT_FP16, torch.float32: OUT_FP32}
 
 c_i32, c_i64, c_ptr, c_size = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
 
@@ -49,7 +51,7 @@ class Tile(ctypes.Structure):
 class MoeShape(ctypes.Structure):
     _fields_ = [("tokens", c_i64), ("hidden", c_i64), ("inter", c_i64), ("topk", c_i32),
                 ("num_experts", c_i32), ("format", c_i32), ("tok_tile", c_i32), ("path", c_i32),
-                ("reserved", c_i32)]
+                ("out_dtype", c_i32)]
 
 
 class MoeArgs(ctypes.Structure):
@@ -60,7 +62,8 @@ class MoeArgs(ctypes.Structure):
 
 _LAYOUT_FIELDS = ["x_q", "x_scales", "x_gscale", "counts", "offsets", "dst2src", "route2dst",
                   "rows_q", "rows_scales", "gateup", "gateup_bytes", "act_q", "act_q_bytes",
-                  "act_scales", "act_scales_bytes", "act_gscale", "down", "down_bytes", "total"]
+                  "act_scales", "act_scales_bytes", "act_gscale", "down", "down_bytes", "partials",
+                  "partials_bytes", "counters", "counters_bytes", "total"]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -86,11 +89,13 @@ _SIGNATURES = [
     ("ftmoe_grouped_gemm_down", c_i32, [ctypes.POINTER(Act), ctypes.POINTER(Routes),
                                         ctypes.POINTER(ExpertBank), c_ptr, c_i64,
                                         ctypes.POINTER(Tile), c_ptr]),
-    ("ftmoe_combine", c_i32, [c_ptr, c_i64, c_ptr, c_ptr, c_ptr, c_i64, c_i32, c_i64, c_ptr, c_i64, c_ptr]),
+    ("ftmoe_combine", c_i32, [c_ptr, c_i64, c_ptr, c_ptr, c_ptr, c_i64, c_i32, c_i64, c_i32, c_ptr, c_i64,
+                              c_ptr]),
     ("ftmoe_forward_workspace_bytes", c_size, [ctypes.POINTER(MoeShape)]),
     ("ftmoe_forward_workspace_layout", c_i32, [ctypes.POINTER(MoeShape), ctypes.POINTER(WorkspaceLayout)]),
     ("ftmoe_moe_forward", c_i32, [ctypes.POINTER(MoeArgs), c_ptr, c_size, c_ptr]),
     ("ftmoe_moe_forward_noalloc", c_i32, [ctypes.POINTER(MoeArgs), c_ptr]),
+    ("ftmoe_selftest_wait_timeout", c_i32, [ctypes.c_uint64, c_ptr, c_ptr]),
     ("ftmoe_read_error_flags", c_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 ]
 
@@ -234,16 +239,28 @@ def ftmoe_silu_mul(gu, q, scales, global_scale=None, fmt=FMT_FP8, rows=None, row
         _stream(stream)))
 
 
+def out_dtype_code(out):
+    """ftmoe_out_dtype of an output tensor (bf16, fp16 or fp32)."""
+    if out.dtype not in _OUT_DTYPES:
+        raise ValueError(f"output dtype {out.dtype} is not one of bf16, fp16, fp32")
+    return _OUT_DTYPES[out.dtype]
+
+
 def ftmoe_combine(y, expert_ids, weights, out, route2dst=None, stream=None):
     T, topk = expert_ids.shape
     H = out.shape[1]
     _check("ftmoe_combine", lib().ftmoe_combine(
-        _p(y), y.stride(0), _p(route2dst), _p(expert_ids), _p(weights), T, topk, H, _p(out),
-        out.stride(0), _stream(stream)))
+        _p(y), y.stride(0), _p(route2dst), _p(expert_ids), _p(weights), T, topk, H, out_dtype_code(out),
+        _p(out), out.stride(0), _stream(stream)))
 
 
-def moe_shape(tokens, hidden, inter, topk, num_experts, fmt=FMT_FP8, tok_tile=0, path=0):
-    return MoeShape(tokens, hidden, inter, topk, num_experts, fmt, tok_tile, path, 0)
+def moe_shape(tokens, hidden, inter, topk, num_experts, fmt=FMT_FP8, tok_tile=0, path=0, out_dtype=OUT_BF16):
+    return MoeShape(tokens, hidden, inter, topk, num_experts, fmt, tok_tile, path, out_dtype)
+
+
+def _check_out(shape, out):
+    if out_dtype_code(out) != shape.out_dtype:
+        raise ValueError(f"output tensor is {out.dtype}, the shape says out_dtype {shape.out_dtype}")
 
 
 def ftmoe_forward_workspace_bytes(shape):
@@ -259,6 +276,7 @@ def ftmoe_forward_workspace_layout(shape):
 
 def ftmoe_moe_forward(shape, x, expert_ids, route_weights, bank_gateup, bank_down, out, workspace,
                       stream=None):
+    _check_out(shape, out)
     args = MoeArgs(shape, _p(x), x.stride(0), _p(expert_ids), _p(route_weights), bank_gateup,
                    bank_down, _p(out), out.stride(0))
     _check("ftmoe_moe_forward", lib().ftmoe_moe_forward(
@@ -268,9 +286,16 @@ def ftmoe_moe_forward(shape, x, expert_ids, route_weights, bank_gateup, bank_dow
 
 def ftmoe_moe_forward_noalloc(shape, x, expert_ids, route_weights, bank_gateup, bank_down, out, stream=None):
     """The fused forward with its intermediates in the library's own device array (no workspace)."""
+    _check_out(shape, out)
     args = MoeArgs(shape, _p(x), x.stride(0), _p(expert_ids), _p(route_weights), bank_gateup,
                    bank_down, _p(out), out.stride(0))
     _check("ftmoe_moe_forward_noalloc", lib().ftmoe_moe_forward_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+def ftmoe_selftest_wait_timeout(timeout_ns, elapsed_ns=None, stream=None):
+    """One bounded pipeline wait that nothing completes, given up after timeout_ns."""
+    _check("ftmoe_selftest_wait_timeout", lib().ftmoe_selftest_wait_timeout(
+        int(timeout_ns), _p(elapsed_ns), _stream(stream)))
 
 
 def ftmoe_read_error_flags():

@@ -175,14 +175,36 @@ cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, 
   return launch_kernel(amax_to_gscale_1, dim3(1), dim3(1), 0, st, true, gscale);
 }
 
-// ---- combine: out[t, h] = bf16( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
+// ---- combine: out[t, h] = round( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
+// Output element types: bf16 and fp16 (one round to nearest even of the fp32 sum) or fp32.
+struct OutBf16 {
+  using T = uint16_t;
+  static __device__ __forceinline__ uint16_t cvt(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+};
+struct OutF16 {
+  using T = uint16_t;
+  static __device__ __forceinline__ uint16_t cvt(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
+struct OutF32 {
+  using T = float;
+  static __device__ __forceinline__ float cvt(float v) { return v; }
+};
+
+// four outputs of one row, one vector store when aligned
+__device__ __forceinline__ void store4(uint16_t* o, const uint16_t* b) {
+  *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+}
+__device__ __forceinline__ void store4(float* o, const float* b) {
+  *reinterpret_cast<float4*>(o) = make_float4(b[0], b[1], b[2], b[3]);
+}
+
 // The slot ids, weights and rows of a token are loaded eight slots at a time with
 // independent loads, then accumulated in ascending slot order.
-template <bool kVec>
+template <bool kVec, typename Out>
 __global__ void __launch_bounds__(128) combine_kernel(
     const float* __restrict__ y, int64_t ld_y, const int32_t* __restrict__ route2dst,
     const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t tokens, int32_t topk,
-    int64_t hidden, uint16_t* __restrict__ out, int64_t ld_out) {
+    int64_t hidden, typename Out::T* __restrict__ out, int64_t ld_out) {
   pdl_wait();  // the predecessor's outputs are complete from here on
   pdl_trigger();
   const int64_t t = blockIdx.y;
@@ -232,13 +254,12 @@ __global__ void __launch_bounds__(128) combine_kernel(
       }
     }
   }
-  uint16_t b[4];
+  typename Out::T b[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
-  uint16_t* o = out + t * ld_out + h0;
+  for (int i = 0; i < 4; ++i) b[i] = Out::cvt(acc[i]);
+  typename Out::T* o = out + t * ld_out + h0;
   if (full) {
-    *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16),
-                                              (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+    store4(o, b);
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -246,26 +267,45 @@ __global__ void __launch_bounds__(128) combine_kernel(
   }
 }
 
-cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
-                           const int32_t* ids, const float* w, int64_t tokens, int32_t topk,
-                           int64_t hidden, uint16_t* out, int64_t ld_out, cudaStream_t st) {
+template <typename Out>
+static cudaError_t launch_combine_t(const float* y, int64_t ld_y, const int32_t* route2dst, const int32_t* ids,
+                                   const float* w, int64_t tokens, int32_t topk, int64_t hidden,
+                                   typename Out::T* out, int64_t ld_out, cudaStream_t st) {
   if (tokens > 65535) {
     // one launch per 65535-token slab keeps grid.y in range
     for (int64_t t0 = 0; t0 < tokens; t0 += 65535) {
       const int64_t tn = tokens - t0 < 65535 ? tokens - t0 : 65535;
-      cudaError_t e = launch_combine(y, ld_y, route2dst ? route2dst + t0 * topk : nullptr,
-                                     ids + t0 * topk, w + t0 * topk, tn, topk, hidden,
-                                     out + t0 * ld_out, ld_out, st);
+      cudaError_t e = launch_combine_t<Out>(y, ld_y, route2dst ? route2dst + t0 * topk : nullptr, ids + t0 * topk,
+                                            w + t0 * topk, tn, topk, hidden, out + t0 * ld_out, ld_out, st);
       if (e != cudaSuccess) return e;
       if (route2dst == nullptr) y += tn * topk * ld_y;
     }
     return cudaSuccess;
   }
-  const bool vec = (hidden % 4 == 0) && (ld_y % 4 == 0) && ((uintptr_t)y % 16 == 0) &&
-                   (ld_out % 4 == 0) && ((uintptr_t)out % 8 == 0);
+  constexpr int kOutBytes = (int)sizeof(typename Out::T);
+  const bool vec = (hidden % 4 == 0) && (ld_y % 4 == 0) && ((uintptr_t)y % 16 == 0) && (ld_out % 4 == 0) &&
+                   ((uintptr_t)out % (4 * kOutBytes) == 0);
   dim3 grid((unsigned)cdiv(hidden, 4 * 128), (unsigned)tokens);
-  return launch_kernel(vec ? combine_kernel<true> : combine_kernel<false>, grid, dim3(128), 0, st, true, y, ld_y,
-                       route2dst, ids, w, tokens, topk, hidden, out, ld_out);
+  return launch_kernel(vec ? combine_kernel<true, Out> : combine_kernel<false, Out>, grid, dim3(128), 0, st, true, y,
+                       ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
+}
+
+cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
+                           const int32_t* ids, const float* w, int64_t tokens, int32_t topk,
+                           int64_t hidden, int32_t out_dtype, void* out, int64_t ld_out, cudaStream_t st) {
+  switch (out_dtype) {
+    case FTMOE_OUT_BF16:
+      return launch_combine_t<OutBf16>(y, ld_y, route2dst, ids, w, tokens, topk, hidden,
+                                       static_cast<uint16_t*>(out), ld_out, st);
+    case FTMOE_OUT_FP16:
+      return launch_combine_t<OutF16>(y, ld_y, route2dst, ids, w, tokens, topk, hidden,
+                                      static_cast<uint16_t*>(out), ld_out, st);
+    case FTMOE_OUT_FP32:
+      return launch_combine_t<OutF32>(y, ld_y, route2dst, ids, w, tokens, topk, hidden, static_cast<float*>(out),
+                                      ld_out, st);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_act)

@@ -30,6 +30,7 @@ inline ftmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FTMOE_O
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 bool valid_format(int32_t f) { return f == FTMOE_FMT_FP8 || f == FTMOE_FMT_NVFP4; }
+bool valid_out_dtype(int32_t d) { return d == FTMOE_OUT_BF16 || d == FTMOE_OUT_FP16 || d == FTMOE_OUT_FP32; }
 
 // bytes of one quantized row of k elements and of its scale row
 size_t code_row_bytes(int32_t fmt, int64_t k) { return fmt == FTMOE_FMT_FP8 ? (size_t)k : (size_t)(k / 2); }
@@ -215,14 +216,17 @@ ftmoe_status gateup_silu(const ftmoe_act* a, const ftmoe_routes* routes, const f
 struct Layout {
   ftmoe_workspace_layout l;
   bool grouped;
-  bool fused;  // SiLU-and-mul inside the gate/up GEMM: no fp32 gate/up buffer
+  bool fused;   // SiLU-and-mul inside the gate/up GEMM: no fp32 gate/up buffer
+  bool decode;  // the fused decode path (prep launch + one persistent kernel)
+  DecodePlan plan;
 };
 
 ftmoe_status check_shape(const ftmoe_moe_shape* s) {
   if (!s) return FTMOE_INVALID_ARG;
   if (s->tokens < 0 || s->hidden <= 0 || s->inter <= 0 || s->topk <= 0 || s->num_experts <= 0)
     return FTMOE_INVALID_ARG;
-  if (!valid_format(s->format) || s->path < 0 || s->path > 3) return FTMOE_INVALID_ARG;
+  if (!valid_format(s->format) || s->path < 0 || s->path > 4 || !valid_out_dtype(s->out_dtype))
+    return FTMOE_INVALID_ARG;
   if (s->tok_tile != 0 && s->tok_tile != 16 && s->tok_tile != 32 && s->tok_tile != 64 && s->tok_tile != 128)
     return FTMOE_INVALID_ARG;
   if (s->format == FTMOE_FMT_NVFP4 && (s->hidden % 32 != 0 || s->inter % 32 != 0)) return FTMOE_INVALID_ARG;
@@ -233,7 +237,13 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
 // with four K blocks per TMA box, it matches the route-slot streaming kernel at one token
 // (49.6 vs 50.4 us for 8 active routes of 4096/1024) and beats it from two tokens on (68 vs
 // 86 us); the route-slot path stays available as path 1.
-bool use_grouped(const ftmoe_moe_shape* s) { return s->path != 1; }
+bool use_grouped(const ftmoe_moe_shape* s) { return s->path != 1 && s->path != 4; }
+
+// The fused decode path: one persistent kernel after the quantizing launch (path 4).
+bool use_decode(const ftmoe_moe_shape* s) {
+  if (s->format != FTMOE_FMT_FP8 || s->path != 4) return false;
+  return decode_plan(s->tokens, s->topk, s->num_experts, s->hidden, s->inter).ok;
+}
 
 // When the automatic path fuses SiLU-and-mul into the gate/up GEMM. Measured on GB300:
 //  - A fused unit is twice as large as a one-block unit, so with few units per SM the CTAs
@@ -260,8 +270,6 @@ bool use_fused(const ftmoe_moe_shape* s) {
 Layout make_layout(const ftmoe_moe_shape* s) {
   Layout L;
   memset(&L, 0, sizeof(L));
-  L.grouped = use_grouped(s);
-  L.fused = L.grouped && use_fused(s);
   const int64_t T = s->tokens, H = s->hidden, I = s->inter, R = T * s->topk, E = s->num_experts;
   const int32_t f = s->format;
   size_t off = 0;
@@ -270,6 +278,28 @@ Layout make_layout(const ftmoe_moe_shape* s) {
     off += align256(bytes);
     return o;
   };
+  L.decode = use_decode(s);
+  if (L.decode) {
+    // token rows padded to the MMA's 16 columns, the re-quantized intermediate and the down
+    // rows per route, the gate/up partial sums and the arrival counters
+    L.plan = decode_plan(T, s->topk, (int32_t)E, H, I);
+    L.l.x_q = take(16 * H);
+    L.l.x_scales = take(16 * (H / 128) * 4);
+    L.l.act_q_bytes = R * I;
+    L.l.act_q = take(L.l.act_q_bytes);
+    L.l.act_scales_bytes = R * (I / 128) * 4;
+    L.l.act_scales = take(L.l.act_scales_bytes);
+    L.l.down_bytes = (size_t)R * H * 4;
+    L.l.down = take(L.l.down_bytes);
+    L.l.partials_bytes = L.plan.part_bytes;
+    L.l.partials = take(L.l.partials_bytes);
+    L.l.counters_bytes = L.plan.cnt_words * 4;
+    L.l.counters = take(L.l.counters_bytes);
+    L.l.total = off;
+    return L;
+  }
+  L.grouped = use_grouped(s);
+  L.fused = L.grouped && use_fused(s);
   L.l.x_q = take(T * code_row_bytes(f, H));
   L.l.x_scales = take(T * scale_row_bytes(f, H));
   L.l.x_gscale = take(16);
@@ -407,12 +437,13 @@ ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_
 
 ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
                            const int32_t* expert_ids, const float* weights, int64_t tokens,
-                           int32_t topk, int64_t hidden, uint16_t* out, int64_t ld_out,
-                           void* stream) {
+                           int32_t topk, int64_t hidden, int32_t out_dtype, void* out,
+                           int64_t ld_out, void* stream) {
   if (tokens < 0 || topk <= 0 || hidden <= 0 || ld_y < hidden || ld_out < hidden) return FTMOE_INVALID_ARG;
+  if (!valid_out_dtype(out_dtype)) return FTMOE_INVALID_ARG;
   if (tokens == 0) return FTMOE_OK;
   if (!y || !expert_ids || !weights || !out) return FTMOE_INVALID_ARG;
-  return from_cuda(launch_combine(y, ld_y, route2dst, expert_ids, weights, tokens, topk, hidden, out,
+  return from_cuda(launch_combine(y, ld_y, route2dst, expert_ids, weights, tokens, topk, hidden, out_dtype, out,
                                   ld_out, as_stream(stream)));
 }
 
@@ -453,6 +484,7 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   if (!workspace) return FTMOE_INVALID_ARG;
   if (workspace_bytes < L.l.total) return FTMOE_WORKSPACE_TOO_SMALL;
   if (f == FTMOE_FMT_NVFP4 && !L.grouped) return FTMOE_UNSUPPORTED;  // no route-slot kernel for e2m1
+  if (s->path == 4 && !L.decode) return FTMOE_UNSUPPORTED;           // outside the fused decode limits
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t R = T * s->topk;
@@ -478,6 +510,41 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   if (prep && R > 0x7fffffff) return FTMOE_UNSUPPORTED;
 
   OverlapScope overlap;
+  if (L.decode) {
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.l.counters);
+    st = from_cuda(launch_decode_prep(args->x, T, H, args->ld_x, xq, static_cast<float*>(xs), args->expert_ids,
+                                      s->topk, (int32_t)E, cnt, L.plan.cnt_words, args->out, args->ld_out,
+                                      s->out_dtype, strm));
+    if (st != FTMOE_OK) return st;
+    overlap.enable();
+    DecodeArgs d;
+    memset(&d, 0, sizeof(d));
+    d.x_q = xq;
+    d.x_s = static_cast<const float*>(xs);
+    d.ids = args->expert_ids;
+    d.rw = args->route_weights;
+    d.wg_q = wg.q;
+    d.wg_s = static_cast<const float*>(wg.scales);
+    d.wd_q = wd.q;
+    d.wd_s = static_cast<const float*>(wd.scales);
+    d.act_q = aq;
+    d.act_s = static_cast<float*>(as);
+    d.y = y;
+    d.part = reinterpret_cast<float*>(ws + L.l.partials);
+    d.cnt = cnt;
+    d.out = args->out;
+    d.ld_out = args->ld_out;
+    d.out_dtype = s->out_dtype;
+    d.T = T;
+    d.H = H;
+    d.I = I;
+    d.topk = s->topk;
+    d.E = (int32_t)E;
+    int unsupported = 0;
+    const cudaError_t e = launch_decode_fused(d, L.plan, strm, &unsupported);
+    if (unsupported) return FTMOE_UNSUPPORTED;
+    return from_cuda(e);
+  }
   if (prep)
     st = from_cuda(launch_prep_fp8(args->x, T, H, args->ld_x, xq, static_cast<float*>(xs), args->expert_ids, R,
                                    s->topk, (int32_t)E, counts, offsets, dst2src, route2dst, strm));
@@ -500,7 +567,7 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
     ftmoe_act a2 = {f, 0, R, I, aq, as, ag};
     st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
     if (st != FTMOE_OK) return st;
-    return ftmoe_combine(y, H, nullptr, args->expert_ids, args->route_weights, T, s->topk, H,
+    return ftmoe_combine(y, H, nullptr, args->expert_ids, args->route_weights, T, s->topk, H, s->out_dtype,
                          args->out, args->ld_out, stream);
   }
   uint8_t* rq = ws + L.l.rows_q;
@@ -529,7 +596,7 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   ftmoe_act a2 = {f, 0, R, I, aq, as, ag};
   st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
   if (st != FTMOE_OK) return st;
-  return ftmoe_combine(y, H, route2dst, args->expert_ids, args->route_weights, T, s->topk, H,
+  return ftmoe_combine(y, H, route2dst, args->expert_ids, args->route_weights, T, s->topk, H, s->out_dtype,
                        args->out, args->ld_out, stream);
 }
 
@@ -537,7 +604,7 @@ ftmoe_status ftmoe_read_error_flags(uint32_t* flags) {
   if (!flags) return FTMOE_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return FTMOE_CUDA_ERROR;
   *flags = read_err_quant() | read_err_segment() | read_err_gather() | read_err_stream_gemm() |
-           read_err_tc_gemm() | read_err_nvfp4() | read_err_act();
+           read_err_tc_gemm() | read_err_nvfp4() | read_err_act() | read_err_selftest() | read_err_decode();
   return FTMOE_OK;
 }
 

@@ -163,7 +163,51 @@ cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, 
                                   float* gscale, cudaStream_t s);
 cudaError_t launch_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
                            const int32_t* ids, const float* w, int64_t tokens, int32_t topk,
-                           int64_t hidden, uint16_t* out, int64_t ld_out, cudaStream_t s);
+                           int64_t hidden, int32_t out_dtype, void* out, int64_t ld_out, cudaStream_t s);
 uint32_t read_err_act();
+
+// selftest.cu
+uint32_t read_err_selftest();
+
+// decode_fused.cu: the fused decode forward (prep launch + one persistent kernel)
+constexpr int kDecodeMaxTokens = 8;     // token columns the kernel keeps
+constexpr int kDecodeMaxRoutes = 64;    // tokens * topk
+constexpr int kDecodeMaxExperts = 1024; // bitmap of active experts
+constexpr int kDecodeGrid = 152;        // persistent CTAs (at most; one per SM)
+struct DecodePlan {
+  bool ok;
+  int KB, KB2, NJ, NB, HB;  // H/128, I/128, I/128, 2I/128, H/128
+  int kbs_g, kbs_d;         // K blocks per TMA stage (gate/up, down)
+  int u_max;                // most distinct experts the routes can reach
+  int spc;                  // partial-sum slots per CTA (for kDecodeGrid CTAs)
+  size_t part_bytes;        // partial sums [kDecodeGrid * spc][8][128] float
+  size_t cnt_words;         // counters: pairs, experts, (token, H block)
+};
+DecodePlan decode_plan(int64_t T, int32_t topk, int32_t E, int64_t H, int64_t I);
+struct DecodeArgs {
+  const uint8_t* x_q;   // [16][H] (rows >= T zero), from the prep launch
+  const float* x_s;     // [16][H/128]
+  const int32_t* ids;
+  const float* rw;
+  const uint8_t* wg_q;
+  const float* wg_s;
+  const uint8_t* wd_q;
+  const float* wd_s;
+  uint8_t* act_q;       // [T*topk][I]
+  float* act_s;         // [T*topk][I/128]
+  float* y;             // [T*topk][H]
+  float* part;
+  uint32_t* cnt;
+  void* out;
+  int64_t ld_out;
+  int32_t out_dtype;
+  int64_t T, H, I;
+  int32_t topk, E;
+};
+cudaError_t launch_decode_prep(const uint16_t* x, int64_t T, int64_t H, int64_t ld_x, uint8_t* xq, float* xs,
+                               const int32_t* ids, int32_t topk, int32_t E, uint32_t* cnt, size_t ncnt, void* out,
+                               int64_t ld_out, int32_t out_dtype, cudaStream_t s);
+cudaError_t launch_decode_fused(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s, int* unsupported);
+uint32_t read_err_decode();
 
 }  // namespace ftmoe

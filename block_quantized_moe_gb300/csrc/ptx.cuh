@@ -52,14 +52,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete. Returns false (and raises the
+// Bounded wait for the phase of `parity` to complete, giving up after limit_ns (the
+// pipelines use the 4 s default). Returns false (and raises FTMOE_ERR_WAIT_TIMEOUT and the
 // abort flag) on timeout, or if another role already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kTimeoutNs) {
+    if (globaltimer() - t0 > limit_ns) {
       raise_error(FTMOE_ERR_WAIT_TIMEOUT);
       *abort_flag = 1;
       return false;

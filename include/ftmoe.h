@@ -64,6 +64,16 @@ typedef enum ftmoe_format {
   FTMOE_FMT_NVFP4 = 1
 } ftmoe_format;
 
+/* Element type of the forward's output rows (FreeToken "perf(moe): skip inactive block-fp8
+ * decode routes", Validation: bf16, fp16 and fp32 outputs). The combine accumulates in fp32
+ * either way; bf16 and fp16 are rounded to nearest even once at the end, fp32 is stored as
+ * accumulated. */
+typedef enum ftmoe_out_dtype {
+  FTMOE_OUT_BF16 = 0,
+  FTMOE_OUT_FP16 = 1,
+  FTMOE_OUT_FP32 = 2
+} ftmoe_out_dtype;
+
 /* Device error word bits (see ftmoe_read_error_flags). */
 #define FTMOE_ERR_EXPERT_ID_RANGE 0x1u  /* an expert id >= num_experts was skipped */
 #define FTMOE_ERR_MAP_RANGE 0x2u        /* a dst2src entry outside [0, n_src) was skipped */
@@ -235,16 +245,19 @@ ftmoe_status ftmoe_grouped_gemm_down(const ftmoe_act* a, const ftmoe_routes* rou
                                      const ftmoe_expert_bank* w, float* out, int64_t ld_out,
                                      const ftmoe_tile* tile, void* stream);
 
-/* Routing-weighted top-k combine:
- *   out[t, h] = bf16_rne( sum_{j ascending, expert_ids[t*topk+j] >= 0}
- *                         weights[t*topk+j] * y[row(t*topk+j), h] )   (fp32 accumulate)
- * row(r) = route2dst[r] if route2dst != NULL, else r (route-major y). Inactive slots
- * are skipped without reading their weight or y row. y float [*, hidden] with row
- * stride ld_y; out bf16 [tokens, hidden] with row stride ld_out. */
+/* Routing-weighted top-k combine (FreeToken "perf(moe): skip inactive block-fp8 decode
+ * routes", first section: the reduction that follows the down GEMM; it reads no routing
+ * weight of an inactive route):
+ *   out[t, h] = round( sum_{j ascending, expert_ids[t*topk+j] >= 0}
+ *                      weights[t*topk+j] * y[row(t*topk+j), h] )   (fp32 accumulate)
+ * round = out_dtype's conversion (ftmoe_out_dtype: bf16 or fp16 round to nearest even, fp32
+ * none). row(r) = route2dst[r] if route2dst != NULL, else r (route-major y). Inactive slots
+ * are skipped without reading their weight or y row. y float [*, hidden] with row stride
+ * ld_y; out [tokens, hidden] of out_dtype with row stride ld_out (elements). */
 ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2dst,
                            const int32_t* expert_ids, const float* weights, int64_t tokens,
-                           int32_t topk, int64_t hidden, uint16_t* out, int64_t ld_out,
-                           void* stream);
+                           int32_t topk, int64_t hidden, int32_t out_dtype, void* out,
+                           int64_t ld_out, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Fused forward (FreeToken "perf(moe): skip inactive block-fp8 decode routes": first
@@ -255,12 +268,17 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * and inputs change in place.
  * path: 0 = automatic, 1 = route-slot streaming path (FP8 only), 2 = grouped path with
  * the separate SiLU-and-mul kernel, 3 = grouped path with SiLU-and-mul fused into the
- * gate/up GEMM (ftmoe_grouped_gemm_gateup_silu; FP8, I % 128 == 0, H % 128 == 0).
- * Automatic: the grouped path at every batch size, fused where the token tile is at most
- * 64, the bank has at most 1024 experts and the routes can reach at least 2048 (expert,
- * gate/up block pair) units
- * (min(T*topk, E) * I/128 >= 2048), else with the separate kernel. Paths 2 and 3 give
- * bit-identical outputs.
+ * gate/up GEMM (ftmoe_grouped_gemm_gateup_silu; FP8, I % 128 == 0, H % 128 == 0),
+ * 4 = fused decode path: after a launch that quantizes the token rows, gate/up, SiLU-and-mul
+ * with FP8 re-quantization, down and the combine run in one persistent tensor-core kernel
+ * whose weight stream is split evenly over the SMs (FP8; T <= 8, T*topk <= 64, E <= 1024,
+ * H and I multiples of 128, H <= 8192, I <= 2048; at most 16 routes per expert, further
+ * routes to one expert are skipped and raise FTMOE_ERR_EXPERT_ID_RANGE).
+ * Automatic: the grouped path, fused where the token tile is at most 64, the bank has at
+ * most 1024 experts and the routes can reach at least 2048 (expert, gate/up block pair) units
+ * (min(T*topk, E) * I/128 >= 2048), else with the separate kernel. Paths 2 and 3 give bit-identical outputs; path 4 adds the partial
+ * sums of a gate/up element in another order, so it agrees with them within the fp32
+ * rounding of that sum.
  * ------------------------------------------------------------------------------------ */
 typedef struct ftmoe_moe_shape {
   int64_t tokens;     /* T */
@@ -271,7 +289,7 @@ typedef struct ftmoe_moe_shape {
   int32_t format;     /* ftmoe_format of weights and activations */
   int32_t tok_tile;   /* 0 = ftmoe_pick_tile(T*topk, E) */
   int32_t path;
-  int32_t reserved;
+  int32_t out_dtype;  /* ftmoe_out_dtype of out (0 = bf16) */
 } ftmoe_moe_shape;
 
 typedef struct ftmoe_moe_args {
@@ -282,7 +300,7 @@ typedef struct ftmoe_moe_args {
   const float* route_weights; /* float [T*topk]; entries of inactive routes are never read */
   ftmoe_expert_bank w_gateup; /* n = 2I, k = H */
   ftmoe_expert_bank w_down;   /* n = H, k = I */
-  uint16_t* out;              /* bf16 [T][ld_out] */
+  void* out;                  /* [T][ld_out] elements of shape.out_dtype */
   int64_t ld_out;
 } ftmoe_moe_args;
 
@@ -295,6 +313,8 @@ typedef struct ftmoe_workspace_layout {
   size_t gateup, gateup_bytes;               /* float gate/up output [R][2I] (not in path 3) */
   size_t act_q, act_q_bytes, act_scales, act_scales_bytes, act_gscale;
   size_t down, down_bytes;                   /* float down output [R][H] */
+  size_t partials, partials_bytes;           /* fused decode path: gate/up partial sums */
+  size_t counters, counters_bytes;           /* fused decode path: arrival counters */
   size_t total;
 } ftmoe_workspace_layout;
 
@@ -322,6 +342,17 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
  * call's contents are never used. No cudaMalloc, cudaFree or allocating library routine is
  * called. Inputs, outputs and their ownership are as for ftmoe_moe_forward. */
 ftmoe_status ftmoe_moe_forward_noalloc(const ftmoe_moe_args* args, void* stream);
+
+/* Self-test of the bounded pipeline waits (failure detection; the pages have no counterpart).
+ * Every wait of the TMA/tensor-core pipelines gives up after a time limit (4 s), raises
+ * FTMOE_ERR_WAIT_TIMEOUT in the device error word and lets its kernel return normally, so a
+ * stalled pipeline never hangs the GPU. This call launches one CTA whose single waiting
+ * thread runs that same bounded wait on a shared-memory mbarrier nothing ever arrives on,
+ * with the limit timeout_ns (1 us .. 1 s, else FTMOE_INVALID_ARG). The wait runs out, the
+ * kernel raises FTMOE_ERR_WAIT_TIMEOUT and returns; ftmoe_read_error_flags reports the bit.
+ * elapsed_ns: optional device pointer receiving the nanoseconds the wait took before it
+ * gave up (0 if it completed, which cannot happen). */
+ftmoe_status ftmoe_selftest_wait_timeout(uint64_t timeout_ns, unsigned long long* elapsed_ns, void* stream);
 
 /* Reads and clears the device error word of the current device (FTMOE_ERR_* bits) into
  * *flags (host pointer). Synchronises the device; not for use inside graph capture. */

@@ -14,26 +14,68 @@ from oracle import moe as M
 TOL_REL, TOL_ABS_OF_MAX = 2e-2, 1e-3
 
 
-def out_tolerance_violations(got, ref):
-    """Number of elements with |got - ref| > 2e-2 |ref| + 1e-3 max|ref|, and the worst excess."""
+# The re-quantization allowance (requant_flip_bound, nvfp4_requant_flip_bound) may carry at
+# most this share of a call's output elements; every other element meets the stated
+# tolerance on its own.
+ALLOWANCE_SHARE_LIMIT = 1e-3
+
+
+def _log():
+    """Session-wide record of the output checks, read by the terminal summary in conftest.py
+    (kept under one sys.modules key, whichever name this module was imported by)."""
+    import sys
+    import types
+    mod = sys.modules.get("_ftmoe_check_log")
+    if mod is None:
+        mod = types.ModuleType("_ftmoe_check_log")
+        mod.checks, mod.measures = [], []
+        sys.modules["_ftmoe_check_log"] = mod
+    return mod
+
+
+def _test_name():
+    import os
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+
+
+def record_measure(what, value, bound):
+    """A measured quantity held to a stated bound (e.g. a GEMM's largest relative error)."""
+    _log().measures.append(dict(test=_test_name(), what=what, value=float(value), bound=float(bound)))
+
+
+def tolerance_report(got, ref, extra=0.0):
+    """Counts of a comparison with the stated tolerance |got - ref| <= 2e-2 |ref| + 1e-3 max|ref|:
+    elements; elements outside it; of those, elements inside it plus the allowance `extra`
+    (they pass only because of the allowance); elements outside both; the largest
+    |got - ref| / tolerance among the allowance-carried elements."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     tol = TOL_REL * np.abs(ref) + TOL_ABS_OF_MAX * (np.max(np.abs(ref)) if ref.size else 0.0)
-    excess = np.abs(got - ref) - tol
-    return int(np.sum(excess > 0)), float(np.max(excess)) if excess.size else 0.0
+    err = np.abs(got - ref)
+    plain = err > tol
+    fail = err > tol + extra
+    carried = plain & ~fail
+    worst = float(np.max(err[carried] / tol[carried])) if carried.any() else 0.0
+    worst_fail = float(np.max(err[fail] - (tol + np.broadcast_to(extra, err.shape))[fail])) if fail.any() else 0.0
+    return dict(n=int(err.size), outside_tolerance=int(plain.sum()), carried_by_allowance=int(carried.sum()),
+                failing=int(fail.sum()), max_err_over_tol_carried=worst, worst_excess=worst_fail)
 
 
-def out_tolerance_violations_extra(got, ref, extra):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    tol = TOL_REL * np.abs(ref) + TOL_ABS_OF_MAX * (np.max(np.abs(ref)) if ref.size else 0.0) + extra
-    excess = np.abs(got - ref) - tol
-    return int(np.sum(excess > 0)), float(np.max(excess)) if excess.size else 0.0
+def out_tolerance_violations(got, ref):
+    """Number of elements with |got - ref| > 2e-2 |ref| + 1e-3 max|ref|, and the worst excess."""
+    r = tolerance_report(got, ref)
+    return r["failing"], r["worst_excess"]
 
 
 def assert_within_tolerance(got, ref, what="output", extra=0.0):
-    n, worst = out_tolerance_violations_extra(got, ref, extra)
-    assert n == 0, f"{what}: {n} elements outside tolerance (worst excess {worst:.3e})"
+    """Every element within the stated tolerance plus `extra` (the re-quantization allowance,
+    zero by default), and at most ALLOWANCE_SHARE_LIMIT of the elements needing the
+    allowance at all. The counts go to the session's check record."""
+    r = tolerance_report(got, ref, extra)
+    _log().checks.append(dict(test=_test_name(), what=what, **r))
+    assert r["failing"] == 0, f"{what}: {r['failing']} elements outside tolerance (worst excess {r['worst_excess']:.3e})"
+    assert r["carried_by_allowance"] <= ALLOWANCE_SHARE_LIMIT * r["n"], (
+        f"{what}: {r['carried_by_allowance']} of {r['n']} elements pass only with the re-quantization allowance")
 
 
 # Relative bound on the kernels' fp32 error in a gate/up output element, as a fraction of
@@ -261,19 +303,22 @@ class Problem:
         extra = bound(res, ids.cpu().numpy(), wv, self.obank_gu, self.obank_dn)
         got = out.float().cpu().numpy()
         rows = list(range(self.T)) if tokens_subset is None else list(tokens_subset)
-        assert_within_tolerance(got[rows], ref[rows], extra=extra[rows])
+        what = (f"{self.fmt} forward T={self.T} H={self.H} I={self.I} E={self.E} top-{self.topk}"
+                + ("" if tokens_subset is None else f" ({len(rows)}-token sample)"))
+        assert_within_tolerance(got[rows], ref[rows], what=what, extra=extra[rows])
         return ref
 
-    def forward(self, path=0, tok_tile=0, ids=None, weights=None, x=None, out=None, ws=None):
+    def forward(self, path=0, tok_tile=0, ids=None, weights=None, x=None, out=None, ws=None,
+                out_dtype=torch.bfloat16):
         import block_quantized_moe_gb300 as ft
         ids = self.ids if ids is None else ids
         weights = self.w if weights is None else weights
         x = self.x if x is None else x
+        if out is None:
+            out = torch.empty(self.T, self.H, dtype=out_dtype, device=self.dev)
         shape = ft.moe_shape(self.T, self.H, self.I, self.topk, self.E, fmt=self.ft_fmt, tok_tile=tok_tile,
-                             path=path)
+                             path=path, out_dtype=ft.out_dtype_code(out))
         if ws is None:
             ws = torch.empty(ft.ftmoe_forward_workspace_bytes(shape), dtype=torch.uint8, device=self.dev)
-        if out is None:
-            out = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=self.dev)
         ft.ftmoe_moe_forward(shape, x, ids, weights, self.bank_gu, self.bank_dn, out, ws)
         return out, ws, shape

@@ -73,8 +73,15 @@ def test_invalid_arguments_rejected_on_host(ft):
     assert L.ftmoe_gather_rows_scales(None, None, 5, 896, 28, None, 0, None, None, None, None) == ft.FTMOE_OK
     assert L.ftmoe_gather_rows_scales(None, None, 5, 896, 28, None, 3, None, None, None, None) == ft.FTMOE_INVALID_ARG
     assert L.ftmoe_segment_routes(None, 4, 2, 0, None, None, None, None, None) == ft.FTMOE_INVALID_ARG
-    assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, None, 16, None) == ft.FTMOE_OK
-    assert L.ftmoe_combine(None, 8, None, None, None, 2, 2, 16, None, 16, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, 0, None, 16, None) == ft.FTMOE_OK
+    assert L.ftmoe_combine(None, 8, None, None, None, 2, 2, 16, 0, None, 16, None) == ft.FTMOE_INVALID_ARG
+    # output element types: bf16, fp16, fp32; anything else is refused
+    for d in (ft.OUT_BF16, ft.OUT_FP16, ft.OUT_FP32):
+        assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, d, None, 16, None) == ft.FTMOE_OK
+    assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, 3, None, 16, None) == ft.FTMOE_INVALID_ARG
+    # the wait self-test takes a limit of 1 us .. 1 s
+    assert L.ftmoe_selftest_wait_timeout(999, None, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_selftest_wait_timeout(2 * 10 ** 9, None, None) == ft.FTMOE_INVALID_ARG
 
 
 def test_forward_workspace_layout(ft):
@@ -99,6 +106,21 @@ def test_forward_workspace_layout(ft):
     assert g["rows_q"] > 0 and g["dst2src"] > 0
     bad = ft.moe_shape(8, 4096, 1024, 8, 64, tok_tile=48)
     assert ft.ftmoe_forward_workspace_bytes(bad) == 0
+    assert ft.ftmoe_forward_workspace_bytes(ft.moe_shape(8, 4096, 1024, 8, 64, out_dtype=3)) == 0
+    # the output element type does not change the workspace
+    sizes = {ft.ftmoe_forward_workspace_bytes(ft.moe_shape(8, 4096, 1024, 8, 64, out_dtype=d))
+             for d in (ft.OUT_BF16, ft.OUT_FP16, ft.OUT_FP32)}
+    assert len(sizes) == 1 and sizes.pop() > 0
+
+
+def test_binding_checks_the_output_tensor_against_the_shape(ft):
+    import torch
+    shape = ft.moe_shape(2, 256, 128, 2, 4, out_dtype=ft.OUT_FP16)
+    with pytest.raises(ValueError):
+        ft._check_out(shape, torch.empty(2, 256, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        ft.out_dtype_code(torch.empty(2, 256, dtype=torch.float64))
+    ft._check_out(shape, torch.empty(2, 256, dtype=torch.float16))
 
 
 def test_forward_rejects_inconsistent_banks(ft):
@@ -135,7 +157,26 @@ def test_automatic_forward_path_choice(ft):
     assert lay(ft.moe_shape(2048, 7168, 2048, 6, 2048))["gateup_bytes"] > 0  # beyond the GEMM's 1024 experts
     assert lay(ft.moe_shape(1, 2048, 768, 8, 8, path=3))["gateup_bytes"] == 0
     with pytest.raises(ft.FtmoeError):
-        lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4))
+        lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=5))
+
+
+def test_fused_decode_workspace(ft):
+    # path 4: token rows padded to 16, the intermediate and the down rows per route, the
+    # gate/up partial sums and the arrival counters; no gather or fp32 gate/up rows
+    lay = ft.ftmoe_forward_workspace_layout
+    d = lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4))
+    R = 64
+    assert d["gateup_bytes"] == 0 and d["rows_q"] == 0 and d["dst2src"] == 0
+    assert d["act_q_bytes"] == R * 1024 and d["act_scales_bytes"] == R * 8 * 4 and d["down_bytes"] == R * 4096 * 4
+    assert d["partials_bytes"] > 0 and d["counters_bytes"] == 4 * (64 * 8 + 64 + 8 * 32)
+    for key in ("x_q", "x_scales", "act_q", "act_scales", "down", "partials", "counters"):
+        assert d[key] % 256 == 0
+    assert d["total"] <= 8 << 20  # the decode shapes still fit the allocation-free forward's array
+    # outside its limits (more than 8 tokens, NVFP4, I > 2048) the path is unsupported: the
+    # layout falls back to another path's and the forward refuses path 4
+    assert lay(ft.moe_shape(9, 4096, 1024, 8, 64, path=4))["partials_bytes"] == 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=4, fmt=ft.FMT_NVFP4))["partials_bytes"] == 0
+    assert lay(ft.moe_shape(8, 4096, 4096, 8, 64, path=4))["partials_bytes"] == 0
 
 
 def test_two_block_and_fused_gemm_host_checks(ft):

@@ -35,6 +35,7 @@ def test_recorded_traffic_entries_are_well_formed():
 
 def test_vs_baseline_only_for_workloads_the_pages_time():
     assert bench.vs_pages("decode-h4096-i1024-e64-t8-a8", 118.0) is None  # no page number
+    assert bench.vs_pages(bench.DEFAULT_WORKLOAD, 3000.0) is None
     assert bench.vs_pages("decode-h2048-i768-e8-t1-a2", 60.589) == 1.0
     assert bench.vs_pages("gather-k7168-t1024", 5.57) == 0.5
     for name in bench.PAGES_US:
@@ -52,14 +53,15 @@ def test_cpu_baseline_oracle_call_equals_the_numpy_oracle():
     x = synth.activations_bf16(T, H, seed, "cpu").float().numpy()
     ids = synth.routes(T, k, E, seed, active_per_token=[3, 2, 0, 3], device="cpu").numpy()
     w = synth.routing_weights(T, k, seed, "cpu").numpy()
+    used = sorted(set(int(e) for e in ids.reshape(-1) if e >= 0))
     for fmt in ("fp8", "nvfp4"):
         bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
         bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
-        got = bench._cpp_oracle_call(M, x, ids, w, bg, bd, fmt)(4)
+        got = bench._cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=seed)(4)
         ref = M.moe_forward(x, ids, w, bg, bd, fmt=fmt)["out"]
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-14 * np.abs(ref).max())
         none = np.full_like(ids, -1)
-        assert not bench._cpp_oracle_call(M, x, none, w, bg, bd, fmt)(2).any()
+        assert not bench._cpp_oracle_call(x, none, w, [], fmt, H, I, seed=seed)(2).any()
 
 
 def test_cpu_baseline_uses_the_cpp_oracle_and_falls_back_to_numpy(monkeypatch):

@@ -8,7 +8,7 @@ import pytest
 
 import synth
 from common import nvfp4_requant_flip_bound, requant_flip_bound
-from fullsize_oracle import forward_subsample
+from fullsize_oracle import forward_calls, forward_subsample
 from oracle import moe as M
 
 
@@ -31,3 +31,21 @@ def test_driver_equals_the_oracle_forward(fmt):
     bound = requant_flip_bound if fmt == "fp8" else nvfp4_requant_flip_bound
     ref_extra = bound(res, ids, wv, bg, bd)
     assert np.allclose(extra[sub], ref_extra[sub], rtol=1e-6, atol=1e-12 * scale)
+
+
+def test_driver_calls_sharing_one_bank_equal_separate_runs():
+    # two calls on one bank in the same passes give each call's own rows (NVFP4: each call's
+    # tensor scales are its own)
+    H, I, E, k, seed = 256, 128, 5, 2, 91
+    calls = []
+    for T, s in ((7, 1), (10, 2)):
+        x = synth.activations_bf16(T, H, seed + s, "cpu").float().numpy()
+        ids = synth.routes(T, k, E, seed + s, device="cpu").numpy()
+        w = synth.routing_weights(T, k, seed + s, "cpu").numpy()
+        calls.append(dict(x32=x, ids=ids, weights=w, checked=list(range(0, T, 2))))
+    for fmt in ("fp8", "nvfp4"):
+        both = forward_calls(calls, H, I, E, seed, fmt, workers=2)
+        for c, (out, extra) in zip(calls, both):
+            one, one_extra = forward_subsample(c["x32"], c["ids"], c["weights"], c["checked"], H, I, E, seed, fmt,
+                                               workers=2)
+            assert np.array_equal(out, one) and np.array_equal(extra, one_extra)

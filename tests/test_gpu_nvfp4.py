@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import synth
-from common import NVFP4_SUM_REL, Problem
+from common import NVFP4_SUM_REL, Problem, record_measure
 from oracle import formats as F
 from oracle import moe as M
 
@@ -150,14 +150,22 @@ def test_grouped_gemm_nvfp4_vs_oracle(ft, tile):
     adeq = M.dequant_nvfp4(M.unpack_e2m1(aq.numpy(), k), asf.numpy(), ga.numpy()[0])
     wdeq = M.dequant_nvfp4(M.unpack_e2m1(wq.numpy(), k), wsf.numpy(), 1.0).reshape(E, n, k)
     off = offsets.cpu().numpy()
+    worst = 0.0
     for e in range(E):
         rows = slice(off[e], off[e + 1])
         if off[e] == off[e + 1]:
             continue
         ref = M.gemm_rows(adeq[rows], wdeq[e]) * np.float64(gw[e])
-        bound = NVFP4_SUM_REL * (np.abs(adeq[rows]) @ np.abs(wdeq[e]).T) * float(gw[e]) + 2.0 ** -21 * np.abs(ref)
+        absum = (np.abs(adeq[rows]) @ np.abs(wdeq[e]).T) * float(gw[e])
+        bound = NVFP4_SUM_REL * absum + 2.0 ** -21 * np.abs(ref)
         err = np.abs(got[rows] - ref)
         assert np.all(err <= bound + 1e-30), (e, float(np.max(err - bound)))
+        nz = absum > 0
+        if nz.any():
+            worst = max(worst, float(np.max(err[nz] / absum[nz])))
+    # the block-scaled MMA's measured error, as a share of the sum of the magnitudes of the
+    # products, against the allowance the forward checks take for it
+    record_measure(f"NVFP4 block-scaled GEMM max |err| / sum|products| (token tile {tile})", worst, NVFP4_SUM_REL)
 
 
 def test_grouped_gemm_nvfp4_rejects_slots_and_unaligned_k(ft):
