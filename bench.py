@@ -59,6 +59,9 @@ WORKLOADS = {
     "decode-h4096-i1024-e64-t2-a8": (2, 4096, 1024, 64, 8, 8, 0),
     "decode-h4096-i1024-e64-t2-a8-slots": (2, 4096, 1024, 64, 8, 8, 1),
     "decode-h4096-i1024-e64-t8-a8-sep": (8, 4096, 1024, 64, 8, 8, 2),
+    # path 4: the fused decode kernel (gate/up, SiLU-and-mul, down and combine in one launch)
+    **{f"decode-h4096-i1024-e64-t{t}-a{a}-dk": (t, 4096, 1024, 64, 8, a, 4) for t in (1, 8) for a in (8, 4, 2, 0)},
+    "decode-h2048-i768-e8-t1-a2-dk": (1, 2048, 768, 8, 8, 2, 4),
     "prefill-fp8-h7168-i2048-e256-r1536": (256, 7168, 2048, 256, 6, 6, 0),
     "prefill-fp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 0),
     "prefill-fp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 0),
@@ -104,7 +107,8 @@ PAGES_US = {
 
 
 def vs_pages(workload, value_us):
-    ref = PAGES_US.get(workload)
+    # the same workload on another forward path of this library has the same page number
+    ref = PAGES_US.get(workload[:-3] if workload.endswith("-dk") else workload)
     return None if ref is None else round(value_us / ref, 4)
 
 
@@ -382,8 +386,10 @@ class MoeWorkload:
         # the path the library takes (path 0 is its automatic choice): the route-slot path,
         # or the grouped path with SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up
         # buffer in the workspace) or in its own kernel
-        self.grouped = path != 1
-        self.fused = self.grouped and ft.ftmoe_forward_workspace_layout(self.shape)["gateup_bytes"] == 0
+        lay = ft.ftmoe_forward_workspace_layout(self.shape)
+        self.decode = lay["partials_bytes"] > 0  # the fused decode kernel (path 4)
+        self.grouped = path != 1 and not self.decode
+        self.fused = self.grouped and lay["gateup_bytes"] == 0
         self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
         self.x_in = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
@@ -396,6 +402,8 @@ class MoeWorkload:
         self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) -
                                   (1 if self.grouped and self.fmt == "fp8" else 0) +
                                   (4 if self.fmt == "nvfp4" else 0))
+        if self.decode:
+            self.launches_per_step = 2  # quantize, then the fused kernel
 
     # algorithmic bytes/flops of one forward on route set i
     def work(self, i):
@@ -409,6 +417,17 @@ class MoeWorkload:
         row = lambda n: code_bytes(f, n) + scale_bytes(f, n)  # noqa: E731 - one quantized row
         w_gu = weight_bytes(f, 2 * I, H)
         w_dn = weight_bytes(f, H, I)
+        if self.decode:
+            # token rows in, each distinct expert's weights once, the intermediate and down
+            # rows of the active routes written and read back once, the output written
+            row = lambda n: code_bytes(f, n) + scale_bytes(f, n)  # noqa: E731
+            w_gu = weight_bytes(f, 2 * I, H)
+            w_dn = weight_bytes(f, H, I)
+            gateup = T * H * 2 + T * row(H) + uniq * w_gu + ra * row(I)
+            total = (T * H * 2 + T * row(H) + uniq * (w_gu + w_dn) + 2 * ra * row(I) + 2 * ra * H * 4 +
+                     T * k * 8 + T * H * 2)
+            return dict(bytes=total, gateup_bytes=total, flops=2 * ra * (2 * I * H + H * I),
+                        gateup_flops=2 * ra * (2 * I * H + H * I), uniq=uniq, active=ra)
         out_rows = ra if self.grouped else R     # the route-slot path also writes zero rows
         if self.fused:   # gate/up + SiLU-and-mul: writes the re-quantized rows, no fp32 rows
             gateup = uniq * w_gu + ra * row(H) + ra * row(I)
@@ -440,8 +459,11 @@ class MoeWorkload:
                                   self.out, self.ws, stream=stream)
 
     def dominant_kernel(self):
-        """The gate/up GEMM alone, on the rows the forward left in the workspace."""
+        """The gate/up GEMM alone, on the rows the forward left in the workspace; on the fused
+        decode path the whole forward (its quantizing launch and the fused kernel)."""
         ft = self.ft
+        if self.decode:
+            return "decode_fused_kernel (+ its quantizing launch; the whole forward)", self.forward
         lay = ft.ftmoe_forward_workspace_layout(self.shape)
         T, H, k = self.T, self.H, self.k
         gu = self.ws[lay["gateup"]:lay["gateup"] + lay["gateup_bytes"]].view(torch.float32).view(T * k, -1)
@@ -660,7 +682,8 @@ def run_gpu(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
-                   "forward_path": ("route slots (streaming kernel)" if not wl.grouped else
+                   "forward_path": ("fused decode kernel (one launch after quantization)" if wl.decode else
+                                    "route slots (streaming kernel)" if not wl.grouped else
                                     "grouped, SiLU-and-mul fused into the gate/up GEMM" if wl.fused else
                                     "grouped, separate SiLU-and-mul kernel"),
                    "l2": L2Flush.DESC, "parallelism": f"replicas x{world}",

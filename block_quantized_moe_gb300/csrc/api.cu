@@ -239,9 +239,14 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
 // 86 us); the route-slot path stays available as path 1.
 bool use_grouped(const ftmoe_moe_shape* s) { return s->path != 1 && s->path != 4; }
 
-// The fused decode path: one persistent kernel after the quantizing launch (path 4).
+// The fused decode path (path 4): one persistent kernel after the quantizing launch. The
+// automatic choice wherever its limits hold (at most 8 tokens). Measured on GB300 against
+// the grouped path (us per forward, one CUDA graph, L2 flushed): hidden 4096, intermediate
+// 1024, 64 experts, top-8 -- 1 token with 8/2/0 active routes 45.6 / 36.0 / 11.2 against
+// 48.3 / 38.1 / 15.9, 8 tokens with 8/2 active 116.8 / 61.1 against 119.5 / 65.2; hidden
+// 2048, intermediate 768, 8 experts, 1 token with 2 active 32.3 against 31.1.
 bool use_decode(const ftmoe_moe_shape* s) {
-  if (s->format != FTMOE_FMT_FP8 || s->path != 4) return false;
+  if (s->format != FTMOE_FMT_FP8 || (s->path != 0 && s->path != 4)) return false;
   return decode_plan(s->tokens, s->topk, s->num_experts, s->hidden, s->inter).ok;
 }
 

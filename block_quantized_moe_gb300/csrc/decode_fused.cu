@@ -10,18 +10,21 @@
 // the whole FFN after quantization is one launch whose work is spread evenly over the SMs:
 //
 //   * Tables. Every CTA derives the same tables from expert_ids: the distinct active
-//     experts in ascending order (slot s), the routes of each (route order), and the active
-//     routes of each token. An inactive route (negative slot) appears in none of them: no
+//     experts in ascending order (slot s), the tokens of each (one row per (token, expert),
+//     in the slot of the token's first listing of the expert), and the distinct active
+//     experts of each token. An inactive route (negative slot) appears in none of them: no
 //     weight, activation, scale or routing weight of it is ever read.
 //   * Gate/up, split evenly ("stream-K"). The 128-row weight blocks of all active experts
-//     (gate block j and up block j adjacent) are cut into chunks of KBS 128-wide K blocks,
-//     and CTA c takes chunks [c * KU / G, (c + 1) * KU / G) of the KU chunks. A CTA's piece of
-//     a block (a segment) is promoted per K block like the grouped GEMM (act_scale x
-//     weight_scale on CUDA cores) and stored as fp32 partial sums of the 8 token columns.
-//     The last segment to arrive for a (gate block j, up block j) pair -- a counter per pair
-//     -- adds the partial sums in K order, forms silu(g) * u for the expert's routes,
-//     re-quantizes each route's 1x128 group to FP8 with its scale amax / 448, and counts the
-//     pair done for the expert.
+//     (gate block j and up block j adjacent) are cut into a fixed number of chunks of whole
+//     TMA stages (chosen from the shape alone), and CTA c takes chunks [c * KU / G,
+//     (c + 1) * KU / G) of the KU chunks. Each chunk is promoted per K block like the grouped
+//     GEMM (act_scale x weight_scale on CUDA cores), from zero, and stored as fp32 partial
+//     sums of the 8 token columns. The last CTA to arrive for a (gate block j, up block j)
+//     pair -- a counter per pair -- adds the chunks of each block in K order, forms
+//     silu(g) * u for the expert's routes, re-quantizes each route's 1x128 group to FP8 with
+//     its scale amax / 448, and counts the pair done for the expert. Since the chunking and
+//     the order of the sums depend on the shape only, a route's result does not depend on
+//     which other experts the batch activates or on how the chunks fell to the CTAs.
 //   * Down, whole blocks. CTA c takes a contiguous range of the (expert, 128-row block of
 //     H) blocks. The weights stream as soon as the ring has room; the B operand (the
 //     expert's intermediate rows, written by other CTAs) is staged by a loader warp once the
@@ -31,11 +34,13 @@
 //     in ascending slot order (fp32, from zero) and writes the output elements.
 //
 // The results differ from the separate kernels only in the order of the fp32 sums of a
-// gate/up element (segments are added after they are formed); the SiLU, quantization,
-// down GEMM and combine arithmetic is the same expression.
+// gate/up element (chunks are added after they are formed); the SiLU, quantization, down
+// GEMM and combine arithmetic is the same expression.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner), warp 2 B loader for the
-// down blocks, warp 3 idle, warps 4-7 epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
+// down blocks, warp 3 scale-product tables (one item ahead), warps 4-7 promotion (warp w
+// reads TMEM lanes 32 (w % 4) ..), warps 8-11 finishers (counters, pair finishing, combine),
+// fed through a queue of mbarriers so that no wait on another CTA stalls the weight stream.
 // MMA: tcgen05.mma kind::f8f6f4, M = 128 weight rows, N = 16 token (or route) columns,
 // K = 32, four per 128-wide K block into a fresh TMEM accumulator; 16 accumulators rotate.
 // Every wait is bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all
@@ -56,14 +61,18 @@ constexpr int kMaxRoutes = kDecodeMaxRoutes;
 constexpr int kMaxRowsPerExpert = 16;
 constexpr int kAcc = 16;            // TMEM accumulators of kN columns in rotation
 constexpr int kTmemCols = kAcc * kN;
-constexpr int kThreads = 256;
-constexpr int kEpiWarp0 = 4;
+constexpr int kThreads = 384;
+constexpr int kScaleWarp = 3;       // builds each item's scale-product table ahead of use
+constexpr int kEpiWarp0 = 4;        // warps 4-7: promotion (one TMEM lane quarter each)
 constexpr int kEpiThreads = 128;
+constexpr int kFinWarp0 = 8;        // warps 8-11: counters, pair finishing, combine
+constexpr int kFinThreads = 128;
+constexpr int kQueue = 4;           // items the promoters may run ahead of the finishers
 constexpr int kPartCols = kDecodeMaxTokens;  // partial sums keep the token columns
 constexpr int kSubW = kBM * kBK;    // 16 KiB: one K block of one weight block
 constexpr int kSubX = kN * kBK;     // 2 KiB: one K block of 16 token rows
 constexpr int kMaxStages = 8;
-constexpr int kEpiBar = 1;          // named barrier of the epilogue warpgroup
+constexpr int kFinBar = 2;          // named barrier of the finisher warpgroup
 
 __device__ __forceinline__ uint32_t idesc_f8_n16() {
   return (1u << 4)                       // D format f32
@@ -84,6 +93,28 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+// Bounded wait until *ctr >= target, polling with a short sleep between reads; false on
+// timeout (raising FTMOE_ERR_WAIT_TIMEOUT and the abort flag) or when another role aborted.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* abort_flag) {
+  if (ld_acquire_u32(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (ld_acquire_u32(ctr) < target) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      raise_error(FTMOE_ERR_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
+}
+
+// Release/acquire fence at GPU scope: orders this thread's (and, through the barriers it
+// took part in, its CTA's) global writes before a counter update, and the reads after an
+// observed count after it.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 struct Params {
@@ -96,7 +127,7 @@ struct Params {
   uint8_t* act_q;          // [R][I]
   float* act_s;            // [R][NJ]
   float* y;                // [R][H]
-  float* part;             // [G * spc][kPartCols][128]
+  float* part;             // [gate/up chunks][128 rows][kPartCols], chunk = block * kch + chunk in block
   uint32_t* cnt;           // pairs [u_max * NJ], experts [u_max], tokens [T * HB]
   void* out;
   int64_t ld_out;
@@ -104,7 +135,7 @@ struct Params {
   int T, topk, E, H, I;
   int KB, KB2, NJ, NB, HB;
   int kbs_g, kbs_d, stages;
-  int spc, u_max;
+  int kch, ckb, u_max;     // chunks per gate/up block, K blocks per chunk, most distinct experts
 };
 
 // Shared-memory tables every role reads (built by all threads at the start).
@@ -112,10 +143,11 @@ struct Tables {
   int ids[kMaxRoutes];          // valid expert id of each route, or -1
   uint32_t bm[32];              // bitmap of active experts (E <= 1024)
   int pre[32];                  // distinct experts in lower bitmap words
+  int canon[kMaxRoutes];        // first route of the same (token, expert): the row it shares
   int ex[kMaxRoutes];           // expert of slot s
-  int m[kMaxRoutes];            // routes of slot s (capped at kMaxRowsPerExpert)
-  int rt[kMaxRoutes][kMaxRowsPerExpert];  // route indices of slot s, ascending
-  int nact[kDecodeMaxTokens];   // active routes per token
+  int m[kMaxRoutes];            // tokens of slot s (at most T)
+  int rt[kMaxRoutes][kMaxRowsPerExpert];  // canonical route of each token of slot s, ascending
+  int nact[kDecodeMaxTokens];   // distinct active experts per token
   int U;                        // distinct active experts
 };
 
@@ -142,9 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   uint8_t* bbuf = ring + (size_t)S * stage_bytes;              // two B buffers of [KB2][16 rows][128 B]
   const int bbuf_bytes = p.KB2 * kSubX;
-  float* prod = reinterpret_cast<float*>(bbuf + 2 * bbuf_bytes);  // [max(KB, KB2)][kN]
   const int prod_kb = p.KB > p.KB2 ? p.KB : p.KB2;
-  float* red = prod + prod_kb * kN;                             // [4 warps][kMaxRowsPerExpert]
+  float* prod = reinterpret_cast<float*>(bbuf + 2 * bbuf_bytes);  // [2][max(KB, KB2)][kN]
+  float* red = prod + 2 * prod_kb * kN;                         // [4 finisher warps][kMaxRowsPerExpert]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * kMaxRowsPerExpert);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -152,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tempty = tfull + kAcc;
   uint64_t* bfull = tempty + kAcc;
   uint64_t* bempty = bfull + 2;
+  uint64_t* pfull = bempty + 2;    // scale-product table i & 1 ready (32 arrivals: the scale warp)
+  uint64_t* pempty = pfull + 2;    // ... read by the promoters (4 arrivals)
+  uint64_t* qdone = pempty + 2;    // item promoted, its rows written (4 arrivals: promoter warps)
+  uint64_t* qfree = qdone + kQueue;  // item finished (4 arrivals: finisher warps)
   __shared__ Tables tb;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -176,6 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bfull[i]), 1);
       mbar_init(smem_u32(&bempty[i]), 1);
+      mbar_init(smem_u32(&pfull[i]), 32);
+      mbar_init(smem_u32(&pempty[i]), kEpiThreads / 32);
+    }
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(smem_u32(&qdone[i]), kEpiThreads / 32);
+      mbar_init(smem_u32(&qfree[i]), kFinThreads / 32);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -200,23 +242,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 31) tb.U = inc;
   }
   __syncthreads();
-  if (tid < R && tb.ids[tid] >= 0) {
+  // A token that lists one expert more than once has one intermediate row and one down row
+  // for that expert, in the slot of its first listing (the canonical route); every listing
+  // reads that row in the combine, with its own routing weight.
+  if (tid < R) {
+    const int id = tb.ids[tid];
+    int c = tid;
+    if (id >= 0)
+      for (int j = (tid / p.topk) * p.topk; j < tid; ++j)
+        if (tb.ids[j] == id) {
+          c = j;
+          break;
+        }
+    tb.canon[tid] = c;
+  }
+  __syncthreads();
+  if (tid < R && tb.ids[tid] >= 0 && tb.canon[tid] == tid) {
     const int id = tb.ids[tid];
     const int s = tb.pre[id >> 5] + __popc(tb.bm[id >> 5] & ((1u << (id & 31)) - 1u));
     int pos = 0, count = 0;
     for (int j = 0; j < R; ++j) {
-      const bool same = tb.ids[j] == id;
+      const bool same = tb.ids[j] == id && tb.canon[j] == j;
       pos += (same && j < tid) ? 1 : 0;
       count += same ? 1 : 0;
     }
-    if (pos < kMaxRowsPerExpert) {
-      tb.rt[s][pos] = tid;
-    } else if (blockIdx.x == 0) {
-      raise_error(FTMOE_ERR_EXPERT_ID_RANGE);  // more than 16 routes to one expert: skipped
-    }
+    tb.rt[s][pos] = tid;  // pos < count <= T <= kMaxRowsPerExpert
     if (pos == 0) {
       tb.ex[s] = id;
-      tb.m[s] = count < kMaxRowsPerExpert ? count : kMaxRowsPerExpert;
+      tb.m[s] = count;
     }
   }
   if (warp == 1) {
@@ -227,19 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  // tables with more than 16 routes for one expert keep the first 16 (the rest were reported)
-  for (int i = tid; i < R; i += kThreads) {
-    const int id = tb.ids[i];
-    if (id < 0) continue;
-    const int s = tb.pre[id >> 5] + __popc(tb.bm[id >> 5] & ((1u << (id & 31)) - 1u));
-    bool kept = false;
-    for (int q = 0; q < tb.m[s]; ++q) kept |= tb.rt[s][q] == i;
-    if (!kept) tb.ids[i] = -1;
-  }
-  __syncthreads();
-  if (tid < p.T) {  // active routes per token: the arrivals its combine waits for
+  if (tid < p.T) {  // distinct active experts per token: the arrivals its combine waits for
     int n = 0;
-    for (int j = 0; j < p.topk; ++j) n += tb.ids[tid * p.topk + j] >= 0 ? 1 : 0;
+    for (int j = 0; j < p.topk; ++j) {
+      const int r = tid * p.topk + j;
+      n += (tb.ids[r] >= 0 && tb.canon[r] == r) ? 1 : 0;
+    }
     tb.nact[tid] = n;
   }
   __syncthreads();
@@ -247,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int U = tb.U;
   const int G = gridDim.x;
   Sched sc;
-  sc.KCH = p.KB / p.kbs_g;
+  sc.KCH = p.kch;
   sc.KU = (int64_t)U * p.NB * sc.KCH;
   sc.Gg = sc.KU < G ? (int)sc.KU : G;
   if ((int)blockIdx.x < sc.Gg) {
@@ -312,14 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it;
         return true;
       };
+      // one walk over the CTA's stages (gate/up chunks, then down blocks), one call site: the
+      // down phase runs the code the gate/up phase already brought into the instruction cache
       bool ok = true;
-      for (int64_t u = sc.u_lo; u < sc.u_hi && ok && !s_abort; ++u) {
-        const int b = (int)(u / sc.KCH), ch = (int)(u % sc.KCH);
-        ok = issue(true, tb.ex[slot_of_block(b)], wrow_block(b), ch * p.kbs_g);
-      }
-      for (int d = sc.d_lo; d < sc.d_hi && ok && !s_abort; ++d) {
-        const int s = d / HB, hb = d % HB;
-        for (int ch = 0; ch < p.KB2 / p.kbs_d && ok; ++ch) ok = issue(false, tb.ex[s], hb, ch * p.kbs_d);
+      int64_t u = sc.u_lo;
+      int d = sc.d_lo, sub = 0;
+      while (ok && !s_abort) {
+        if (u < sc.u_hi) {
+          const int b = (int)(u / sc.KCH), ch = (int)(u % sc.KCH);
+          ok = issue(true, tb.ex[slot_of_block(b)], wrow_block(b), ch * p.ckb + sub * p.kbs_g);
+          if (++sub == p.ckb / p.kbs_g) sub = 0, ++u;
+        } else if (d < sc.d_hi) {
+          ok = issue(false, tb.ex[d / HB], d % HB, sub * p.kbs_d);
+          if (++sub == p.KB2 / p.kbs_d) sub = 0, ++d;
+        } else {
+          break;
+        }
       }
       if (!waited) {
         pdl_wait();
@@ -342,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_f8_n16();
       uint32_t it = 0, kc = 0;
       bool ok = true;
-      // one stage of nkb K blocks against B sub-tiles at b_addr(h)
-      auto consume = [&](int nkb, auto b_addr) -> bool {
+      // one stage of nkb K blocks against the B sub-tiles at b0, b0 + kSubX, ...
+      auto consume = [&](int nkb, uint32_t b0) -> bool {
         const int st = it % S;
         if (!mbar_wait(smem_u32(&full[st]), (it / S) & 1, &s_abort)) return false;
         const uint32_t sw = smem_u32(ring + (size_t)st * stage_bytes);
@@ -352,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(smem_u32(&tempty[acc]), ((kc / kAcc) & 1) ^ 1, &s_abort)) return false;
           fence_after();
           const uint32_t d = tmem_base + acc * kN;
-          const uint32_t wa = sw + h * kSubW, xb = b_addr(h);
+          const uint32_t wa = sw + h * kSubW, xb = b0 + h * kSubX;
 #pragma unroll
           for (int j = 0; j < kBK / 32; ++j)
             mma_f8(d, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(xb + 32 * j), idesc, j > 0 ? 1u : 0u);
@@ -362,26 +416,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it;
         return true;
       };
-      for (int64_t u = sc.u_lo; u < sc.u_hi && ok && !s_abort; ++u) {
-        const uint32_t xs = smem_u32(ring + (size_t)(it % S) * stage_bytes + p.kbs_g * kSubW);
-        ok = consume(p.kbs_g, [&](int h) { return xs + h * kSubX; });
-      }
-      int g = -1, prev_s = -1;
-      for (int d = sc.d_lo; d < sc.d_hi && ok && !s_abort; ++d) {
-        const int s = d / HB;
-        if (s != prev_s) {  // a new expert: its B rows are staged in buffer (g + 1) & 1
-          ++g;
-          prev_s = s;
-          if (!mbar_wait(smem_u32(&bfull[g & 1]), (g >> 1) & 1, &s_abort)) break;
-          fence_after();
+      // the same walk as the producer's: gate/up stages (B = the stage's token tile), then
+      // down stages (B = the expert's staged intermediate rows)
+      int64_t u = sc.u_lo;
+      int d = sc.d_lo, sub = 0, g = -1, prev_s = -1;
+      while (ok && !s_abort) {
+        uint32_t b0;
+        int nkb;
+        bool release_b = false;
+        if (u < sc.u_hi) {
+          b0 = smem_u32(ring + (size_t)(it % S) * stage_bytes + p.kbs_g * kSubW);
+          nkb = p.kbs_g;
+          if (++sub == p.ckb / p.kbs_g) sub = 0, ++u;
+        } else if (d < sc.d_hi) {
+          const int s = d / HB;
+          if (s != prev_s) {  // a new expert: its B rows are staged in buffer (g + 1) & 1
+            ++g;
+            prev_s = s;
+            if (!mbar_wait(smem_u32(&bfull[g & 1]), (g >> 1) & 1, &s_abort)) break;
+            fence_after();
+          }
+          b0 = smem_u32(bbuf + (size_t)(g & 1) * bbuf_bytes) + (uint32_t)(sub * p.kbs_d * kSubX);
+          nkb = p.kbs_d;
+          if (++sub == p.KB2 / p.kbs_d) {
+            sub = 0;
+            ++d;
+            release_b = d >= sc.d_hi || d / HB != s;  // the expert's last block: B may be refilled
+          }
+        } else {
+          break;
         }
-        const uint32_t bb = smem_u32(bbuf + (size_t)(g & 1) * bbuf_bytes);
-        for (int ch = 0; ch < p.KB2 / p.kbs_d && ok; ++ch) {
-          const int kb0 = ch * p.kbs_d;
-          ok = consume(p.kbs_d, [&](int h) { return bb + (uint32_t)((kb0 + h) * kSubX); });
-        }
-        const bool last_of_expert = d + 1 >= sc.d_hi || (d + 1) / HB != s;
-        if (last_of_expert) mma_commit(smem_u32(&bempty[g & 1]));
+        ok = consume(nkb, b0);
+        if (ok && release_b) mma_commit(smem_u32(&bempty[g & 1]));
       }
       // MMAs still running write TMEM and read B: wait (bounded) for each accumulator's last
       // commit before the CTA may free TMEM
@@ -394,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------ B loader (down blocks) -------------------------------
-    // The expert's intermediate rows (one per route, written by the pair finalizers of any
+    // The expert's intermediate rows (one per token, written by the pair finalizers of any
     // CTA) become the MMA's B operand: 16 rows of I bytes in the 128-byte-swizzled K-major
-    // layout, one 2 KiB sub-tile per K block, rows beyond the expert's routes zero.
+    // layout, one 2 KiB sub-tile per K block, rows beyond the expert's tokens zero.
     int g = -1, prev_s = -1;
     pdl_wait();
     for (int d = sc.d_lo; d < sc.d_hi && !s_abort; ++d) {
@@ -404,21 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s == prev_s) continue;
       ++g;
       prev_s = s;
-      if (g >= 2 && !mbar_wait(smem_u32(&bempty[g & 1]), ((g >> 1) - 1) & 1, &s_abort)) break;
+      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[g & 1]), ((g >> 1) - 1) & 1, &s_abort)))
+        break;
       // all of the expert's (gate, up) pairs are re-quantized (bounded wait)
-      bool ready = true;
-      if (lane == 0) {
-        const unsigned long long t0 = globaltimer();
-        while (ld_acquire_u32(cnt_exp + s) < (uint32_t)NJ) {
-          if (s_abort) { ready = false; break; }
-          if (globaltimer() - t0 > kTimeoutNs) {
-            raise_error(FTMOE_ERR_WAIT_TIMEOUT);
-            s_abort = 1;
-            ready = false;
-            break;
-          }
-        }
-      }
+      bool ready = lane == 0 ? wait_count(cnt_exp + s, (uint32_t)NJ, &s_abort) : true;
       ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
       if (!ready) break;
       (void)ld_acquire_u32(cnt_exp + s);  // every lane acquires before it reads the rows
@@ -436,15 +491,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bfull[g & 1]));
     }
-  } else if (warp >= kEpiWarp0) {
-    // --------------------------------- epilogue ---------------------------------
+  } else if (warp == kScaleWarp) {
+    // -------------------- scale products, one item ahead ---------------------------
+    // Item it's table goes to buffer it & 1: gate/up segments x_s[token][kb] * w_s[block][kb],
+    // down blocks act_s[row q][kb] * w_s[e][hb][kb] (once the expert's intermediate rows
+    // are complete). The promoters read it while the next one is being formed.
+    pdl_wait();  // x_s comes from the quantizing launch
+    int item = 0;
+    auto begin = [&](int it) -> bool {
+      bool ok = true;
+      if (it >= 2) ok = mbar_wait(smem_u32(&pempty[it & 1]), ((it >> 1) - 1) & 1, &s_abort);
+      return __all_sync(0xffffffffu, ok) != 0;
+    };
+    for (int64_t u = sc.u_lo; u < sc.u_hi; ++item) {
+      const int b = (int)(u / sc.KCH), c0 = (int)(u % sc.KCH);
+      const int64_t seg_end = ((int64_t)b + 1) * sc.KCH < sc.u_hi ? ((int64_t)b + 1) * sc.KCH : sc.u_hi;
+      const int c1 = (int)(seg_end - (int64_t)b * sc.KCH);
+      u = seg_end;
+      if (!begin(item)) break;
+      float* pr = prod + (item & 1) * prod_kb * kN;
+      const int e = tb.ex[slot_of_block(b)], wrb = wrow_block(b);
+      const int kb0 = c0 * p.ckb, nkb = (c1 - c0) * p.ckb;
+      for (int i = lane; i < nkb * kN; i += 32) {
+        const int kbl = i / kN, c = i - kbl * kN;
+        const int kb = kb0 + kbl;
+        pr[i] = __ldg(p.x_s + (int64_t)c * p.KB + kb) * __ldg(p.wg_s + ((int64_t)e * p.NB + wrb) * p.KB + kb);
+      }
+      mbar_arrive(smem_u32(&pfull[item & 1]));
+    }
+    for (int d = sc.d_lo; d < sc.d_hi && !s_abort; ++d, ++item) {
+      if (!begin(item)) break;
+      const int s = d / HB, hb = d % HB, e = tb.ex[s], m = tb.m[s];
+      bool ready = lane == 0 ? wait_count(cnt_exp + s, (uint32_t)NJ, &s_abort) : true;
+      if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0) == 0) break;
+      (void)ld_acquire_u32(cnt_exp + s);  // every lane acquires before it reads the scales
+      float* pr = prod + (item & 1) * prod_kb * kN;
+      for (int i = lane; i < p.KB2 * kN; i += 32) {
+        const int kb = i / kN, q = i - kb * kN;
+        pr[i] = q < m ? __ldcg(p.act_s + (int64_t)tb.rt[s][q] * NJ + kb) *
+                            __ldg(p.wd_s + ((int64_t)e * HB + hb) * p.KB2 + kb)
+                      : 0.0f;
+      }
+      mbar_arrive(smem_u32(&pfull[item & 1]));
+    }
+  } else if (warp < kFinWarp0) {
+    // ------------------------------- promotion --------------------------------------
+    // Warp w reads TMEM lanes 32 (w % 4) .. (one weight row per thread) of each K block's
+    // accumulator and adds d * (act_scale x weight_scale) per column; gate/up chunks are
+    // stored as partial sums, down blocks as rows of y. Nothing here waits on other CTAs.
     const int et = tid - kEpiWarp0 * 32;  // 0..127 = TMEM lane = weight row in the block
     const int quarter = warp & 3;
-    const int ew = warp - kEpiWarp0;
     uint32_t kc = 0;
     pdl_wait();
-    // promote K blocks [kb0, kb1) of one item: acc[c] += d[c] * prod[kb - kb0][c]
-    auto promote = [&](int nkb, float* acc) -> bool {
+    // promote nkb K blocks: acc[c] += d[c] * pr[i][c]
+    auto promote = [&](int nkb, float* acc, const float* pr) -> bool {
       bool ok = true;
       for (int i = 0; i < nkb; ++i, ++kc) {
         const uint32_t ab = kc % kAcc;
@@ -460,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
-        const float4* p4 = reinterpret_cast<const float4*>(prod + i * kN);
+        const float4* p4 = reinterpret_cast<const float4*>(pr + i * kN);
 #pragma unroll
         for (int c4 = 0; c4 < kN / 4; ++c4) {
           const float4 s4 = p4[c4];
@@ -472,154 +572,209 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return ok;
     };
-
-    // -- gate/up segments --
-    int seg = 0;
-    for (int64_t u = sc.u_lo; u < sc.u_hi; ++seg) {
-      const int b = (int)(u / sc.KCH);
-      const int c0 = (int)(u % sc.KCH);
-      const int64_t seg_end = ((int64_t)b + 1) * sc.KCH < sc.u_hi ? ((int64_t)b + 1) * sc.KCH : sc.u_hi;
-      const int c1 = (int)(seg_end - (int64_t)b * sc.KCH);
-      u = seg_end;
-      if (named_bar_or(kEpiBar, kEpiThreads, s_abort)) break;
-      const int s = slot_of_block(b), e = tb.ex[s], wrb = wrow_block(b);
-      const int kb0 = c0 * p.kbs_g, nkb = (c1 - c0) * p.kbs_g;
-      // scale products of the segment's K blocks: x_s[token][kb] * w_s[block][kb]
-      for (int i = et; i < nkb * kN; i += kEpiThreads) {
-        const int kbl = i / kN, c = i - kbl * kN;
-        const int kb = kb0 + kbl;
-        prod[i] = __ldg(p.x_s + (int64_t)c * p.KB + kb) * __ldg(p.wg_s + ((int64_t)e * p.NB + wrb) * p.KB + kb);
+    // an item's scale table is ready, and its queue slot is free of the item kQueue back
+    auto begin = [&](int it) -> bool {
+      bool ok = true;
+      if (it >= kQueue) ok = mbar_wait(smem_u32(&qfree[it % kQueue]), ((it / kQueue) - 1) & 1, &s_abort);
+      ok = ok && mbar_wait(smem_u32(&pfull[it & 1]), (it >> 1) & 1, &s_abort);
+      return __all_sync(0xffffffffu, ok) != 0;
+    };
+    // the table is read and the item's rows are written: hand it to the finishers
+    auto finish = [&](int it) {
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&pempty[it & 1]));
+        mbar_arrive(smem_u32(&qdone[it % kQueue]));
       }
-      named_bar(kEpiBar, kEpiThreads);
-      float acc[kN];
+    };
+    // one walk over the CTA's items (gate/up segments, then down blocks) with one promotion
+    // call site, so the down phase runs code the gate/up phase already brought into the
+    // instruction cache
+    int item = 0;
+    bool ok = true;
+    int64_t u = sc.u_lo;
+    int d = sc.d_lo;
+    while (ok) {
+      bool gu;
+      int b = 0, c0 = 0, c1 = 1, s = 0, hb = 0;
+      if (u < sc.u_hi) {
+        gu = true;
+        b = (int)(u / sc.KCH);
+        c0 = (int)(u % sc.KCH);
+        const int64_t seg_end = ((int64_t)b + 1) * sc.KCH < sc.u_hi ? ((int64_t)b + 1) * sc.KCH : sc.u_hi;
+        c1 = (int)(seg_end - (int64_t)b * sc.KCH);
+        u = seg_end;
+      } else if (d < sc.d_hi) {
+        gu = false;
+        s = d / HB;
+        hb = d % HB;
+        ++d;
+      } else {
+        break;
+      }
+      if (!begin(item)) break;
+      const float* pr = prod + (item & 1) * prod_kb * kN;
+      const int nkb = gu ? p.ckb : p.KB2;
+      // gate/up: one partial sum per chunk, each from zero (the finishers add a block's chunks
+      // in K order, so the result does not depend on how the chunks were spread over the
+      // CTAs); down: the expert's rows of y
+      for (int ch = c0; ch < c1; ++ch) {
+        float acc[kN];
 #pragma unroll
-      for (int c = 0; c < kN; ++c) acc[c] = 0.0f;
-      const bool ok = promote(nkb, acc);
-      const bool all_ok = !named_bar_or(kEpiBar, kEpiThreads, ok ? 0 : 1);
-      if (!all_ok) break;
-      // partial sums of the token columns, slot (CTA, segment index)
-      float* pp = p.part + ((size_t)blockIdx.x * p.spc + seg) * (kPartCols * kBM);
+        for (int c = 0; c < kN; ++c) acc[c] = 0.0f;
+        ok = promote(nkb, acc, pr + (ch - c0) * nkb * kN) && ok;
+        if (gu) {
+          // [chunk][row][8 token columns]: a row's columns are one 32-byte piece
+          float4* pp = reinterpret_cast<float4*>(p.part + (((size_t)b * sc.KCH + ch) * kBM + et) * kPartCols);
+          __stcg(pp, make_float4(acc[0], acc[1], acc[2], acc[3]));
+          __stcg(pp + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        } else {
+          const int m = tb.m[s], h = hb * kBM + et;
 #pragma unroll
-      for (int c = 0; c < kPartCols; ++c) __stcg(pp + c * kBM + et, acc[c]);
-      __threadfence();
-      named_bar(kEpiBar, kEpiThreads);
-      // the pair's arrivals: every segment of its gate block and of its up block
-      const int bg = b & ~1;
-      if (et == 0) {
+          for (int q = 0; q < kMaxRowsPerExpert; ++q)
+            if (q < m) __stcg(p.y + (int64_t)tb.rt[s][q] * p.H + h, acc[q]);
+        }
+      }
+      finish(item);
+      ++item;
+    }
+  } else {
+    // --------------------------------- finishers ------------------------------------
+    // Per item, after the promoters wrote its rows: a gate/up segment counts its arrival at
+    // the (gate block j, up block j) pair; the last arrival adds each block's chunks in K
+    // order, forms silu(g) * u for the expert's tokens, re-quantizes each token's 1x128 group
+    // (scale amax / 448) and counts the pair done for the expert. A down block counts its
+    // tokens per (token, block of H); the last arrival for a token reduces that token's
+    // active routes in ascending slot order (fp32, from zero) into the output. Thread ft is
+    // weight row ft of the block.
+    const int ft = tid - kFinWarp0 * 32;
+    const int fw = warp - kFinWarp0;
+    pdl_wait();  // the counters are zeroed by the quantizing launch
+    auto begin = [&](int it) -> bool {
+      const bool ok = mbar_wait(smem_u32(&qdone[it % kQueue]), (it / kQueue) & 1, &s_abort);
+      return !named_bar_or(kFinBar, kFinThreads, ok ? 0 : 1);
+    };
+    auto done = [&](int it) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&qfree[it % kQueue]));
+    };
+    int item = 0;
+    for (int64_t u = sc.u_lo; u < sc.u_hi; ++item) {
+      const int b = (int)(u / sc.KCH);
+      const int64_t seg_end = ((int64_t)b + 1) * sc.KCH < sc.u_hi ? ((int64_t)b + 1) * sc.KCH : sc.u_hi;
+      u = seg_end;
+      if (!begin(item)) break;
+      const int s = slot_of_block(b), j = (b >> 1) % NJ, bg = b & ~1;
+      if (ft == 0) {
+        // the pair's arrivals: every segment of its gate block and of its up block
         int expected = 0;
         for (int h = 0; h < 2; ++h) {
           const int64_t a0 = ((int64_t)bg + h) * sc.KCH;
           expected += cta_of(a0 + sc.KCH - 1, sc.KU, sc.Gg) - cta_of(a0, sc.KU, sc.Gg) + 1;
         }
-        const uint32_t old = atomicAdd(cnt_pair + (size_t)s * NJ + ((b >> 1) % NJ), 1u);
+        fence_acq_rel_gpu();  // this CTA's partial sums (seen through the queue) before the count
+        const uint32_t old = atomicAdd(cnt_pair + (size_t)s * NJ + j, 1u);
         s_last = (int)(old + 1 == (uint32_t)expected);
-        __threadfence();
+        fence_acq_rel_gpu();
       }
-      named_bar(kEpiBar, kEpiThreads);
-      if (!s_last) continue;
-      // ---- last arrival: finish the pair ----
-      float gsum[kPartCols], usum[kPartCols];
-      for (int h = 0; h < 2; ++h) {
-        float* sum = h == 0 ? gsum : usum;
+      named_bar(kFinBar, kFinThreads);
+      if (s_last) {
+        // the gate and up blocks' chunk sums of this row, added in K order: per group of four
+        // token columns the call has, every chunk's loads are in flight before the sum
+        float gsum[kPartCols], usum[kPartCols];
+        const float4* g4 = reinterpret_cast<const float4*>(p.part + ((size_t)bg * sc.KCH * kBM + ft) * kPartCols);
+        const float4* u4 = g4 + (size_t)sc.KCH * kBM * 2;
 #pragma unroll
-        for (int c = 0; c < kPartCols; ++c) sum[c] = 0.0f;
-        const int64_t a0 = ((int64_t)bg + h) * sc.KCH;
-        const int cf = cta_of(a0, sc.KU, sc.Gg), cl = cta_of(a0 + sc.KCH - 1, sc.KU, sc.Gg);
-        for (int c2 = cf; c2 <= cl; ++c2) {  // K order
-          const int i2 = bg + h - (int)(chunk_lo(c2, sc.KU, sc.Gg) / sc.KCH);
-          const float* q2 = p.part + ((size_t)c2 * p.spc + i2) * (kPartCols * kBM);
+        for (int cg = 0; cg < kPartCols / 4; ++cg) {
+          float4 gv[kDecodeMaxKch], uv[kDecodeMaxKch];
+          const bool need = cg * 4 < p.T;
 #pragma unroll
-          for (int c = 0; c < kPartCols; ++c) sum[c] += __ldcg(q2 + c * kBM + et);
-        }
-      }
-      // silu(g) * u of each route of the expert (column = its token), one 1x128 group
-      const int m = tb.m[s], j = (b >> 1) % NJ;
-      float a[kMaxRowsPerExpert];
-#pragma unroll
-      for (int q = 0; q < kMaxRowsPerExpert; ++q) {
-        a[q] = 0.0f;
-        if (q < m) {
-          const int t = tb.rt[s][q] / p.topk;
-          a[q] = silu_mul_1(gsum[t], usum[t]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kMaxRowsPerExpert; ++q) {
-        const float w = warp_max(fabsf(a[q]));
-        if (lane == 0) red[ew * kMaxRowsPerExpert + q] = w;
-      }
-      named_bar(kEpiBar, kEpiThreads);
-#pragma unroll
-      for (int q = 0; q < kMaxRowsPerExpert; ++q) {
-        if (q >= m) break;
-        const float amax = fmaxf(fmaxf(red[q], red[kMaxRowsPerExpert + q]),
-                                 fmaxf(red[2 * kMaxRowsPerExpert + q], red[3 * kMaxRowsPerExpert + q]));
-        const float scl = div_rn(amax, kE4M3Max);
-        const uint8_t code = amax > 0.0f ? (uint8_t)(f2_to_e4m3x2(div_rn(a[q], scl), 0.0f) & 0xFF) : (uint8_t)0;
-        const int r = tb.rt[s][q];
-        p.act_q[(int64_t)r * p.I + j * kBK + et] = code;
-        if (et == 0) p.act_s[(int64_t)r * NJ + j] = scl;
-      }
-      __threadfence();
-      named_bar(kEpiBar, kEpiThreads);
-      if (et == 0) atomicAdd(cnt_exp + s, 1u);
-    }
-
-    // -- down blocks --
-    for (int d = sc.d_lo; d < sc.d_hi; ++d) {
-      if (named_bar_or(kEpiBar, kEpiThreads, s_abort)) break;
-      const int s = d / HB, hb = d % HB, e = tb.ex[s], m = tb.m[s];
-      if (et == 0) {  // the expert's intermediate rows are complete (bounded wait)
-        const unsigned long long t0 = globaltimer();
-        while (ld_acquire_u32(cnt_exp + s) < (uint32_t)NJ) {
-          if (s_abort) break;
-          if (globaltimer() - t0 > kTimeoutNs) {
-            raise_error(FTMOE_ERR_WAIT_TIMEOUT);
-            s_abort = 1;
-            break;
+          for (int ch = 0; ch < kDecodeMaxKch; ++ch) {
+            if (need && ch < sc.KCH) {
+              gv[ch] = __ldcg(g4 + (size_t)ch * kBM * 2 + cg);
+              uv[ch] = __ldcg(u4 + (size_t)ch * kBM * 2 + cg);
+            } else {
+              gv[ch] = uv[ch] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
           }
+          float4 ga = gv[0], ua = uv[0];
+#pragma unroll
+          for (int ch = 1; ch < kDecodeMaxKch; ++ch) {
+            if (ch < sc.KCH) {
+              ga.x += gv[ch].x, ga.y += gv[ch].y, ga.z += gv[ch].z, ga.w += gv[ch].w;
+              ua.x += uv[ch].x, ua.y += uv[ch].y, ua.z += uv[ch].z, ua.w += uv[ch].w;
+            }
+          }
+          gsum[4 * cg + 0] = ga.x, gsum[4 * cg + 1] = ga.y, gsum[4 * cg + 2] = ga.z, gsum[4 * cg + 3] = ga.w;
+          usum[4 * cg + 0] = ua.x, usum[4 * cg + 1] = ua.y, usum[4 * cg + 2] = ua.z, usum[4 * cg + 3] = ua.w;
         }
-        __threadfence();
-      }
-      if (named_bar_or(kEpiBar, kEpiThreads, s_abort)) break;
-      // scale products: act_s[route q][kb] * w_s[e][hb][kb]
-      for (int i = et; i < p.KB2 * kN; i += kEpiThreads) {
-        const int kb = i / kN, q = i - kb * kN;
-        prod[i] = q < m ? __ldcg(p.act_s + (int64_t)tb.rt[s][q] * NJ + kb) *
-                              __ldg(p.wd_s + ((int64_t)e * HB + hb) * p.KB2 + kb)
-                        : 0.0f;
-      }
-      named_bar(kEpiBar, kEpiThreads);
-      float acc[kN];
-#pragma unroll
-      for (int c = 0; c < kN; ++c) acc[c] = 0.0f;
-      const bool ok = promote(p.KB2, acc);
-      const bool all_ok = !named_bar_or(kEpiBar, kEpiThreads, ok ? 0 : 1);
-      if (!all_ok) break;
-      const int h = hb * kBM + et;
-#pragma unroll
-      for (int q = 0; q < kMaxRowsPerExpert; ++q)
-        if (q < m) __stcg(p.y + (int64_t)tb.rt[s][q] * p.H + h, acc[q]);
-      __threadfence();
-      named_bar(kEpiBar, kEpiThreads);
-      if (et == 0) {
-        for (int q = 0; q < m; ++q) {
+        const int m = tb.m[s];
+        // silu(g) * u of the token of the expert's q-th row (its column of the sums); compact
+        // loops over the expert's tokens, the value recomputed where it is quantized (the same
+        // expression on the same inputs: the same bits)
+        auto a_of = [&](int q) {
           const int t = tb.rt[s][q] / p.topk;
-          const uint32_t old = atomicAdd(cnt_tok + (size_t)t * HB + hb, 1u);
-          s_mark[q] = (int)(old + 1 == (uint32_t)tb.nact[t]);
+          float gt = 0.0f, ut = 0.0f;
+#pragma unroll
+          for (int c = 0; c < kPartCols; ++c)  // a select, not a dynamic index into registers
+            if (c == t) gt = gsum[c], ut = usum[c];
+          return silu_mul_1(gt, ut);
+        };
+#pragma unroll 1
+        for (int q = 0; q < m; ++q) {
+          const float w = warp_max(fabsf(a_of(q)));
+          if (lane == 0) red[fw * kMaxRowsPerExpert + q] = w;
         }
-        __threadfence();
+        named_bar(kFinBar, kFinThreads);
+#pragma unroll 1
+        for (int q = 0; q < m; ++q) {
+          const float amax = fmaxf(fmaxf(red[q], red[kMaxRowsPerExpert + q]),
+                                   fmaxf(red[2 * kMaxRowsPerExpert + q], red[3 * kMaxRowsPerExpert + q]));
+          const float scl = div_rn(amax, kE4M3Max);
+          const uint8_t code = amax > 0.0f ? (uint8_t)(f2_to_e4m3x2(div_rn(a_of(q), scl), 0.0f) & 0xFF) : (uint8_t)0;
+          const int r = tb.rt[s][q];
+          p.act_q[(int64_t)r * p.I + j * kBK + ft] = code;
+          if (ft == 0) p.act_s[(int64_t)r * NJ + j] = scl;
+        }
+        named_bar(kFinBar, kFinThreads);  // every row written (and red read) before the count
+        if (ft == 0) {
+          fence_acq_rel_gpu();
+          atomicAdd(cnt_exp + s, 1u);
+        }
       }
-      named_bar(kEpiBar, kEpiThreads);
-      // the last arrival for a token reduces its active routes in ascending slot order
+      done(item);
+    }
+    for (int d = sc.d_lo; d < sc.d_hi; ++d, ++item) {
+      if (!begin(item)) break;
+      const int s = d / HB, hb = d % HB, m = tb.m[s];
+      if (ft < m) {  // one thread per token of the expert, the counts in parallel
+        const int t = tb.rt[s][ft] / p.topk;
+        fence_acq_rel_gpu();  // this CTA's rows of y (seen through the queue) before the count
+        const uint32_t old = atomicAdd(cnt_tok + (size_t)t * HB + hb, 1u);
+        s_mark[ft] = (int)(old + 1 == (uint32_t)tb.nact[t]);
+        fence_acq_rel_gpu();
+      }
+      named_bar(kFinBar, kFinThreads);
+      const int h = hb * kBM + ft;
       for (int q = 0; q < m; ++q) {
         if (!s_mark[q]) continue;
         const int t = tb.rt[s][q] / p.topk;
         float v = 0.0f;
-        for (int jj = 0; jj < p.topk; ++jj) {
-          const int r = t * p.topk + jj;
-          if (tb.ids[r] < 0) continue;  // inactive: neither its weight nor its row is read
-          v = fmaf(__ldg(p.rw + r), __ldcg(p.y + (int64_t)r * p.H + h), v);
+        // the token's routes eight at a time: loads first, then the sum in slot order
+        for (int j0 = 0; j0 < p.topk; j0 += 8) {
+          float wv[8], yv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = t * p.topk + j0 + u;
+            const bool act = j0 + u < p.topk && tb.ids[r] >= 0;  // inactive: nothing of it is read
+            wv[u] = act ? __ldg(p.rw + r) : 0.0f;
+            yv[u] = act ? __ldcg(p.y + (int64_t)tb.canon[r] * p.H + h) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = t * p.topk + j0 + u;
+            if (j0 + u < p.topk && tb.ids[r] >= 0) v = fmaf(wv[u], yv[u], v);
+          }
         }
         if (p.out_dtype == FTMOE_OUT_FP32) {
           reinterpret_cast<float*>(p.out)[(int64_t)t * p.ld_out + h] = v;
@@ -630,10 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               __bfloat16_as_ushort(__float2bfloat16_rn(v));
         }
       }
-      named_bar(kEpiBar, kEpiThreads);  // s_mark is rewritten by the next block
+      named_bar(kFinBar, kFinThreads);  // s_mark is rewritten by the next block
+      done(item);
     }
-  } else {
-    pdl_wait();
   }
 
   fence_before();
@@ -705,13 +859,18 @@ DecodePlan decode_plan(int64_t T, int32_t topk, int32_t E, int64_t H, int64_t I)
   // divide their K-block counts, so the smaller still divides KB2)
   pl.kbs_d = kbs_for_blocks(pl.KB2) < pl.kbs_g ? kbs_for_blocks(pl.KB2) : pl.kbs_g;
   pl.u_max = (int)(T * topk < E ? T * topk : E);
-  // segments per CTA: a range of at most ceil(KU / G) chunks crosses at most that many
-  // chunks / KCH block boundaries, plus one
-  const int64_t kch = pl.KB / pl.kbs_g;
-  const int64_t ku_max = (int64_t)pl.u_max * pl.NB * kch;
-  const int64_t per = (ku_max + kDecodeGrid - 1) / kDecodeGrid;
-  pl.spc = (int)((per + kch - 1) / kch + 1);
-  pl.part_bytes = (size_t)kDecodeGrid * pl.spc * dk::kPartCols * dk::kBM * 4;
+  // Chunks per gate/up block: as many as the partial-sum budget allows (finer chunks spread
+  // the weight stream more evenly over the SMs), a divisor of the block's TMA stages. The
+  // chunking depends on the shape only, never on which experts are active.
+  const int stages_per_block = pl.KB / pl.kbs_g;
+  pl.kch = 1;
+  // (at most kDecodeMaxKch chunks, 4 beyond four tokens: the finisher keeps one load per
+  // chunk and group of four token columns in flight)
+  const int kch_cap = T > 4 ? kDecodeMaxKch / 2 : kDecodeMaxKch;
+  for (int d = 1; d <= stages_per_block && d <= kch_cap; ++d)
+    if (stages_per_block % d == 0 && (int64_t)pl.u_max * pl.NB * d <= kDecodeMaxChunks) pl.kch = d;
+  pl.ckb = pl.KB / pl.kch;
+  pl.part_bytes = (size_t)pl.u_max * pl.NB * pl.kch * dk::kPartCols * dk::kBM * 4;
   pl.cnt_words = (size_t)pl.u_max * pl.NJ + pl.u_max + (size_t)T * pl.HB;
   return pl;
 }
@@ -738,14 +897,6 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, const DecodePlan& pl, cudaS
     return cudaSuccess;
   }
   const int G = sm_count() < kDecodeGrid ? sm_count() : kDecodeGrid;
-  // partial-sum slots: the plan sized them for kDecodeGrid CTAs; fewer CTAs take more each
-  const int64_t kch = pl.KB / pl.kbs_g;
-  const int64_t per = ((int64_t)pl.u_max * pl.NB * kch + G - 1) / G;
-  const int spc = (int)((per + kch - 1) / kch + 1);
-  if ((size_t)G * spc * dk::kPartCols * dk::kBM * 4 > pl.part_bytes) {
-    *unsupported = 1;
-    return cudaSuccess;
-  }
   int dev = 0;
   cudaGetDevice(&dev);
   static size_t budget[64] = {};
@@ -760,10 +911,12 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, const DecodePlan& pl, cudaS
   }
   const size_t stage = (size_t)pl.kbs_g * (dk::kSubW + dk::kSubX);
   const int prod_kb = pl.KB > pl.KB2 ? pl.KB : pl.KB2;
-  const size_t fixed = 1024 + 2 * (size_t)pl.KB2 * dk::kSubX + (size_t)prod_kb * dk::kN * 4 +
+  const size_t fixed = 1024 + 2 * (size_t)pl.KB2 * dk::kSubX + 2 * (size_t)prod_kb * dk::kN * 4 +
                        4 * dk::kMaxRowsPerExpert * 4 + 8 /*bar align*/;
   int stages = dk::kMaxStages;
-  auto bytes = [&](int s) { return fixed + (size_t)s * stage + (size_t)(2 * s + 2 * dk::kAcc + 4) * 8; };
+  auto bytes = [&](int s) {
+    return fixed + (size_t)s * stage + (size_t)(2 * s + 2 * dk::kAcc + 8 + 2 * dk::kQueue) * 8;
+  };
   while (stages > 2 && bytes(stages) > max_smem) --stages;
   const size_t smem = bytes(stages);
   if (smem > max_smem) {
@@ -817,7 +970,8 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, const DecodePlan& pl, cudaS
   p.kbs_g = pl.kbs_g;
   p.kbs_d = pl.kbs_d;
   p.stages = stages;
-  p.spc = spc;
+  p.kch = pl.kch;
+  p.ckb = pl.ckb;
   p.u_max = pl.u_max;
   static size_t granted[64] = {};
   if (dev < 0 || dev >= 64 || smem > granted[dev]) {

@@ -174,13 +174,15 @@ constexpr int kDecodeMaxTokens = 8;     // token columns the kernel keeps
 constexpr int kDecodeMaxRoutes = 64;    // tokens * topk
 constexpr int kDecodeMaxExperts = 1024; // bitmap of active experts
 constexpr int kDecodeGrid = 152;        // persistent CTAs (at most; one per SM)
+constexpr int kDecodeMaxChunks = 2048;  // gate/up chunks the partial sums are sized for (8 MiB)
+constexpr int kDecodeMaxKch = 8;        // chunks per gate/up block
 struct DecodePlan {
   bool ok;
   int KB, KB2, NJ, NB, HB;  // H/128, I/128, I/128, 2I/128, H/128
   int kbs_g, kbs_d;         // K blocks per TMA stage (gate/up, down)
   int u_max;                // most distinct experts the routes can reach
-  int spc;                  // partial-sum slots per CTA (for kDecodeGrid CTAs)
-  size_t part_bytes;        // partial sums [kDecodeGrid * spc][8][128] float
+  int kch, ckb;             // chunks per gate/up block, K blocks per chunk
+  size_t part_bytes;        // partial sums [u_max * NB * kch][8][128] float
   size_t cnt_words;         // counters: pairs, experts, (token, H block)
 };
 DecodePlan decode_plan(int64_t T, int32_t topk, int32_t E, int64_t H, int64_t I);

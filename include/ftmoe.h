@@ -272,11 +272,12 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * 4 = fused decode path: after a launch that quantizes the token rows, gate/up, SiLU-and-mul
  * with FP8 re-quantization, down and the combine run in one persistent tensor-core kernel
  * whose weight stream is split evenly over the SMs (FP8; T <= 8, T*topk <= 64, E <= 1024,
- * H and I multiples of 128, H <= 8192, I <= 2048; at most 16 routes per expert, further
- * routes to one expert are skipped and raise FTMOE_ERR_EXPERT_ID_RANGE).
- * Automatic: the grouped path, fused where the token tile is at most 64, the bank has at
- * most 1024 experts and the routes can reach at least 2048 (expert, gate/up block pair) units
- * (min(T*topk, E) * I/128 >= 2048), else with the separate kernel. Paths 2 and 3 give bit-identical outputs; path 4 adds the partial
+ * H and I multiples of 128, H <= 8192, I <= 2048; a token that lists one expert twice
+ * computes that expert once and weights it per listing).
+ * Automatic: the fused decode path where its limits hold; else the grouped path, fused where
+ * the token tile is at most 64, the bank has at most 1024 experts and the routes can reach at
+ * least 2048 (expert, gate/up block pair) units (min(T*topk, E) * I/128 >= 2048), else with
+ * the separate kernel. Paths 2 and 3 give bit-identical outputs; path 4 adds the partial
  * sums of a gate/up element in another order, so it agrees with them within the fp32
  * rounding of that sum.
  * ------------------------------------------------------------------------------------ */
@@ -328,10 +329,10 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
  * this library). For callers that cannot allocate device memory themselves: a plugin
  * hosted by a runtime that owns all device memory and exposes no allocator, or a latency
  * path that cannot afford an allocation's implicit synchronisation. The intermediates
- * live in a file-scope device array of 8 MiB that every GPU loading the library keeps
+ * live in a file-scope device array of 16 MiB that every GPU loading the library keeps
  * until the process exits; shapes whose workspace (ftmoe_forward_workspace_bytes)
  * exceeds it return FTMOE_WORKSPACE_TOO_SMALL. Decode-size shapes fit (8 tokens, top-8,
- * hidden 4096, intermediate 1024 need about 1.7 MiB).
+ * hidden 4096, intermediate 1024 need about 9.2 MiB on the fused decode path).
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current and caches it; make that first call before any stream capture.
  * The cached address belongs to the device's primary context: after the context is

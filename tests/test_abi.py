@@ -99,7 +99,9 @@ def test_forward_workspace_layout(ft):
         assert lay[key] % 256 == 0
     assert lay["rows_q"] > 0  # eight tokens take the grouped path: gather buffers
     auto2 = ft.ftmoe_forward_workspace_layout(ft.moe_shape(2, 4096, 1024, 8, 64))
-    assert auto2["rows_q"] > 0  # the automatic path is the grouped one at every batch size
+    assert auto2["rows_q"] == 0 and auto2["partials_bytes"] > 0  # automatic at 2 tokens: fused decode
+    auto16 = ft.ftmoe_forward_workspace_layout(ft.moe_shape(16, 4096, 1024, 8, 64))
+    assert auto16["rows_q"] > 0  # beyond 8 tokens: the grouped path
     slot = ft.ftmoe_forward_workspace_layout(ft.moe_shape(2, 4096, 1024, 8, 64, path=1))
     assert slot["rows_q"] == 0 and slot["dst2src"] == 0  # route-slot path: no gather buffers
     g = ft.ftmoe_forward_workspace_layout(ft.moe_shape(256, 7168, 2048, 6, 256))
@@ -140,18 +142,20 @@ def test_forward_rejects_inconsistent_banks(ft):
 
 
 def test_automatic_forward_path_choice(ft):
-    # SiLU-and-mul fused into the gate/up GEMM (no fp32 gate/up buffer) where the token
-    # tile is at most 64 and min(T * topk, E) * I / 128 >= 2048; the separate kernel
-    # otherwise and for NVFP4
+    # the fused decode path up to 8 tokens (FP8); beyond, SiLU-and-mul fused into the gate/up
+    # GEMM (no fp32 gate/up buffer) where the token tile is at most 64 and
+    # min(T * topk, E) * I / 128 >= 2048; the separate kernel otherwise and for NVFP4
     lay = ft.ftmoe_forward_workspace_layout
-    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64))["partials_bytes"] > 0         # fused decode path
+    assert lay(ft.moe_shape(16, 4096, 1024, 8, 64))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256))["gateup_bytes"] > 0       # tile 128
     assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, tok_tile=32))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(1024, 7168, 2048, 6, 256))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(256, 7168, 2048, 6, 256))["gateup_bytes"] == 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=3))["gateup_bytes"] == 0
-    assert lay(ft.moe_shape(1, 4096, 1024, 8, 64))["gateup_bytes"] > 0
-    assert lay(ft.moe_shape(1, 2048, 768, 8, 8))["gateup_bytes"] > 0
+    assert lay(ft.moe_shape(1, 4096, 1024, 8, 64))["partials_bytes"] > 0
+    assert lay(ft.moe_shape(1, 2048, 768, 8, 8))["partials_bytes"] > 0
+    assert lay(ft.moe_shape(1, 4096, 1024, 8, 64, path=2))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, fmt=ft.FMT_NVFP4))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=2))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(2048, 7168, 2048, 6, 2048))["gateup_bytes"] > 0  # beyond the GEMM's 1024 experts
@@ -171,7 +175,7 @@ def test_fused_decode_workspace(ft):
     assert d["partials_bytes"] > 0 and d["counters_bytes"] == 4 * (64 * 8 + 64 + 8 * 32)
     for key in ("x_q", "x_scales", "act_q", "act_scales", "down", "partials", "counters"):
         assert d[key] % 256 == 0
-    assert d["total"] <= 8 << 20  # the decode shapes still fit the allocation-free forward's array
+    assert d["total"] <= 16 << 20  # the decode shapes still fit the allocation-free forward's array
     # outside its limits (more than 8 tokens, NVFP4, I > 2048) the path is unsupported: the
     # layout falls back to another path's and the forward refuses path 4
     assert lay(ft.moe_shape(9, 4096, 1024, 8, 64, path=4))["partials_bytes"] == 0

@@ -30,7 +30,7 @@ def _check(prob, out, ids=None, weights=None, x=None):
     return prob.check(out, ids=ids, weights=weights, x=x)
 
 
-@pytest.mark.parametrize("path", [0, 1, 2, 3])
+@pytest.mark.parametrize("path", [0, 1, 2, 3, 4])
 def test_decode_2048_768_two_of_eight_active(ft, path):
     # hidden 2048, intermediate 768, 8 resident experts, top-k 8, 6 of 8 slots -1
     p = Problem(1, 2048, 768, 8, 8, seed=0xF7E00001, active=2)
@@ -40,12 +40,13 @@ def test_decode_2048_768_two_of_eight_active(ft, path):
     _check(p, out)
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 @pytest.mark.parametrize("T", [1, 8])
 @pytest.mark.parametrize("active", [8, 4, 2, 0])
 def test_decode_4096_1024_sweep(ft, T, active, path):
     # path 1: route-slot streaming kernel; path 2: segment + gather + tcgen05 grouped GEMMs;
-    # path 3: the same with SiLU-and-mul fused into the gate/up GEMM
+    # path 3: the same with SiLU-and-mul fused into the gate/up GEMM; path 4: the fused
+    # decode kernel (gate/up, SiLU-and-mul, down and combine in one launch)
     p = Problem(T, 4096, 1024, 64, 8, seed=0xF7E00002, active=active)
     out, ws, shape = p.forward(path=path)
     torch.cuda.synchronize()
@@ -57,9 +58,13 @@ def test_decode_4096_1024_sweep(ft, T, active, path):
 
 def _poison(ws, lay):
     nan = torch.tensor([0x7FC00000], dtype=torch.int32).view(torch.float32).item()
+    # the fused decode path's partial sums and arrival counters too (the counters must be
+    # zeroed by the forward itself on every call)
     for off, nbytes, kind in ((lay["gateup"], lay["gateup_bytes"], "f"), (lay["down"], lay["down_bytes"], "f"),
                               (lay["act_q"], lay["act_q_bytes"], "b"),
-                              (lay["act_scales"], lay["act_scales_bytes"], "f")):
+                              (lay["act_scales"], lay["act_scales_bytes"], "f"),
+                              (lay["partials"], lay["partials_bytes"], "f"),
+                              (lay["counters"], lay["counters_bytes"], "b")):
         region = ws[off:off + nbytes]
         if kind == "f":
             region.view(torch.float32).fill_(nan)
@@ -67,7 +72,7 @@ def _poison(ws, lay):
             region.fill_(0xFF)
 
 
-@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (8, 2), (8, 3)])
+@pytest.mark.parametrize("T,path", [(1, 1), (8, 1), (8, 2), (8, 3), (1, 4), (8, 4)])
 def test_graph_replay_with_poisoned_intermediates(ft, T, path):
     H, I, E, k = 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=8)
@@ -121,7 +126,7 @@ def test_graph_replay_with_poisoned_intermediates(ft, T, path):
         assert not torch.any(torch.isnan(out.float()))
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 def test_negative_slots_equal_clamped_zero_weight_path(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=2)
@@ -135,7 +140,7 @@ def test_negative_slots_equal_clamped_zero_weight_path(ft, path):
     assert torch.equal(out_new.view(torch.int16), out_old.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 def test_all_inactive_and_empty_bank_use(ft, path):
     T, H, I, E, k = 8, 4096, 1024, 64, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00002, active=0)
@@ -145,14 +150,15 @@ def test_all_inactive_and_empty_bank_use(ft, path):
     assert torch.all(out.view(torch.int16) == 0)
 
 
-def test_out_of_range_expert_id_is_flagged_not_read(ft):
+@pytest.mark.parametrize("path", [1, 4])
+def test_out_of_range_expert_id_is_flagged_not_read(ft, path):
     T, H, I, E, k = 1, 2048, 768, 8, 8
     p = Problem(T, H, I, E, k, seed=0xF7E00001, active=2)
     ft.ftmoe_read_error_flags()
     ids = p.ids.clone()
     ids[0, (ids[0] < 0).nonzero()[0, 0]] = E + 3  # one bad id in place of an inactive slot
     w = p.w.clone()
-    out, _, _ = p.forward(path=1, ids=ids, weights=w)
+    out, _, _ = p.forward(path=path, ids=ids, weights=w)
     flags = ft.ftmoe_read_error_flags()
     assert flags & ft.ERR_EXPERT_ID_RANGE
     ref_ids = torch.where(ids >= E, torch.full_like(ids, -1), ids)

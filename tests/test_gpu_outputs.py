@@ -41,7 +41,7 @@ def test_combine_single_route_of_weight_one_is_the_rounded_row(ft, dtype):
     assert torch.equal(out, rows.to(dtype))
 
 
-@pytest.mark.parametrize("path", [0, 1, 3])
+@pytest.mark.parametrize("path", [0, 1, 3, 4])
 def test_forward_output_types_agree_and_match_the_oracle(ft, path):
     T, H, I, E, k = 8, 1024, 512, 16, 4
     p = Problem(T, H, I, E, k, seed=0xF7E0_0F16, active=[4, 3, 0, 4, 2, 4, 1, 4])

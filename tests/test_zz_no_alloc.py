@@ -31,9 +31,9 @@ def _problem(ft, T, H, I, E, k, seed):
     return x, ids, w, (gq, gs, dq, ds)
 
 
-# path 0: the automatic choice (grouped path, separate SiLU-and-mul kernel at this size);
-# path 3: SiLU-and-mul fused into the gate/up GEMM
-@pytest.mark.parametrize("path", [0, 3])
+# path 0: the automatic choice; path 3: SiLU-and-mul fused into the gate/up GEMM; path 4: the
+# fused decode kernel (its partial sums and counters live in the shared array too)
+@pytest.mark.parametrize("path", [0, 3, 4])
 def test_noalloc_forward_equals_workspace_forward_two_calls(path):
     import block_quantized_moe_gb300 as ft
     T, H, I, E, k = 4, 1024, 512, 16, 4
