@@ -534,6 +534,14 @@ def time_in_graph(fn, prep, steps):
     return total
 
 
+def event_floor_us(prep, steps, device):
+    """Time between two event nodes around a one-element tensor update in its own graph (the
+    same method as the kernels' launch_us): the floor that every launch_us figure includes."""
+    tiny = torch.zeros(1, device=device)
+    ms = time_in_graph(lambda: tiny.add_(1.0), prep, steps)
+    return None if ms is None else round(ms * 1e3 / steps, 3)
+
+
 def time_events(fn, prep, steps, stream):
     """Sum of per-call CUDA-event durations (ms) over `steps` calls; prep() runs outside."""
     total = 0.0
@@ -699,6 +707,7 @@ def run_gpu(args, rank, world, local):
                      "achieved": round(k_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(k_gbs / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
                      "launch_us": round(k_us, 3), "timing": k_timing,
+                     "event_floor_us": event_floor_us(prep, args.steps, dev),
                      "algorithmic_bytes_per_launch": int(gu_bytes_avg),
                      f"{mma_name}_tflops": round(k_tflops, 2),
                      f"{mma_name}_frac_of_dense_peak": round(k_tflops / mma_peak, 4),
@@ -809,7 +818,8 @@ def run_gather(args, rank, world, local):
         "algorithmic_bytes_per_call": int(bytes_avg),
         "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": round(bytes_avg / (k_us * 1e-6) / 1e9, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(bytes_avg / (k_us * 1e-6) / 1e9 / hbm_peak, 4),
-                     "traffic": None, "launch_us": round(k_us, 3), "timing": k_timing, "peak_source": peak_src},
+                     "traffic": None, "launch_us": round(k_us, 3), "timing": k_timing,
+                     "event_floor_us": event_floor_us(prep, args.steps, dev), "peak_source": peak_src},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": T * k + T * ng * 4 + n_dst * 4,
                 "d2h_bytes_per_step": n_dst * row},
         "gpu_launches": args.steps, "clocks": clk,
