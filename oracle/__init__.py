@@ -19,9 +19,13 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   moe.silu_mul                        pinned: scipy.special.expit, closed-form points
   moe.combine                         pinned: single route of weight 1, all inactive
   moe.pick_tile                       pinned: the dsfp4 page's table (tests/golden)
+  slots.step                          pinned: a worked example, closed-form cases (empty pool,
+                                      no fetch budget, slots used this step), invariants on
+                                      random step sequences against the minimum-(usage, slot)
+                                      formulation of the victim choice
   cpu (cpu_oracle.cpp)                the same definitions written again in plain C++17 with
                                       std::thread; pinned to the numpy oracle above (codes,
                                       scales, indices and bytes bit for bit; FFN outputs to
                                       float64 rounding) and to the same closed forms
 """
-from . import formats, moe  # noqa: F401
+from . import formats, moe, slots  # noqa: F401
