@@ -96,6 +96,8 @@ _SIGNATURES = [
     ("ftmoe_moe_forward", c_i32, [ctypes.POINTER(MoeArgs), c_ptr, c_size, c_ptr]),
     ("ftmoe_moe_forward_noalloc", c_i32, [ctypes.POINTER(MoeArgs), c_ptr]),
     ("ftmoe_selftest_wait_timeout", c_i32, [ctypes.c_uint64, c_ptr, c_ptr]),
+    ("ftmoe_expert_slots", c_i32, [c_ptr, c_i64, c_ptr, c_ptr, c_i32, c_ptr, c_i32, c_i64, c_i32, c_ptr, c_ptr,
+                                   c_ptr]),
     ("ftmoe_read_error_flags", c_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 ]
 
@@ -290,6 +292,16 @@ def ftmoe_moe_forward_noalloc(shape, x, expert_ids, route_weights, bank_gateup, 
     args = MoeArgs(shape, _p(x), x.stride(0), _p(expert_ids), _p(route_weights), bank_gateup,
                    bank_down, _p(out), out.stride(0))
     _check("ftmoe_moe_forward_noalloc", lib().ftmoe_moe_forward_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+def ftmoe_expert_slots(expert_ids, slot_expert, slot_usage, expert_slot, step, max_fetch, fetch_plan, n_fetch,
+                       stream=None):
+    """One step of the device-side expert-slot pool: expert_ids (int32, any shape) become slot
+    ids in place; the pool state tensors are updated in place."""
+    _check("ftmoe_expert_slots", lib().ftmoe_expert_slots(
+        _p(expert_ids), expert_ids.numel(), _p(slot_expert), _p(slot_usage), slot_expert.numel(),
+        _p(expert_slot), expert_slot.numel(), int(step), int(max_fetch), _p(fetch_plan), _p(n_fetch),
+        _stream(stream)))
 
 
 def ftmoe_selftest_wait_timeout(timeout_ns, elapsed_ns=None, stream=None):

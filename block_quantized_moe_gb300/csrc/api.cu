@@ -609,7 +609,8 @@ ftmoe_status ftmoe_read_error_flags(uint32_t* flags) {
   if (!flags) return FTMOE_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return FTMOE_CUDA_ERROR;
   *flags = read_err_quant() | read_err_segment() | read_err_gather() | read_err_stream_gemm() |
-           read_err_tc_gemm() | read_err_nvfp4() | read_err_act() | read_err_selftest() | read_err_decode();
+           read_err_tc_gemm() | read_err_nvfp4() | read_err_act() | read_err_selftest() | read_err_decode() |
+           read_err_slots();
   return FTMOE_OK;
 }
 

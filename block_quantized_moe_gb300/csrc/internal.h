@@ -169,6 +169,11 @@ uint32_t read_err_act();
 // selftest.cu
 uint32_t read_err_selftest();
 
+// slot_pool.cu: device-side expert-slot pool (one CTA; routes and experts staged in shared memory)
+constexpr int64_t kSlotPoolMaxRoutes = 16384;
+constexpr int32_t kSlotPoolMaxExperts = 16384;
+uint32_t read_err_slots();
+
 // decode_fused.cu: the fused decode forward (prep launch + one persistent kernel)
 constexpr int kDecodeMaxTokens = 8;     // token columns the kernel keeps
 constexpr int kDecodeMaxRoutes = 64;    // tokens * topk

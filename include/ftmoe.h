@@ -344,6 +344,33 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
  * called. Inputs, outputs and their ownership are as for ftmoe_moe_forward. */
 ftmoe_status ftmoe_moe_forward_noalloc(const ftmoe_moe_args* args, void* stream);
 
+/* Device-side expert-slot pool, one decode step per call (FreeToken hybrid expert-cache page,
+ * the pull request that speeds up victim selection in its ensure-experts kernel: Summary,
+ * Change and Fix). It keeps a pool of num_slots expert slots on the device and turns a step's
+ * routes into slot ids for the forward (a slot id in expert_ids, -1 for a route whose expert
+ * is not resident and runs elsewhere):
+ *   1. every requested expert that is resident marks its slot used: slot_usage = step, which
+ *      makes it the most recently used slot of the pool;
+ *   2. the distinct requested experts that are not resident, in order of first appearance
+ *      among the routes and at most max_fetch of them, each take the least recently used slot
+ *      among those not used in this step (slot_usage < step), ties to the lowest slot; the
+ *      slot's previous expert is evicted and fetch_plan[i] = {slot, expert} (int32 pairs,
+ *      host's copy list) for i < *n_fetch; when every slot was used in this step the
+ *      remaining misses stay missing;
+ *   3. expert_ids[r] is rewritten in place to the slot of its expert, or -1 -- after every
+ *      route has been read.
+ * State (device, owned by the caller, updated in place): slot_expert int32 [num_slots] (expert
+ * held, -1 empty), slot_usage int64 [num_slots] (step of last use, -1 never; start with -1),
+ * expert_slot int32 [num_experts] (slot of expert e, -1 if not resident); the two maps must be
+ * inverse to each other (an empty pool: all -1). step must exceed every slot_usage entry.
+ * expert_ids int32 [routes] (< 0 inactive; ids >= num_experts are treated as inactive and
+ * raise FTMOE_ERR_EXPERT_ID_RANGE). fetch_plan int32 [max_fetch][2]; n_fetch device int32.
+ * Limits: routes <= 16384, num_experts <= 16384 (else FTMOE_INVALID_ARG). One CTA; the
+ * results are deterministic. */
+ftmoe_status ftmoe_expert_slots(int32_t* expert_ids, int64_t routes, int32_t* slot_expert, int64_t* slot_usage,
+                                int32_t num_slots, int32_t* expert_slot, int32_t num_experts, int64_t step,
+                                int32_t max_fetch, int32_t* fetch_plan, int32_t* n_fetch, void* stream);
+
 /* Self-test of the bounded pipeline waits (failure detection; the pages have no counterpart).
  * Every wait of the TMA/tensor-core pipelines gives up after a time limit (4 s), raises
  * FTMOE_ERR_WAIT_TIMEOUT in the device error word and lets its kernel return normally, so a

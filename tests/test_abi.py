@@ -79,6 +79,12 @@ def test_invalid_arguments_rejected_on_host(ft):
     for d in (ft.OUT_BF16, ft.OUT_FP16, ft.OUT_FP32):
         assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, d, None, 16, None) == ft.FTMOE_OK
     assert L.ftmoe_combine(None, 16, None, None, None, 0, 2, 16, 3, None, 16, None) == ft.FTMOE_INVALID_ARG
+    # the expert-slot pool: sizes and the pointers it needs are checked on the host
+    fake = ctypes.c_void_p(256)
+    assert L.ftmoe_expert_slots(fake, 4, fake, fake, 0, fake, 8, 0, 1, fake, fake, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_expert_slots(fake, 4, fake, fake, 4, fake, 20000, 0, 1, fake, fake, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_expert_slots(fake, 20000, fake, fake, 4, fake, 8, 0, 1, fake, fake, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_expert_slots(fake, 4, fake, fake, 4, fake, 8, 0, 2, None, fake, None) == ft.FTMOE_INVALID_ARG
     # the wait self-test takes a limit of 1 us .. 1 s
     assert L.ftmoe_selftest_wait_timeout(999, None, None) == ft.FTMOE_INVALID_ARG
     assert L.ftmoe_selftest_wait_timeout(2 * 10 ** 9, None, None) == ft.FTMOE_INVALID_ARG
