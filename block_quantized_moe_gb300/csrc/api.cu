@@ -233,8 +233,8 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
   return FTMOE_OK;
 }
 
-// Automatic path: the grouped tensor-core path at every batch size. Measured on GB300
-// with four K blocks per TMA box, it matches the route-slot streaming kernel at one token
+// Automatic path beyond the fused decode path's limits: the grouped tensor-core path. Measured
+// on GB300 with four K blocks per TMA box, it matches the route-slot streaming kernel at one token
 // (49.6 vs 50.4 us for 8 active routes of 4096/1024) and beats it from two tokens on (68 vs
 // 86 us); the route-slot path stays available as path 1.
 bool use_grouped(const ftmoe_moe_shape* s) { return s->path != 1 && s->path != 4; }
