@@ -20,10 +20,14 @@
 // products formed once per chunk of K blocks. Up to sixteen TMEM accumulators (512 columns
 // at most) rotate so the MMA runs ahead of the promotion.
 //
-// One persistent CTA per SM takes a contiguous range of units, weight blocks innermost:
-// every weight tile is read once and a token tile is read again from L2 by the units that
-// share it; the weight-scale rows of the next unit and the next chunk of activation scales
-// are fetched while the current ones are in use. Roles: warp 0 = TMA producer, warp 1 = MMA
+// One persistent CTA per SM; CTA c takes units c, c + G, c + 2G, ... (G CTAs) of the list
+// ordered (expert, token tile, weight block), weight blocks innermost. At any moment the CTAs
+// work on G consecutive units, a few experts' token tiles, which L2 serves to the CTAs that
+// read them at about the same time; every weight tile is read once. (Contiguous ranges per
+// CTA kept one token tile per CTA live for its whole run: at token tile 128 and K = 7168 that
+// is 152 tiles of 0.9 MB, more than L2 holds, and the re-reads went to DRAM.) The
+// weight-scale rows of the next unit and the next chunk of activation scales are fetched
+// while the current ones are in use. Roles: warp 0 = TMA producer, warp 1 = MMA
 // issuer (and TMEM owner), the last 16 warps = epilogue (four groups of four warps, one
 // group per quarter of the token columns; warp w reads TMEM lanes 32*(w%4) .. +31). Every
 // mbarrier wait is bounded: on timeout the kernel raises FTMOE_ERR_WAIT_TIMEOUT, stops all
@@ -237,10 +241,11 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   }
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
-  // a contiguous range of units per CTA; units run (expert, token tile, weight block) with
-  // the weight block innermost, so the token tile stays in L2 across units
-  const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
-  const int u_end = (int)(((int64_t)(blockIdx.x + 1) * total_units) / gridDim.x);
+  // units c, c + G, ...: the CTAs sweep the (expert, token tile, weight block) list together,
+  // so a token tile is read by several CTAs at about the same time and stays in L2
+  const int u_begin = blockIdx.x;
+  const int u_end = total_units;
+  const int u_step = gridDim.x;
 
   // unit -> (expert, weight block or block pair, token tile, first row, rows in tile)
   auto decode = [&](int u, int& e, int& nb, int& tt, int& row0, int& rows) {
@@ -295,7 +300,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       auto advance = [&]() {
         if (++sp == SP) {
           sp = 0;
-          if (++u < u_end) decode(u, e, nb, tt, row0, rows);
+          if ((u += u_step) < u_end) decode(u, e, nb, tt, row0, rows);
         }
       };
       // The weight tiles of the first pass over the ring go out before the wait: they do
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       uint32_t it = 0, kc = 0;
       constexpr uint32_t idesc = idesc_f8(TT);
       const int SP = (KB + KBS - 1) / KBS;
-      for (int u = u_begin; u < u_end && !s_abort; ++u) {
+      for (int u = u_begin; u < u_end && !s_abort; u += u_step) {
         bool ok = true;
         for (int sp = 0; sp < SP && ok; ++sp, ++it) {
           const int st = it % S;
@@ -441,7 +446,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       decode(u_begin, e0, nb0, tt0, r00, rows0);
       sa_issue(r00, rows0, 0, 0);
     }
-    for (int u = u_begin; u < u_end; ++u) {
+    for (int u = u_begin; u < u_end; u += u_step) {
       int e, nb, tt, row0, rows;
       decode(u, e, nb, tt, row0, rows);
       // all warps of the group leave together on an abort; the barrier also orders the
@@ -455,9 +460,9 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
               have_next ? sw_next[b] : __ldg(p.w_s + ((int64_t)e * NB + wblock(nb, b)) * KB + tid_g);
       }
       have_next = false;
-      if (u + 1 < u_end && tid_g < KB) {
+      if (u + u_step < u_end && tid_g < KB) {
         int e2, nb2, tt2, r02, rows2;
-        decode(u + 1, e2, nb2, tt2, r02, rows2);
+        decode(u + u_step, e2, nb2, tt2, r02, rows2);
 #pragma unroll
         for (int b = 0; b < WB; ++b) sw_next[b] = __ldg(p.w_s + ((int64_t)e2 * NB + wblock(nb2, b)) * KB + tid_g);
         have_next = true;
@@ -480,9 +485,9 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
           named_bar(1 + grp, 128);
           if (ch + 1 < nchunks) {
             sa_issue(row0, rows, ch + 1, (gch + 1) & 1);
-          } else if (u + 1 < u_end) {
+          } else if (u + u_step < u_end) {
             int e2, nb2, tt2, r02, rows2;
-            decode(u + 1, e2, nb2, tt2, r02, rows2);
+            decode(u + u_step, e2, nb2, tt2, r02, rows2);
             sa_issue(r02, rows2, 0, (gch + 1) & 1);
           }
           ++gch;

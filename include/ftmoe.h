@@ -132,7 +132,7 @@ typedef struct ftmoe_routes {
  * 16/32/64/128; 0 = ftmoe_pick_tile's choice. wblocks: 128-row weight blocks per
  * tensor-core unit, sharing one token tile: 1, 2 (adjacent blocks; needs n % 256 == 0 and
  * k % 128 == 0, else the request is treated as unsupported by the tcgen05 kernel), or 0 =
- * automatic (2 from token tile 64 on where allowed, else 1). Results do not depend on it. */
+ * automatic (2 at token tile 64 where allowed, else 1). Results do not depend on it. */
 typedef struct ftmoe_tile {
   int32_t tok_tile;
   int32_t variant;
