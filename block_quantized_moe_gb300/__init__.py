@@ -45,7 +45,7 @@ class Routes(ctypes.Structure):
 
 
 class Tile(ctypes.Structure):
-    _fields_ = [("tok_tile", c_i32), ("variant", c_i32), ("wblocks", c_i32), ("reserved", c_i32)]
+    _fields_ = [("tok_tile", c_i32), ("variant", c_i32), ("wblocks", c_i32), ("ctas", c_i32)]
 
 
 class MoeShape(ctypes.Structure):
@@ -208,12 +208,12 @@ def slot_routes(expert_ids):
     return Routes(ROUTES_SLOTS, topk, T, None, _p(expert_ids))
 
 
-def _tile(tok_tile=0, variant=0, wblocks=0):
-    return Tile(tok_tile, variant, wblocks, 0)
+def _tile(tok_tile=0, variant=0, wblocks=0, ctas=0):
+    return Tile(tok_tile, variant, wblocks, ctas)
 
 
-def ftmoe_grouped_gemm_gateup(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, stream=None):
-    t = _tile(tok_tile, variant, wblocks)
+def ftmoe_grouped_gemm_gateup(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, ctas=0, stream=None):
+    t = _tile(tok_tile, variant, wblocks, ctas)
     _check("ftmoe_grouped_gemm_gateup", lib().ftmoe_grouped_gemm_gateup(
         ctypes.byref(act), ctypes.byref(routes), ctypes.byref(bank), _p(out), out.stride(0),
         ctypes.byref(t), _stream(stream)))
@@ -226,8 +226,8 @@ def ftmoe_grouped_gemm_gateup_silu(act, routes, bank, q, scales, tok_tile=0, str
         ctypes.byref(t), _stream(stream)))
 
 
-def ftmoe_grouped_gemm_down(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, stream=None):
-    t = _tile(tok_tile, variant, wblocks)
+def ftmoe_grouped_gemm_down(act, routes, bank, out, tok_tile=0, variant=0, wblocks=0, ctas=0, stream=None):
+    t = _tile(tok_tile, variant, wblocks, ctas)
     _check("ftmoe_grouped_gemm_down", lib().ftmoe_grouped_gemm_down(
         ctypes.byref(act), ctypes.byref(routes), ctypes.byref(bank), _p(out), out.stride(0),
         ctypes.byref(t), _stream(stream)))

@@ -43,6 +43,47 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same as launch_kernel, in clusters of cluster_x CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t st, bool allow_overlap, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (allow_overlap && pdl_enabled()) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Clusters of cluster_x CTAs of this kernel that can be resident at once on the device (0 if
+// the query fails).
+template <typename... KArgs>
+inline int max_active_clusters(void (*kernel)(KArgs...), dim3 block, size_t smem, int cluster_x, int grid_x) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_x);
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
 // tc_gemm.cu: host helpers shared by the TMA-fed kernels
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -123,6 +164,7 @@ struct TcGemmArgs {
   const int32_t* offsets;
   int32_t tok_tile;
   int32_t wblocks;         // 1: one 128-row weight block per unit, 2: two adjacent blocks
+  int32_t ctas;            // 1: a unit on one SM; 2: a CTA pair (cluster of two), one block each
   int32_t silu;            // 1: gate block j + up block j per unit, SiLU-and-mul + FP8 requant
   uint8_t* q_out;          // silu: codes [a_rows][n/2]
   float* s_out;            // silu: scales [a_rows][n/256]

@@ -70,6 +70,43 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return true;
 }
 
+// ---- clusters of two CTAs (a CTA pair sharing one tcgen05 MMA) ----
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// arrive on an mbarrier of any CTA of the cluster. The default semantics (release at CTA
+// scope) cost no fence; what the arrival hands over is ordered by the tcgen05 fences around
+// it (an accumulator's TMEM reads are complete before tcgen05.fence::before_thread_sync).
+// A cluster-scope release put a memory barrier in front of every arrival: measured on GB300,
+// it made the CTA-pair GEMM's epilogue stall on it more than on anything else.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// every thread of both CTAs: release what each wrote, then acquire what the other wrote
+// (the forms without .aligned, so a warp need not be converged)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -135,6 +172,27 @@ __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// TMA loads of a CTA pair: the box lands in this CTA's shared memory and its bytes are
+// counted on `bar`, a shared::cluster address that may lie in the other CTA of the pair
+// (the pair's MMA issuer waits on one barrier for both CTAs' operands).
+__device__ __forceinline__ void tma_load_3d_hint_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                      int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                      int z, int w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
+
 // 4-byte global -> shared copy that bypasses registers; valid = false writes a zero
 // without reading (src must still be a valid address).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool valid) {
@@ -181,6 +239,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// CTA-pair MMAs: one arrival, once the issuing thread's earlier MMAs are complete, on the
+// barrier at shared-memory offset `bar` of every CTA in `mask` (bit r = cluster rank r)
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 
 // 16 consecutive fp32 TMEM columns of this thread's lane.

@@ -55,26 +55,44 @@ constexpr int kMaxExperts = 1024;
 //               matrix; the epilogue forms silu(g) * u for intermediate columns
 //               [128 j, 128 j + 128) -- exactly one 1x128 group -- and re-quantizes it to FP8
 //               with its group scale, so no fp32 gate/up row is ever written
+//   kCtaPair    weight blocks 2p and 2p + 1 on the two CTAs of a cluster (two SMs): CTA r
+//               streams block 2p + r and loads half of the token tile (rows r TT/2 ..); the
+//               first CTA issues tcgen05.mma.cta_group::2 with M = 256, which reads the
+//               weights and the token halves of both CTAs and leaves each CTA the fp32
+//               accumulator of its own block over all TT token columns
 // Two weight blocks per token tile halve the token bytes each stage carries for every
-// weight byte, so more weight bytes fit in flight in the same shared memory.
-enum Mode { kSingle = 0, kPair = 1, kGateUpSilu = 2 };
-__host__ __device__ constexpr int wb_of(int mode) { return mode == kSingle ? 1 : 2; }
+// weight byte, so more weight bytes fit in flight in the same shared memory. kPair does it
+// on one SM (twice the epilogue work per K block); kCtaPair across two, with the epilogue
+// work of one block per SM.
+enum Mode { kSingle = 0, kPair = 1, kGateUpSilu = 2, kCtaPair = 3 };
+__host__ __device__ constexpr int wb_of(int mode) { return mode == kPair || mode == kGateUpSilu ? 2 : 1; }
 
 // TMEM accumulators in rotation: as many (weight blocks x TT)-column accumulators as 512
 // columns hold, at most 16, so the MMA can run that many K blocks ahead of the promotion
 __host__ __device__ constexpr int acc_count(int cols) { return 512 / cols > 16 ? 16 : 512 / cols; }
 
-// Instruction descriptor, kind::f8f6f4: D fp32, A = B = e4m3, both K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_f8(int n) {
+// Instruction descriptor, kind::f8f6f4: D fp32, A = B = e4m3, both K-major, M = m, N = n.
+__host__ __device__ constexpr uint32_t idesc_f8(int n, int m = kBM) {
   return (1u << 4)                      // D format f32
          | (0u << 7) | (0u << 10)       // A, B format e4m3
          | ((uint32_t)(n >> 3) << 17)   // N >> 3
-         | ((uint32_t)(kBM >> 4) << 24);  // M >> 4
+         | ((uint32_t)(m >> 4) << 24);  // M >> 4
 }
 
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// CTA pair: one MMA over both CTAs' operands (M = 256, each CTA 128 weight rows and half of
+// the N token rows); each CTA's TMEM receives its own 128 rows of D
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -102,11 +120,13 @@ constexpr int kSaChunk = 8;                      // K blocks of activation scale
 // 128-byte-swizzled sub-tile (1024-byte aligned), exactly as in a one-block stage. Each TMA
 // instruction costs the SM a fixed time, so fewer, larger boxes move more bytes per SM: four
 // K blocks per box up to token tile 64, two at 128 (two or three stages still fit); with two
-// weight blocks per unit a box already carries twice the weight bytes per K block. A K that
-// is not a multiple of 128 keeps one K block per stage and the per-row maps, whose x extent
-// is K itself, so the partial last block is zero-filled rather than read past the row.
+// weight blocks per unit a box already carries twice the weight bytes per K block. A CTA pair
+// at token tile 128 carries four (two stages of 96 KiB): measured on GB300 at 24,576 routes,
+// gate/up took 1478 us with four, 1556 us with two and 1711 us with one. A K that is not a
+// multiple of 128 keeps one K block per stage and the per-row maps, whose x extent is K
+// itself, so the partial last block is zero-filled rather than read past the row.
 __host__ __device__ constexpr int kbs_for(int tt, int mode) {
-  return mode == kSingle ? (tt <= 64 ? 4 : 2) : (tt <= 32 ? 2 : 1);
+  return mode == kSingle ? (tt <= 64 ? 4 : 2) : (mode == kCtaPair ? 4 : (tt <= 32 ? 2 : 1));
 }
 
 // Warp roles. Warp 0 issues TMA, warp 1 issues MMAs, the last kEpiWarps warps promote.
@@ -129,7 +149,7 @@ template <int TT, int KBS, int MODE>
 struct Smem {
   static constexpr int kWB = wb_of(MODE);
   static constexpr int kSubW = kBM * kBK;     // 16 KiB: one K block of one weight block
-  static constexpr int kSubA = TT * kBK;      // TT * 128 B: one K block of tokens
+  static constexpr int kSubA = (MODE == kCtaPair ? TT / 2 : TT) * kBK;  // one K block of this CTA's tokens
   static constexpr int kTileW = kSubW * KBS * kWB;
   static constexpr int kTileA = kSubA * KBS;
   static constexpr int kStage = kTileW + kTileA;
@@ -182,6 +202,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, NB = p.nb_count, KB = p.kb_count;
   const int NBU = MODE == kSingle ? NB : NB / 2;  // units per token tile
+  // CTA pair: rank 0 issues the MMAs and owns the barriers that both CTAs' loads and
+  // epilogues report to; rank 1 works on weight block 2p + 1 and token rows TT/2 ..
+  constexpr bool kCP = MODE == kCtaPair;
+  const uint32_t crank = kCP ? cluster_rank() : 0u;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -191,7 +215,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(smem_u32(&tempty[i]), kCP ? 2 * kEpiWarps : kEpiWarps);  // one arrival per epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -224,12 +248,22 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     if (lane == 0) cum[E] = run;
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (kCP) {
+      // one warp of each CTA of the pair allocates, together: the same columns in both
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   fence_before();
-  __syncthreads();
+  if constexpr (kCP)
+    cluster_sync();  // both CTAs' barriers are initialised before either reports to the other
+  else
+    __syncthreads();
   fence_after();
   // everything above overlapped the previous kernel's tail; the token rows and their
   // scales come from the previous kernel (the producer thread waits after it has sent the
@@ -243,9 +277,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   const int total_units = cum[E];
   // units c, c + G, ...: the CTAs sweep the (expert, token tile, weight block) list together,
   // so a token tile is read by several CTAs at about the same time and stays in L2
-  const int u_begin = blockIdx.x;
+  // (a CTA pair counts as one: both CTAs run the same units)
+  const int u_begin = kCP ? (int)cluster_id_x() : (int)blockIdx.x;
   const int u_end = total_units;
-  const int u_step = gridDim.x;
+  const int u_step = kCP ? (int)cluster_count_x() : (int)gridDim.x;
 
   // unit -> (expert, weight block or block pair, token tile, first row, rows in tile)
   auto decode = [&](int u, int& e, int& nb, int& tt, int& row0, int& rows) {
@@ -264,7 +299,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   };
   // weight block (row block of the n x k matrix) b of unit index nb
   auto wblock = [&](int nb, int b) {
-    return MODE == kSingle ? nb : (MODE == kPair ? 2 * nb + b : b * NBU + nb);
+    return MODE == kSingle ? nb : (MODE == kPair ? 2 * nb + b : (kCP ? 2 * nb + (int)crank : b * NBU + nb));
   };
 
   if (warp < W::kCtl) {
@@ -278,7 +313,9 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
       // stage sp of a unit: K blocks [sp * KBS, sp * KBS + KBS)
       auto load_w = [&](uint32_t dst, uint32_t bar, int sp, int nb, int e, uint64_t pol) {
-        if constexpr (MODE == kGateUpSilu)
+        if constexpr (kCP)
+          tma_load_4d_hint_pair(dst, &map_w, bar, 0, (2 * nb + (int)crank) * kBM, sp * KBS, e, pol);
+        else if constexpr (MODE == kGateUpSilu)
           tma_load_5d_hint(dst, &map_w, bar, 0, 0, sp * KBS, nb, 2 * e, pol);
         else if constexpr (MODE == kPair)
           tma_load_4d_hint(dst, &map_w, bar, 0, nb * 2 * kBM, sp * KBS, e, pol);
@@ -288,13 +325,24 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
           tma_load_4d_hint(dst, &map_w, bar, 0, nb * kBM, sp * KBS, e, pol);
       };
       auto load_a = [&](uint32_t dst, uint32_t bar, int sp, int row0, uint64_t pol) {
-        if constexpr (KBS == 1 && MODE == kSingle)
+        if constexpr (kCP)
+          tma_load_3d_hint_pair(dst, &map_a, bar, 0, row0 + (int)crank * (TT / 2), sp * KBS, pol);
+        else if constexpr (KBS == 1 && MODE == kSingle)
           tma_load_2d_hint(dst, &map_a, bar, sp * kBK, row0, pol);
         else
           tma_load_3d_hint(dst, &map_a, bar, 0, row0, sp * KBS, pol);
       };
       uint32_t it = 0;
       const int SP = (KB + KBS - 1) / KBS;  // stages per unit
+      // CTA pair: both CTAs' bytes are counted on the first CTA's full barrier, which that
+      // CTA alone arms, for both (a box may land before it is armed: the phase cannot
+      // complete while the arming arrival is still pending)
+      auto full_target = [&](int st) {
+        return kCP ? mapa_shared(smem_u32(&full[st]), 0) : smem_u32(&full[st]);
+      };
+      auto arm_full = [&](int st) {
+        if (!kCP || crank == 0) mbar_expect_tx(smem_u32(&full[st]), kCP ? 2 * SM::kStage : SM::kStage);
+      };
       int u = u_begin, sp = 0, e = 0, nb = 0, tt = 0, row0 = 0, rows = 0;
       if (u < u_end) decode(u, e, nb, tt, row0, rows);
       auto advance = [&]() {
@@ -309,9 +357,8 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       int npre = 0;
       while (npre < S && u < u_end) {
         uint8_t* tw = tiles + (size_t)npre * SM::kStage;
-        const uint32_t fb = smem_u32(&full[npre]);
-        mbar_expect_tx(fb, SM::kStage);
-        load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
+        arm_full(npre);
+        load_w(smem_u32(tw), full_target(npre), sp, nb, e, pol_w);
         pre_sp[npre] = sp;
         pre_row0[npre] = row0;
         ++npre;
@@ -321,24 +368,25 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
       pdl_wait();
       pdl_trigger();
       for (int i = 0; i < npre; ++i)
-        load_a(smem_u32(tiles + (size_t)i * SM::kStage + SM::kTileW), smem_u32(&full[i]), pre_sp[i], pre_row0[i],
-               pol_a);
+        load_a(smem_u32(tiles + (size_t)i * SM::kStage + SM::kTileW), full_target(i), pre_sp[i], pre_row0[i], pol_a);
       while (u < u_end && !s_abort) {
         const int st = it % S;
         const uint32_t ph = (it / S) & 1;
         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, &s_abort)) break;
         uint8_t* tw = tiles + (size_t)st * SM::kStage;
         uint8_t* ta = tw + SM::kTileW;
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, SM::kStage);
+        const uint32_t fb = full_target(st);
+        arm_full(st);
         load_w(smem_u32(tw), fb, sp, nb, e, pol_w);
         load_a(smem_u32(ta), fb, sp, row0, pol_a);
         ++it;
         advance();
       }
       // loads still in flight complete on their full barrier: wait for the last phase
-      // issued on each stage (a bounded wait; the phase completes once its bytes land)
-      const uint32_t issued = it;
+      // issued on each stage (a bounded wait; the phase completes once its bytes land). In
+      // a CTA pair the first CTA waits for both: its phases count the second CTA's bytes,
+      // and the second CTA does not leave before the first (the closing cluster barrier).
+      const uint32_t issued = (kCP && crank != 0) ? 0u : it;
       for (int st = 0; st < S && (uint32_t)st < issued; ++st) {
         const uint32_t last = issued - 1 - ((issued - 1 - st) % S);
         const uint32_t ph = (last / S) & 1;
@@ -349,9 +397,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------- MMA issuer --------------------------------
-    if (lane == 0) {
+    // (CTA pair: the first CTA issues every MMA of the pair; the second only holds TMEM)
+    if (lane == 0 && crank == 0) {
       uint32_t it = 0, kc = 0;
-      constexpr uint32_t idesc = idesc_f8(TT);
+      constexpr uint32_t idesc = idesc_f8(TT, kCP ? 2 * kBM : kBM);
       const int SP = (KB + KBS - 1) / KBS;
       for (int u = u_begin; u < u_end && !s_abort; u += u_step) {
         bool ok = true;
@@ -371,13 +420,24 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
               const uint32_t d = tmem_base + acc * (WB * TT) + b * TT;
               const uint32_t tw_h = tw + SM::w_off(b, h);
 #pragma unroll
-              for (int j = 0; j < kBK / 32; ++j)
-                mma_f8(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+              for (int j = 0; j < kBK / 32; ++j) {
+                if constexpr (kCP)
+                  mma_f8_pair(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+                else
+                  mma_f8(d, smem_desc_sw128(tw_h + 32 * j), smem_desc_sw128(ta_h + 32 * j), idesc, j > 0 ? 1u : 0u);
+              }
             }
-            mma_commit(smem_u32(&tfull[acc]));
+            // (CTA pair: the accumulator of each CTA is full, on each CTA's barrier)
+            if constexpr (kCP)
+              mma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+            else
+              mma_commit(smem_u32(&tfull[acc]));
           }
           if (!ok) break;
-          mma_commit(smem_u32(&empty[st]));
+          if constexpr (kCP)
+            mma_commit_pair(smem_u32(&empty[st]), 0x3);  // both CTAs' stage is free
+          else
+            mma_commit(smem_u32(&empty[st]));
         }
         if (!ok) break;
       }
@@ -512,7 +572,12 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
             // every TMEM read of this accumulator is complete: hand it back to the MMA
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+            if (lane == 0) {
+              if constexpr (kCP)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[ab]), 0));  // the issuing CTA's barrier
+              else
+                mbar_arrive(smem_u32(&tempty[ab]));
+            }
           }
 #pragma unroll
           for (int b = 0; b < WB; ++b) {
@@ -598,11 +663,20 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   }
 
   fence_before();
-  __syncthreads();
+  if constexpr (kCP) {
+    // neither CTA of the pair leaves, or frees TMEM, while the other may still read its
+    // shared memory, signal its barriers or (the MMAs of the first) write its TMEM
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols));
+    if constexpr (kCP)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols));
   }
 }
 
@@ -723,7 +797,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     const uint64_t ws[4] = {(uint64_t)a.k, 128, 128 * (uint64_t)a.k, half * (uint64_t)a.k};
     const uint32_t wb[5] = {128, 128, (uint32_t)KBS, 1, 2};
     if (!encode_u8_tmap(&mw, a.w_q, 5, wd, ws, wb)) return cudaErrorInvalidValue;
-  } else if constexpr (MODE == tc::kPair || KBS > 1) {
+  } else if constexpr (MODE == tc::kPair || MODE == tc::kCtaPair || KBS > 1) {
+    // (the CTA pair's loads are always 4-D: this map at every KBS)
     const uint64_t wd[4] = {128, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
     const uint64_t ws[3] = {(uint64_t)a.k, 128, (uint64_t)a.k * (uint64_t)a.n};
     const uint32_t wb[4] = {128, (uint32_t)(128 * SM::kWB), (uint32_t)KBS, 1};
@@ -735,9 +810,10 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     if (!encode_u8_tmap(&mw, a.w_q, 3, wd, ws, wb)) return cudaErrorInvalidValue;
   }
   if constexpr (MODE != tc::kSingle || KBS > 1) {
+    // (a CTA pair loads half of the token tile in each CTA)
     const uint64_t ad[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
     const uint64_t as[2] = {(uint64_t)a.k, 128};
-    const uint32_t ab[3] = {128, (uint32_t)TT, (uint32_t)KBS};
+    const uint32_t ab[3] = {128, (uint32_t)(MODE == tc::kCtaPair ? TT / 2 : TT), (uint32_t)KBS};
     if (!encode_u8_tmap(&ma, a.a_q, 3, ad, as, ab)) return cudaErrorInvalidValue;
   } else {
     const uint64_t ad[2] = {(uint64_t)a.k, (uint64_t)a.a_rows};
@@ -773,6 +849,23 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
         cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  if constexpr (MODE == tc::kCtaPair) {
+    // as many CTA pairs as can be resident at once (one CTA per SM; a pair needs two SMs
+    // of one cluster-capable group, so this may be a little under half the SMs)
+    static int pairs[64] = {};
+    int np = (dev >= 0 && dev < 64) ? pairs[dev] : 0;
+    if (np == 0) {
+      np = max_active_clusters(tc::tc_gemm_kernel<TT, KBS, MODE>, dim3(W::kThreads), smem, 2, 2 * (sm_count() / 2));
+      if (np > sm_count() / 2) np = sm_count() / 2;
+      if (dev >= 0 && dev < 64) pairs[dev] = np;
+    }
+    if (np < 1) {
+      *unsupported = 1;
+      return cudaSuccess;
+    }
+    return launch_kernel_cluster(tc::tc_gemm_kernel<TT, KBS, MODE>, dim3(2 * np), dim3(W::kThreads), smem, st, true, 2,
+                                 mw, ma, p);
+  }
   return launch_kernel(tc::tc_gemm_kernel<TT, KBS, MODE>, dim3(sm_count()), dim3(W::kThreads), smem, st, true, mw,
                        ma, p);
 }
@@ -798,6 +891,16 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupporte
       a.n > (1 << 30) || a.k > (1 << 30) || a.a_rows > (1 << 30) || a.E > 65535) {
     *unsupported = 1;
     return cudaSuccess;
+  }
+  // a CTA pair: one weight block per CTA, token tile 64 or 128, whole block pairs and K blocks
+  if (a.ctas == 2) {
+    if (a.silu || a.wblocks == 2 || !tc_gemm_pairs_ok(a.n, a.k) || (a.tok_tile != 64 && a.tok_tile != 128)) {
+      *unsupported = 1;
+      return cudaSuccess;
+    }
+    return a.tok_tile == 64
+               ? launch_tt<64, tc::kbs_for(64, tc::kCtaPair), tc::kCtaPair>(a, st, unsupported)
+               : launch_tt<128, tc::kbs_for(128, tc::kCtaPair), tc::kCtaPair>(a, st, unsupported);
   }
   // two weight blocks per unit need whole 256-row block pairs and whole K blocks
   if (a.wblocks == 2 || a.silu) {

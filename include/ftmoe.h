@@ -130,14 +130,20 @@ typedef struct ftmoe_routes {
  * kernel, GROUPED -> the tcgen05 tensor-core kernel), 1 = the streaming kernel,
  * 2 = the tcgen05 kernel. tok_tile: token columns per tensor-core tile, one of
  * 16/32/64/128; 0 = ftmoe_pick_tile's choice. wblocks: 128-row weight blocks per
- * tensor-core unit, sharing one token tile: 1, 2 (adjacent blocks; needs n % 256 == 0 and
- * k % 128 == 0, else the request is treated as unsupported by the tcgen05 kernel), or 0 =
- * automatic (2 at token tile 64 where allowed, else 1). Results do not depend on it. */
+ * tensor-core unit on one SM, sharing one token tile: 1, 2 (adjacent blocks; needs
+ * n % 256 == 0 and k % 128 == 0, else the request is treated as unsupported by the tcgen05
+ * kernel), or 0 = automatic (2 at token tile 64 where allowed, else 1). ctas: SMs per
+ * tensor-core unit: 1, 2 (a CTA pair, a cluster of two CTAs on two SMs: each streams one of
+ * two adjacent weight blocks and loads half of the token tile, one MMA of M = 256 covers
+ * both; needs token tile 64 or 128, n % 256 == 0, k % 128 == 0 and wblocks 0 or 1, else
+ * the request is treated as unsupported by the tcgen05 kernel), or 0 = automatic (2 at token
+ * tile 128 where allowed and wblocks is not 2, else 1). Results do not depend on wblocks or
+ * ctas: every output element is the same sum in the same order. */
 typedef struct ftmoe_tile {
   int32_t tok_tile;
   int32_t variant;
   int32_t wblocks;
-  int32_t reserved;
+  int32_t ctas;
 } ftmoe_tile;
 
 const char* ftmoe_status_string(int status);

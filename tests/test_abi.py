@@ -219,9 +219,10 @@ def test_two_block_and_fused_gemm_host_checks(ft):
     act.rows = 0  # zero rows: OK without a launch
     assert silu(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, fake, ctypes.byref(t),
                 None) == ft.FTMOE_OK
-    # ftmoe_tile.wblocks outside {0, 1, 2} is refused by the GEMM entry points
+    # ftmoe_tile.wblocks outside {0, 1, 2}, ctas outside {0, 1, 2}, and a CTA pair asked for
+    # two weight blocks per CTA are refused by the GEMM entry points
     act.rows = 8
-    bad = ft.Tile(16, 2, 3, 0)
-    for fn in (L.ftmoe_grouped_gemm_gateup, L.ftmoe_grouped_gemm_down):
-        assert fn(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, 512, ctypes.byref(bad),
-                  None) == ft.FTMOE_INVALID_ARG
+    for bad in (ft.Tile(16, 2, 3, 0), ft.Tile(128, 2, 0, 3), ft.Tile(128, 2, 0, -1), ft.Tile(128, 2, 2, 2)):
+        for fn in (L.ftmoe_grouped_gemm_gateup, L.ftmoe_grouped_gemm_down):
+            assert fn(ctypes.byref(act), ctypes.byref(rt), ctypes.byref(bank), fake, 512, ctypes.byref(bad),
+                      None) == ft.FTMOE_INVALID_ARG

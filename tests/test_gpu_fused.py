@@ -1,9 +1,12 @@
-"""Two weight blocks per tensor-core unit, and SiLU-and-mul fused into the gate/up GEMM.
+"""Two weight blocks per tensor-core unit, CTA pairs, and SiLU-and-mul fused into the gate/up
+GEMM.
 
 The tcgen05 grouped GEMM can give each token tile two 128-row weight blocks (adjacent
-blocks of one matrix, or gate block j with up block j). Its per-K-block promotion is the
-same fp32 arithmetic in the same order whichever blocks share a tile, so:
-  - the GEMM with two blocks per unit equals the one-block GEMM bit for bit;
+blocks of one matrix, or gate block j with up block j), on one SM or on the two CTAs of a
+cluster (one M = 256 MMA over both). Its per-K-block promotion is the same fp32 arithmetic
+in the same order whichever blocks share a tile, so:
+  - the GEMM with two blocks per unit, and with CTA pairs, equals the one-block GEMM bit for
+    bit;
   - ftmoe_grouped_gemm_gateup_silu equals ftmoe_grouped_gemm_gateup followed by
     ftmoe_silu_mul bit for bit (codes and scales), and both match the oracle;
   - the forward with the fused gate/up (path 3) equals the forward with the separate
@@ -69,6 +72,60 @@ def test_pair_units_equal_single_units(ft, tok_tile, K):
             ref = M.gemm_rows(adeq[lo:hi], wd)
             scale = np.max(np.abs(ref))
             assert np.all(np.abs(got[lo:hi] - ref) <= 1e-4 * np.abs(ref) + 1e-5 * scale)
+
+
+@pytest.mark.parametrize("tok_tile", [64, 128])
+@pytest.mark.parametrize("K", [384, 1152, 2176])
+@pytest.mark.parametrize("E", [5, 48])
+def test_cta_pair_units_equal_single_units(ft, tok_tile, K, E):
+    # CTA pairs (clusters of two, M = 256): few units (most pairs idle) and more units than
+    # pairs (each pair runs several), experts with 0 and 1 rows, ragged tails, one to three
+    # chunks of activation scales
+    N = 512
+    if E == 5:
+        counts = [0, 1, 17, 140, 3]
+    else:
+        rng = np.random.default_rng(K + tok_tile)
+        counts = [int(c) for c in rng.integers(0, 300, E)]
+        counts[3] = 0
+        counts[7] = 1
+    x, w, aq, as_, wq, ws, offsets = _rows_case(ft, E, N, K, counts, seed=K + tok_tile + E)
+    R = int(offsets[-1])
+    off = torch.from_numpy(offsets).to(DEV)  # kept alive: the routes struct holds its raw pointer
+    act, rt, bank = ft.make_act(aq, as_), ft.grouped_routes(off), ft.make_bank(wq, ws)
+    o1 = torch.full((R + 2, N), float("nan"), device=DEV)
+    o2 = torch.full((R + 2, N), float("nan"), device=DEV)
+    ft.ftmoe_grouped_gemm_down(act, rt, bank, o1, tok_tile=tok_tile, variant=2, wblocks=1, ctas=1)
+    ft.ftmoe_grouped_gemm_down(act, rt, bank, o2, tok_tile=tok_tile, variant=2, ctas=2)
+    torch.cuda.synchronize()
+    assert ft.ftmoe_read_error_flags() == 0
+    assert torch.equal(o1[:R].view(torch.int32), o2[:R].view(torch.int32))
+    assert torch.all(torch.isnan(o2[R:]))  # rows past the segments are not touched
+    rq, rs = M.quantize_act_fp8_fast(x.float().cpu().numpy())
+    adeq = M.dequant_act_fp8(rq, rs)
+    got = o2[:R].cpu().numpy()
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            wd = M.dequant_weight_fp8(*M.quantize_weight_fp8_fast(w[e].cpu().numpy()))
+            ref = M.gemm_rows(adeq[lo:hi], wd)
+            scale = np.max(np.abs(ref))
+            assert np.all(np.abs(got[lo:hi] - ref) <= 1e-4 * np.abs(ref) + 1e-5 * scale)
+
+
+def test_cta_pair_refused_where_it_does_not_apply(ft):
+    # token tiles 16 and 32, and matrices that are not whole 256-row block pairs, are
+    # unsupported for CTA pairs (the tensor-core variant is forced, so nothing falls back)
+    E, N, K = 2, 384, 256
+    counts = [20, 5]
+    x, w, aq, as_, wq, ws, offsets = _rows_case(ft, E, N, K, counts, seed=3)
+    off = torch.from_numpy(offsets).to(DEV)
+    act, rt, bank = ft.make_act(aq, as_), ft.grouped_routes(off), ft.make_bank(wq, ws)
+    o = torch.empty(25, N, device=DEV)
+    for tile in (16, 32, 128):  # N = 384: three blocks, no whole pairs
+        with pytest.raises(ft.FtmoeError) as ei:
+            ft.ftmoe_grouped_gemm_down(act, rt, bank, o, tok_tile=tile, variant=2, ctas=2)
+        assert ei.value.status == ft.FTMOE_UNSUPPORTED
 
 
 @pytest.mark.parametrize("tok_tile", [16, 32, 64, 128])
