@@ -12,6 +12,10 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   moe.quantize_act_fp8 / weight_fp8   pinned: closed forms (a 448 code in every nonzero group,
                                       exact power-of-two scales, round trip of representable values)
   moe.quantize_nvfp4                  pinned: closed forms (exact block/global scales, 6.0 codes)
+  moe.quantize_mxfp8 / mx_shared_exp  pinned: closed forms (shared exponents, exact blocks, the
+                                      clamp to 448, zero and partial blocks), floor(log2) from the
+                                      fp32 bit pattern, torch float8_e4m3fn on the scaled values,
+                                      the error bound, a brute-force MXFP8 FFN per element
   moe.segment_routes                  pinned: brute-force double loop, invariants
   moe.gather_rows_scales              pinned: identity map, duplicate rows, empty map
   moe.gemm_rows / moe_forward         pinned: brute-force dense FFN per token, one-hot columns,

@@ -26,6 +26,12 @@ Everything here is the slow, direct definition of each step:
   (FreeToken page, first section).
 * NVFP4 -- e2m1 codes, one e4m3 scale per 16 elements, one fp32 scale per
   tensor (the two-level recipe; the pages name the format only).
+* MXFP8 -- e4m3 codes with one power-of-two (E8M0) scale per 32 consecutive
+  elements of a row. The SGLang gather page (Modifications) names the format
+  ("mxfp8") and its branch, which gathers a bf16 activation and leaves the
+  quantization to after the gather; the recipe is the OCP Microscaling one:
+  shared exponent floor(log2(amax)) - 8 (8 = the largest exponent of an E4M3
+  normal), clamped to E8M0's [-127, 127], codes e4m3_rne_sat(x / 2^shared).
 
 Readings where the pages are silent are listed in the repository's design
 notes (gate rows first then up rows; fp32 gate/up intermediate re-quantized per
@@ -39,6 +45,9 @@ from .formats import (E2M1_MAX, E4M3_MAX, decode_e2m1, decode_e4m3,
 
 GROUP = 128        # activation group width; weight block edge
 NVFP4_BLOCK = 16   # elements per e4m3 scale in NVFP4
+MX_BLOCK = 32      # elements per E8M0 scale in MXFP8
+E4M3_EMAX = 8      # exponent of E4M3's largest power of two (448 = 1.75 * 2^8)
+E8M0_BIAS = 127
 
 
 def ceil_div(a, b):
@@ -227,6 +236,72 @@ def unpack_e2m1(packed, k):
 
 
 # --------------------------------------------------------------------------
+# MXFP8: e4m3 codes, one E8M0 (power-of-two) scale per 32 elements of a row
+# --------------------------------------------------------------------------
+
+def mx_shared_exp(amax):
+    """floor(log2(amax)) - 8, clamped to [-127, 127]; amax == 0 gives -127.
+
+    amax is a float32 magnitude. frexp gives amax = m * 2^e with m in [0.5, 1), so
+    floor(log2(amax)) = e - 1 exactly (no floating-point logarithm is taken).
+    """
+    a = float(np.float32(amax))
+    if a == 0.0:
+        return -E8M0_BIAS
+    _, e = np.frexp(a)
+    return int(min(E8M0_BIAS, max(-E8M0_BIAS, (int(e) - 1) - E4M3_EMAX)))
+
+
+def quantize_mxfp8(x):
+    """MXFP8 quantization of a [rows, k] float32 tensor along its rows.
+
+    Per 32 consecutive elements of a row (a partial last block takes its amax over its
+    valid elements): shared = mx_shared_exp(amax), scale byte = shared + 127, codes
+    e4m3_rne_sat(x / 2^shared). Dividing by a power of two is exact here (the quotient's
+    magnitude is below 512 and far above E4M3's smallest step), so the codes follow from
+    the inputs alone. Returns (codes uint8 [rows, k], scale bytes uint8 [rows, ceil(k/32)]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    rows, k = x.shape
+    nblk = ceil_div(k, MX_BLOCK)
+    q = np.zeros((rows, k), np.uint8)
+    sb = np.zeros((rows, nblk), np.uint8)
+    for b in range(nblk):
+        sl = slice(b * MX_BLOCK, min(k, (b + 1) * MX_BLOCK))
+        blk = x[:, sl].astype(np.float64)
+        amax = np.max(np.abs(blk), axis=1)
+        for r in range(rows):
+            e = mx_shared_exp(amax[r])
+            sb[r, b] = e + E8M0_BIAS
+            q[r, sl] = encode_e4m3(blk[r] * np.ldexp(1.0, -e))
+    return q, sb
+
+
+def quantize_mxfp8_fast(x):
+    """Same result as quantize_mxfp8, vectorised over rows and blocks (for large inputs)."""
+    x = np.asarray(x, dtype=np.float32)
+    rows, k = x.shape
+    nblk = ceil_div(k, MX_BLOCK)
+    pad = np.zeros((rows, nblk * MX_BLOCK), np.float64)
+    pad[:, :k] = x
+    blk = pad.reshape(rows, nblk, MX_BLOCK)
+    amax = np.max(np.abs(blk), axis=2)  # padding zeros never win
+    _, e = np.frexp(amax)
+    shared = np.clip(e.astype(np.int64) - 1 - E4M3_EMAX, -E8M0_BIAS, E8M0_BIAS)
+    shared = np.where(amax == 0, -E8M0_BIAS, shared)
+    q = encode_e4m3(blk * np.ldexp(1.0, -shared)[:, :, None])
+    return q.reshape(rows, nblk * MX_BLOCK)[:, :k].copy(), (shared + E8M0_BIAS).astype(np.uint8)
+
+
+def dequant_mxfp8(q, sb):
+    """codes [rows, k] + E8M0 scale bytes [rows, ceil(k/32)] -> float64 [rows, k]."""
+    q = np.asarray(q)
+    k = q.shape[1]
+    scale = np.ldexp(1.0, np.asarray(sb, np.int64) - E8M0_BIAS)
+    return decode_e4m3(q) * np.repeat(scale, MX_BLOCK, axis=1)[:, :k]
+
+
+# --------------------------------------------------------------------------
 # routing: segmenter, gather, combine
 # --------------------------------------------------------------------------
 
@@ -323,6 +398,7 @@ class Bank:
     fmt 'fp8': q [E, n, k] uint8, s [E, ceil(n/128), ceil(k/128)] float32.
     fmt 'nvfp4': q [E, n, k] codes 0..15 (unpacked), sb [E, n, ceil(k/16)] e4m3
     codes, g [E] float32.
+    fmt 'mxfp8': q [E, n, k] uint8, s [E, n, ceil(k/32)] E8M0 scale bytes.
     """
 
     def __init__(self, fmt, q, s, g=None):
@@ -332,6 +408,8 @@ class Bank:
     def dequant(self, e):
         if self.fmt == "fp8":
             return dequant_weight_fp8(self.q[e], self.s[e])
+        if self.fmt == "mxfp8":
+            return dequant_mxfp8(self.q[e], self.s[e])
         return dequant_nvfp4(self.q[e], self.s[e], self.g[e])
 
 
@@ -351,6 +429,8 @@ class LazyBank:
             w = np.asarray(self.raw(e), np.float32)
             if self.fmt == "fp8":
                 self._cache[e] = quantize_weight_fp8_fast(w)
+            elif self.fmt == "mxfp8":
+                self._cache[e] = quantize_mxfp8_fast(w)
             else:
                 self._cache[e] = quantize_nvfp4(w)
         return self._cache[e]
@@ -359,6 +439,8 @@ class LazyBank:
         p = self.parts(e)
         if self.fmt == "fp8":
             return dequant_weight_fp8(*p)
+        if self.fmt == "mxfp8":
+            return dequant_mxfp8(*p)
         return dequant_nvfp4(*p)
 
 
@@ -368,6 +450,9 @@ def quantize_bank(weights_fp32, fmt="fp8"):
     if fmt == "fp8":
         qs = [quantize_weight_fp8(w[e]) for e in range(w.shape[0])]
         return Bank("fp8", np.stack([a for a, _ in qs]), np.stack([b for _, b in qs]))
+    if fmt == "mxfp8":
+        qs = [quantize_mxfp8(w[e]) for e in range(w.shape[0])]
+        return Bank("mxfp8", np.stack([a for a, _ in qs]), np.stack([b for _, b in qs]))
     qs = [quantize_nvfp4(w[e]) for e in range(w.shape[0])]
     return Bank("nvfp4", np.stack([a for a, _, _ in qs]), np.stack([b for _, b, _ in qs]),
                 np.array([c for _, _, c in qs], np.float32))
@@ -378,6 +463,9 @@ def quantize_acts(x, fmt, global_amax=None):
     if fmt == "fp8":
         q, s = quantize_act_fp8_fast(x)
         return dequant_act_fp8(q, s), (q, s)
+    if fmt == "mxfp8":
+        q, sb = quantize_mxfp8_fast(x)
+        return dequant_mxfp8(q, sb), (q, sb)
     q, sb, g = quantize_nvfp4(x, global_amax)
     return dequant_nvfp4(q, sb, g), (q, sb, g)
 
@@ -387,7 +475,7 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
 
     x [T, H] float32 (exact bf16 values); expert_ids [T, topk] (negative = inactive);
     weights [T, topk] float32; banks: gate/up [E, 2I, H] (gate rows first), down [E, H, I].
-    Steps: quantize x per 1x128 (or NVFP4) -> for each active route: gate/up GEMM in
+    Steps: quantize x per 1x128 (or NVFP4, or MXFP8) -> for each active route: gate/up GEMM in
     float64 -> silu(g)*u -> re-quantize that intermediate (the down GEMM's FP8/FP4
     operand) -> down GEMM in float64 -> routing-weighted combine.
     The grouping (segment + gather) only reorders rows and changes no value, so the
