@@ -77,6 +77,11 @@ WORKLOADS = {
     "prefill-nvfp4-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
     "prefill-nvfp4-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
     "prefill-nvfp4-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
+    # MXFP8 (e4m3 codes, one E8M0 scale per 32 elements; the bf16 activation is gathered and
+    # quantized after the gather): the prefill geometry
+    "prefill-mxfp8-h7168-i2048-e256-r6144": (1024, 7168, 2048, 256, 6, 6, 2),
+    "prefill-mxfp8-h7168-i2048-e256-r24576": (4096, 7168, 2048, 256, 6, 6, 2),
+    "prefill-mxfp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 2),
 }
 DEFAULT_WORKLOAD = "prefill-fp8-h7168-i2048-e256-r24576"
 
@@ -113,16 +118,18 @@ def vs_pages(workload, value_us):
 
 
 def workload_format(name):
-    return "nvfp4" if "-nvfp4-" in name else "fp8"
+    return "nvfp4" if "-nvfp4-" in name else ("mxfp8" if "-mxfp8-" in name else "fp8")
 
 
 def code_bytes(fmt, n):
     """Bytes of one quantized row of n elements."""
-    return n if fmt == "fp8" else n // 2
+    return n // 2 if fmt == "nvfp4" else n
 
 
 def scale_bytes(fmt, n):
     """Bytes of the scales of one quantized activation row of n elements."""
+    if fmt == "mxfp8":
+        return n // 32
     return 4 * (-(-n // 128)) if fmt == "fp8" else n // 16
 
 
@@ -130,6 +137,8 @@ def weight_bytes(fmt, n, k):
     """Bytes of one expert matrix [n, k] with its scales."""
     if fmt == "fp8":
         return n * k + 4 * (-(-n // 128)) * (-(-k // 128))
+    if fmt == "mxfp8":
+        return n * k + n * k // 32
     return n * k // 2 + n * k // 16 + 4
 
 
@@ -356,12 +365,16 @@ class MoeWorkload:
         if T >= 256:
             self.NSETS = 2
         self.fmt = workload_format(name)
-        self.ft_fmt = ft.FMT_FP8 if self.fmt == "fp8" else ft.FMT_NVFP4
+        self.ft_fmt = {"fp8": ft.FMT_FP8, "nvfp4": ft.FMT_NVFP4, "mxfp8": ft.FMT_MXFP8}[self.fmt]
         banks = []
         for n, kk, tag in ((2 * I, H, "gateup"), (H, I, "down")):
             if self.fmt == "fp8":
                 q = torch.empty(E, n, kk, dtype=torch.uint8, device=device)
                 sc = torch.empty(E, -(-n // 128), -(-kk // 128), dtype=torch.float32, device=device)
+                gsc = None
+            elif self.fmt == "mxfp8":
+                q = torch.empty(E, n, kk, dtype=torch.uint8, device=device)
+                sc = torch.empty(E, n, kk // 32, dtype=torch.uint8, device=device)
                 gsc = None
             else:
                 q = torch.empty(E, n, kk // 2, dtype=torch.uint8, device=device)
@@ -398,9 +411,9 @@ class MoeWorkload:
         # kernels per forward: quantize, [segment, gather,] gate/up, SiLU-and-mul, down, combine;
         # FP8 on the grouped path quantizes and segments in one launch, and the fused path has
         # no SiLU-and-mul launch; each NVFP4 quantizer adds an amax pass and the tensor-scale
-        # conversion
+        # conversion; MXFP8 quantizes inside the gather (no quantizing launch)
         self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) -
-                                  (1 if self.grouped and self.fmt == "fp8" else 0) +
+                                  (1 if self.grouped and self.fmt in ("fp8", "mxfp8") else 0) +
                                   (4 if self.fmt == "nvfp4" else 0))
         if self.decode:
             self.launches_per_step = 2  # quantize, then the fused kernel
@@ -436,14 +449,19 @@ class MoeWorkload:
             gateup = uniq * w_gu + (ra if self.grouped else T) * row(H) + out_rows * 2 * I * 4
             silu = out_rows * 2 * I * 4 + out_rows * row(I)
         down = uniq * w_dn + out_rows * row(I) + out_rows * H * 4
-        total = (T * H * 2 + T * row(H)                            # quantize
-                 + gateup + silu
+        total = (gateup + silu
                  + down
                  + ra * H * 4 + T * k * 8 + T * H * 2)             # combine
         if f == "nvfp4":
             total += T * H * 2 + out_rows * 2 * I * 4              # amax passes of the tensor scales
-        if self.grouped:
-            total += T * k * 4 * 3 + ra * row(H) * 2               # segment + gather
+        if f == "mxfp8":
+            # segment, then the gather reads each bf16 token row once and writes the quantized
+            # rows of the active routes
+            total += T * k * 4 * 3 + T * H * 2 + ra * row(H)
+        else:
+            total += T * H * 2 + T * row(H)                        # quantize
+            if self.grouped:
+                total += T * k * 4 * 3 + ra * row(H) * 2           # segment + gather
         flops = 2 * ra * (2 * I * H + H * I)
         return dict(bytes=total, gateup_bytes=gateup, flops=flops, gateup_flops=2 * ra * 2 * I * H,
                     uniq=uniq, active=ra)
@@ -482,6 +500,9 @@ class MoeWorkload:
         tile = ft.ftmoe_pick_tile(R, self.E)
         if f == "fp8":
             act, kname = ft.make_act(rq, rs), f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)"
+        elif f == "mxfp8":
+            act = ft.make_act(rq, rs, fmt=ft.FMT_MXFP8)
+            kname = f"mxfp8_gemm_kernel<{tile}> (gate/up, grouped, tcgen05 block-scaled)"
         else:
             xg = self.ws[lay["x_gscale"]:lay["x_gscale"] + 4].view(torch.float32)
             act = ft.make_act(rq, rs, xg, fmt=ft.FMT_NVFP4)
@@ -617,8 +638,8 @@ def run_gpu(args, rank, world, local):
     gu_flops_avg = float(np.mean([w["gateup_flops"] for w in works]))
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
     # dense FP8 = 2x bf16 and dense FP4 = 6x bf16 (nominal ratios 4.5 / 2.25 and 13.5 / 2.25)
-    mma_peak = (2.0 if wl.fmt == "fp8" else 6.0) * bf16_peak
-    mma_name = "fp8" if wl.fmt == "fp8" else "fp4"
+    mma_peak = (6.0 if wl.fmt == "nvfp4" else 2.0) * bf16_peak
+    mma_name = "fp4" if wl.fmt == "nvfp4" else "fp8"
 
     # dominant kernel alone (gate/up GEMM), captured in a graph so that host-side launch
     # preparation stays out of the timed region; timed by event nodes inside that graph
@@ -685,8 +706,9 @@ def run_gpu(args, rank, world, local):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": vs_pages(wl.name, value),
-        "dtype": ("fp8-e4m3 (fp32 accumulate)" if wl.fmt == "fp8" else
-                  "nvfp4-e2m1 with e4m3 block scales (fp32 accumulate)"),
+        "dtype": {"fp8": "fp8-e4m3 (fp32 accumulate)",
+                  "mxfp8": "mxfp8-e4m3 with E8M0 scales per 32 (fp32 accumulate)",
+                  "nvfp4": "nvfp4-e2m1 with e4m3 block scales (fp32 accumulate)"}[wl.fmt],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantized by libftmoe)",
         "config": {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "inter": wl.I, "experts": wl.E,
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
@@ -866,8 +888,8 @@ def _oracle_token(M, x, ids, w, bg, bd, fmt, t):
     """The numpy oracle's forward for token t alone. FP8 quantizes per token, so one token of
     the call is exact; the NVFP4 tensor scales span the whole call, so there the token is run
     as a call of its own (the same work per token)."""
-    if fmt == "fp8":
-        M.moe_forward(x, ids, w, bg, bd, tokens_subset=[t])
+    if fmt in ("fp8", "mxfp8"):  # scales per row: one token of the call is exact
+        M.moe_forward(x, ids, w, bg, bd, fmt=fmt, tokens_subset=[t])
     else:
         M.moe_forward(x[t:t + 1], ids[t:t + 1], w[t:t + 1], bg, bd, fmt="nvfp4")
 
@@ -881,6 +903,8 @@ def _cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=0xF7E00002):
     import concurrent.futures
     from oracle import cpu as C
     C.lib()  # raises if the C++ oracle cannot be built or loaded
+    if fmt == "mxfp8":
+        raise RuntimeError("the C++ oracle has no MXFP8 path")
     remap = np.full(max(used) + 1 if used else 1, -1, np.int32)
     remap[used] = np.arange(len(used), dtype=np.int32)
     ids_c = np.where(ids >= 0, remap[np.maximum(ids, 0)], -1).astype(np.int32)

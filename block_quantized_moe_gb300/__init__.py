@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 
 FTMOE_OK, FTMOE_INVALID_ARG, FTMOE_UNSUPPORTED, FTMOE_CUDA_ERROR, FTMOE_WORKSPACE_TOO_SMALL, FTMOE_CHECK_FAILED = range(6)
-FMT_FP8, FMT_NVFP4 = 0, 1
+FMT_FP8, FMT_NVFP4, FMT_MXFP8 = 0, 1, 2
 ROUTES_GROUPED, ROUTES_SLOTS = 0, 1
 ERR_EXPERT_ID_RANGE, ERR_MAP_RANGE, ERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 OUT_BF16, OUT_FP16, OUT_FP32 = 0, 1, 2
@@ -79,6 +79,8 @@ _SIGNATURES = [
     ("ftmoe_segment_routes", c_i32, [c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     ("ftmoe_gather_rows_scales", c_i32, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_ptr, c_i64, c_ptr,
                                          c_ptr, c_ptr, c_ptr]),
+    ("ftmoe_gather_quantize_act", c_i32, [c_ptr, c_i64, c_i64, c_i64, c_ptr, c_i64, c_ptr, c_i32, c_ptr, c_ptr,
+                                          c_ptr]),
     ("ftmoe_grouped_gemm_gateup", c_i32, [ctypes.POINTER(Act), ctypes.POINTER(Routes),
                                           ctypes.POINTER(ExpertBank), c_ptr, c_i64,
                                           ctypes.POINTER(Tile), c_ptr]),
@@ -186,16 +188,24 @@ def ftmoe_gather_rows_scales(src, src_scales, dst2src, dst, dst_scales, n_dst=No
         _p(dst), _p(dst_scales), _stream(stream)))
 
 
+def ftmoe_gather_quantize_act(x, dst2src, q, scales, fmt=FMT_MXFP8, n_dst=None, n_dst_dev=None, stream=None):
+    """bf16 rows x[dst2src[d]] quantized into q [n_dst, k] and scales (MXFP8: [n_dst, k/32])."""
+    n_src, k = x.shape
+    n_dst = dst2src.shape[0] if n_dst is None else n_dst
+    _check("ftmoe_gather_quantize_act", lib().ftmoe_gather_quantize_act(
+        _p(x), n_src, k, x.stride(0), _p(dst2src), n_dst, _p(n_dst_dev), fmt, _p(q), _p(scales), _stream(stream)))
+
+
 def make_bank(q, scales, global_scale=None, fmt=FMT_FP8):
     """ExpertBank view of tensors q [E, n, k(/2)], scales, global_scale."""
     E, n, kk = q.shape
-    k = kk if fmt == FMT_FP8 else 2 * kk
+    k = 2 * kk if fmt == FMT_NVFP4 else kk
     return ExpertBank(fmt, E, n, k, _p(q), _p(scales), _p(global_scale))
 
 
 def make_act(q, scales, global_scale=None, fmt=FMT_FP8):
     rows, kk = q.shape
-    k = kk if fmt == FMT_FP8 else 2 * kk
+    k = 2 * kk if fmt == FMT_NVFP4 else kk
     return Act(fmt, 0, rows, k, _p(q), _p(scales), _p(global_scale))
 
 
@@ -333,6 +343,11 @@ def quantize_act(x, fmt=FMT_FP8, stream=None):
         s = torch.empty(rows, cdiv(k, 128), dtype=torch.float32, device=dev)
         ftmoe_quantize_act(x, q, s, None, fmt, stream=stream)
         return q, s, None
+    if fmt == FMT_MXFP8:
+        q = torch.empty(rows, k, dtype=torch.uint8, device=dev)
+        s = torch.empty(rows, k // 32, dtype=torch.uint8, device=dev)
+        ftmoe_quantize_act(x, q, s, None, fmt, stream=stream)
+        return q, s, None
     q = torch.empty(rows, k // 2, dtype=torch.uint8, device=dev)
     s = torch.empty(rows, k // 16, dtype=torch.uint8, device=dev)
     g = torch.empty(1, dtype=torch.float32, device=dev)
@@ -347,6 +362,11 @@ def quantize_weights(w, fmt=FMT_FP8, stream=None):
     if fmt == FMT_FP8:
         q = torch.empty(E, n, k, dtype=torch.uint8, device=dev)
         s = torch.empty(E, cdiv(n, 128), cdiv(k, 128), dtype=torch.float32, device=dev)
+        ftmoe_quantize_weights(w, q, s, None, fmt, stream=stream)
+        return q, s, None
+    if fmt == FMT_MXFP8:
+        q = torch.empty(E, n, k, dtype=torch.uint8, device=dev)
+        s = torch.empty(E, n, k // 32, dtype=torch.uint8, device=dev)
         ftmoe_quantize_weights(w, q, s, None, fmt, stream=stream)
         return q, s, None
     q = torch.empty(E, n, k // 2, dtype=torch.uint8, device=dev)

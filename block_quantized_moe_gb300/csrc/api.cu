@@ -29,12 +29,13 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 inline ftmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FTMOE_OK : FTMOE_CUDA_ERROR; }
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-bool valid_format(int32_t f) { return f == FTMOE_FMT_FP8 || f == FTMOE_FMT_NVFP4; }
+bool valid_format(int32_t f) { return f == FTMOE_FMT_FP8 || f == FTMOE_FMT_NVFP4 || f == FTMOE_FMT_MXFP8; }
 bool valid_out_dtype(int32_t d) { return d == FTMOE_OUT_BF16 || d == FTMOE_OUT_FP16 || d == FTMOE_OUT_FP32; }
 
 // bytes of one quantized row of k elements and of its scale row
-size_t code_row_bytes(int32_t fmt, int64_t k) { return fmt == FTMOE_FMT_FP8 ? (size_t)k : (size_t)(k / 2); }
+size_t code_row_bytes(int32_t fmt, int64_t k) { return fmt == FTMOE_FMT_NVFP4 ? (size_t)(k / 2) : (size_t)k; }
 size_t scale_row_bytes(int32_t fmt, int64_t k) {
+  if (fmt == FTMOE_FMT_MXFP8) return (size_t)(k / kMxBlock);
   return fmt == FTMOE_FMT_FP8 ? (size_t)cdiv(k, kGroup) * 4 : (size_t)(k / kNvfp4Block);
 }
 
@@ -66,7 +67,36 @@ ftmoe_status check_bank(const ftmoe_expert_bank* w) {
   if (!w || !w->q || !w->scales) return FTMOE_INVALID_ARG;
   if (w->num_experts <= 0 || w->n <= 0 || w->k <= 0 || !valid_format(w->format)) return FTMOE_INVALID_ARG;
   if (w->format == FTMOE_FMT_NVFP4 && (!w->global_scale || w->k % 32 != 0)) return FTMOE_INVALID_ARG;
+  if (w->format == FTMOE_FMT_MXFP8 && w->k % kMxBlock != 0) return FTMOE_INVALID_ARG;
   return FTMOE_OK;
+}
+
+// MXFP8: the grouped layout on the block-scaled tensor-core kernel only. Scale rows of k/32
+// bytes are read by TMA in 16-byte boxes, so k % 512 == 0.
+ftmoe_status grouped_gemm_mxfp8(const ftmoe_act* a, const ftmoe_routes* routes, const ftmoe_expert_bank* w,
+                                float* out, int64_t ld_out, const ftmoe_tile* tile, int variant, void* stream) {
+  if (routes->kind == FTMOE_ROUTES_SLOTS) return FTMOE_UNSUPPORTED;
+  if (routes->kind != FTMOE_ROUTES_GROUPED || !routes->offsets) return FTMOE_INVALID_ARG;
+  if (a->rows == 0) return FTMOE_OK;
+  if (variant == 1) return FTMOE_UNSUPPORTED;
+  MxGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a_q = a->q;
+  g.a_sf = static_cast<const uint8_t*>(a->scales);
+  g.a_rows = a->rows;
+  g.w_q = w->q;
+  g.w_sf = static_cast<const uint8_t*>(w->scales);
+  g.out = out;
+  g.ld_out = ld_out;
+  g.n = w->n;
+  g.k = w->k;
+  g.E = w->num_experts;
+  g.offsets = routes->offsets;
+  g.tok_tile = (tile && tile->tok_tile) ? tile->tok_tile : pick_tile_value(a->rows, w->num_experts);
+  int unsupported = 0;
+  cudaError_t e = launch_mxfp8_gemm(g, as_stream(stream), &unsupported);
+  if (unsupported) return FTMOE_UNSUPPORTED;
+  return from_cuda(e);
 }
 
 // NVFP4: the grouped layout on the block-scaled tensor-core kernel only (no streaming
@@ -116,6 +146,7 @@ ftmoe_status grouped_gemm(const ftmoe_act* a, const ftmoe_routes* routes, const 
   if (tile && (tile->ctas < 0 || tile->ctas > 2 || (tile->ctas == 2 && tile->wblocks == 2))) return FTMOE_INVALID_ARG;
   const int variant = tile ? tile->variant : 0;
   if (w->format == FTMOE_FMT_NVFP4) return grouped_gemm_nvfp4(a, routes, w, out, ld_out, tile, variant, stream);
+  if (w->format == FTMOE_FMT_MXFP8) return grouped_gemm_mxfp8(a, routes, w, out, ld_out, tile, variant, stream);
   // both GEMM kernels read K-contiguous rows through TMA: 16-byte aligned rows
   if (w->k % 16 != 0 || (uintptr_t)w->q % 16 != 0 || (a->rows > 0 && (uintptr_t)a->q % 16 != 0))
     return FTMOE_UNSUPPORTED;
@@ -243,7 +274,7 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
     return FTMOE_INVALID_ARG;
   if (s->tok_tile != 0 && s->tok_tile != 16 && s->tok_tile != 32 && s->tok_tile != 64 && s->tok_tile != 128)
     return FTMOE_INVALID_ARG;
-  if (s->format == FTMOE_FMT_NVFP4 && (s->hidden % 32 != 0 || s->inter % 32 != 0)) return FTMOE_INVALID_ARG;
+  if (s->format != FTMOE_FMT_FP8 && (s->hidden % 32 != 0 || s->inter % 32 != 0)) return FTMOE_INVALID_ARG;
   return FTMOE_OK;
 }
 
@@ -319,8 +350,9 @@ Layout make_layout(const ftmoe_moe_shape* s) {
   }
   L.grouped = use_grouped(s);
   L.fused = L.grouped && use_fused(s);
-  L.l.x_q = take(T * code_row_bytes(f, H));
-  L.l.x_scales = take(T * scale_row_bytes(f, H));
+  // (MXFP8 quantizes the gathered rows: no quantized token rows)
+  L.l.x_q = take(f == FTMOE_FMT_MXFP8 ? 0 : T * code_row_bytes(f, H));
+  L.l.x_scales = take(f == FTMOE_FMT_MXFP8 ? 0 : T * scale_row_bytes(f, H));
   L.l.x_gscale = take(16);
   if (L.grouped) {
     L.l.counts = take(E * 4);
@@ -377,6 +409,11 @@ ftmoe_status ftmoe_quantize_act(const uint16_t* x, int64_t rows, int64_t k, int6
   if (format == FTMOE_FMT_FP8)
     return from_cuda(launch_quantize_act_fp8(x, rows, k, ld_x, q, static_cast<float*>(scales),
                                              as_stream(stream)));
+  if (format == FTMOE_FMT_MXFP8) {
+    if (global_scale || k % kMxBlock != 0) return FTMOE_INVALID_ARG;
+    return from_cuda(launch_mxfp8_quant_bf16(x, rows, k, ld_x, nullptr, rows, nullptr, q,
+                                             static_cast<uint8_t*>(scales), as_stream(stream)));
+  }
   if (!global_scale || k % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
   return from_cuda(launch_quantize_act_nvfp4(x, rows, k, ld_x, q, static_cast<uint8_t*>(scales),
                                              global_scale, as_stream(stream)));
@@ -391,6 +428,11 @@ ftmoe_status ftmoe_quantize_weights(const float* w, int32_t num_experts, int64_t
   if (format == FTMOE_FMT_FP8)
     return from_cuda(launch_quantize_weights_fp8(w, num_experts, n, k, q, static_cast<float*>(scales),
                                                  as_stream(stream)));
+  if (format == FTMOE_FMT_MXFP8) {
+    if (global_scale || k % kMxBlock != 0) return FTMOE_INVALID_ARG;
+    return from_cuda(launch_mxfp8_quant_f32(w, (int64_t)num_experts * n, k, k, q, static_cast<uint8_t*>(scales),
+                                            as_stream(stream)));
+  }
   if (!global_scale || k % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
   return from_cuda(launch_quantize_weights_nvfp4(w, num_experts, n, k, q, static_cast<uint8_t*>(scales),
                                                  global_scale, as_stream(stream)));
@@ -421,6 +463,18 @@ ftmoe_status ftmoe_gather_rows_scales(const uint8_t* src, const void* src_scales
                                  static_cast<uint8_t*>(dst_scales), as_stream(stream)));
 }
 
+ftmoe_status ftmoe_gather_quantize_act(const uint16_t* x, int64_t n_src, int64_t k, int64_t ld_x,
+                                       const int32_t* dst2src, int64_t n_dst, const int32_t* n_dst_dev,
+                                       int32_t format, uint8_t* q, void* scales, void* stream) {
+  if (n_dst < 0 || n_src < 0 || k <= 0 || ld_x < k || !valid_format(format)) return FTMOE_INVALID_ARG;
+  if (format != FTMOE_FMT_MXFP8) return FTMOE_UNSUPPORTED;
+  if (k % kMxBlock != 0) return FTMOE_INVALID_ARG;
+  if (n_dst == 0) return FTMOE_OK;
+  if (!x || !dst2src || !q || !scales) return FTMOE_INVALID_ARG;
+  return from_cuda(launch_mxfp8_quant_bf16(x, n_dst, k, ld_x, dst2src, n_src, n_dst_dev, q,
+                                           static_cast<uint8_t*>(scales), as_stream(stream)));
+}
+
 ftmoe_status ftmoe_grouped_gemm_gateup(const ftmoe_act* a, const ftmoe_routes* routes,
                                        const ftmoe_expert_bank* w, float* out, int64_t ld_out,
                                        const ftmoe_tile* tile, void* stream) {
@@ -448,6 +502,11 @@ ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_
   if (format == FTMOE_FMT_FP8)
     return from_cuda(launch_silu_mul_fp8(gu, rows, inter, ld_gu, rows_dev, q,
                                          static_cast<float*>(scales), as_stream(stream)));
+  if (format == FTMOE_FMT_MXFP8) {
+    if (global_scale || inter % kMxBlock != 0) return FTMOE_INVALID_ARG;
+    return from_cuda(launch_silu_mul_mxfp8(gu, rows, inter, ld_gu, rows_dev, q, static_cast<uint8_t*>(scales),
+                                           as_stream(stream)));
+  }
   if (!global_scale || inter % 32 != 0 || (uintptr_t)q % 8 != 0) return FTMOE_INVALID_ARG;
   return from_cuda(launch_silu_mul_nvfp4(gu, rows, inter, ld_gu, rows_dev, q,
                                          static_cast<uint8_t*>(scales), global_scale,
@@ -502,7 +561,8 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   const Layout L = make_layout(s);
   if (!workspace) return FTMOE_INVALID_ARG;
   if (workspace_bytes < L.l.total) return FTMOE_WORKSPACE_TOO_SMALL;
-  if (f == FTMOE_FMT_NVFP4 && !L.grouped) return FTMOE_UNSUPPORTED;  // no route-slot kernel for e2m1
+  // no route-slot kernel for e2m1 codes or E8M0-scaled rows; no fused gate/up + SiLU for them
+  if (f != FTMOE_FMT_FP8 && (!L.grouped || L.fused)) return FTMOE_UNSUPPORTED;
   if (s->path == 4 && !L.decode) return FTMOE_UNSUPPORTED;           // outside the fused decode limits
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -564,9 +624,15 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
     if (unsupported) return FTMOE_UNSUPPORTED;
     return from_cuda(e);
   }
+  // MXFP8 gathers the bf16 activation and quantizes the gathered rows (the SGLang gather
+  // page's mxfp8 branch): its first launch is the segmenter
+  const bool mx = f == FTMOE_FMT_MXFP8;
   if (prep)
     st = from_cuda(launch_prep_fp8(args->x, T, H, args->ld_x, xq, static_cast<float*>(xs), args->expert_ids, R,
                                    s->topk, (int32_t)E, counts, offsets, dst2src, route2dst, strm));
+  else if (mx)
+    st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src, route2dst,
+                              stream);
   else
     st = ftmoe_quantize_act(args->x, T, H, args->ld_x, f, xq, xs, xg, stream);
   if (st != FTMOE_OK) return st;
@@ -591,13 +657,16 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   }
   uint8_t* rq = ws + L.l.rows_q;
   void* rs = ws + L.l.rows_scales;
-  if (!prep) {
+  if (!prep && !mx) {
     st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src,
                               route2dst, stream);
     if (st != FTMOE_OK) return st;
   }
-  st = ftmoe_gather_rows_scales(xq, xs, T, (int64_t)code_row_bytes(f, H), (int64_t)scale_row_bytes(f, H), dst2src, R,
-                                offsets + E, rq, rs, stream);
+  if (mx)
+    st = ftmoe_gather_quantize_act(args->x, T, H, args->ld_x, dst2src, R, offsets + E, f, rq, rs, stream);
+  else
+    st = ftmoe_gather_rows_scales(xq, xs, T, (int64_t)code_row_bytes(f, H), (int64_t)scale_row_bytes(f, H), dst2src,
+                                  R, offsets + E, rq, rs, stream);
   if (st != FTMOE_OK) return st;
   ftmoe_routes rt;
   memset(&rt, 0, sizeof(rt));
@@ -624,7 +693,7 @@ ftmoe_status ftmoe_read_error_flags(uint32_t* flags) {
   if (cudaDeviceSynchronize() != cudaSuccess) return FTMOE_CUDA_ERROR;
   *flags = read_err_quant() | read_err_segment() | read_err_gather() | read_err_stream_gemm() |
            read_err_tc_gemm() | read_err_nvfp4() | read_err_act() | read_err_selftest() | read_err_decode() |
-           read_err_slots();
+           read_err_slots() | read_err_mxfp8() | read_err_tc_mxfp8();
   return FTMOE_OK;
 }
 

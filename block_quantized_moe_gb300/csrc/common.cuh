@@ -15,6 +15,7 @@ constexpr int kGroup = 128;        // activation group width = weight block edge
 constexpr float kE4M3Max = 448.0f;
 constexpr float kE2M1Max = 6.0f;
 constexpr int kNvfp4Block = 16;
+constexpr int kMxBlock = 32;    // elements per E8M0 scale (MXFP8)
 
 // Each translation unit keeps its own device error word; the host reads all of them.
 // An index read on the device that is out of range is skipped and reported here.

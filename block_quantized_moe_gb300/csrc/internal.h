@@ -196,6 +196,35 @@ struct NvGemmArgs {
 cudaError_t launch_nvfp4_gemm(const NvGemmArgs& a, cudaStream_t s, int* unsupported);
 uint32_t read_err_nvfp4();
 
+// tc_mxfp8.cu: block-scaled MXFP8 grouped GEMM (kind::mxf8f6f4)
+struct MxGemmArgs {
+  const uint8_t* a_q;       // e4m3 codes [a_rows][k]
+  const uint8_t* a_sf;      // E8M0 scale bytes [a_rows][k/32]
+  int64_t a_rows;
+  const uint8_t* w_q;       // [E][n][k]
+  const uint8_t* w_sf;      // [E][n][k/32]
+  float* out;
+  int64_t ld_out;
+  int64_t n, k;
+  int32_t E;
+  const int32_t* offsets;
+  int32_t tok_tile;
+};
+cudaError_t launch_mxfp8_gemm(const MxGemmArgs& a, cudaStream_t s, int* unsupported);
+uint32_t read_err_tc_mxfp8();
+
+// mxfp8.cu: MXFP8 quantization (E8M0 scale per 32 elements of a row, k % 32 == 0)
+// bf16 rows [rows][k] (stride ld_x); with map, destination row d reads source row map[d]
+// (entries outside [0, n_src) raise FTMOE_ERR_MAP_RANGE and leave the row untouched);
+// n_dev: optional device count of destination rows to write
+cudaError_t launch_mxfp8_quant_bf16(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x, const int32_t* map,
+                                    int64_t n_src, const int32_t* n_dev, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_mxfp8_quant_f32(const float* x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* q, uint8_t* s,
+                                   cudaStream_t st);
+cudaError_t launch_silu_mul_mxfp8(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu, const int32_t* rows_dev,
+                                  uint8_t* q, uint8_t* s, cudaStream_t st);
+uint32_t read_err_mxfp8();
+
 // act.cu: silu_mul and combine
 cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
                                 const int32_t* rows_dev, uint8_t* q, float* scales,

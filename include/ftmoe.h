@@ -61,7 +61,13 @@ typedef enum ftmoe_format {
   /* NVFP4: e2m1 codes packed two per byte (even column in the low nibble), one e4m3
    * scale per 16 consecutive elements of a row, one fp32 scale per tensor.
    * value = code * block_scale * global_scale. */
-  FTMOE_FMT_NVFP4 = 1
+  FTMOE_FMT_NVFP4 = 1,
+  /* MXFP8 (SGLang gather page, Modifications: the mxfp8 branch, a ue8m0 scale per 32):
+   * e4m3 codes, one E8M0 byte b per 32 consecutive elements of a row, value = code * 2^(b -
+   * 127). Quantization (OCP Microscaling recipe): shared = floor(log2(amax)) - 8, clamped to
+   * [-127, 127] (zero and subnormal amax give -127), b = shared + 127, code =
+   * e4m3_rne_satfinite(x * 2^-shared). No tensor scale (global_scale must be NULL). */
+  FTMOE_FMT_MXFP8 = 2
 } ftmoe_format;
 
 /* Element type of the forward's output rows (FreeToken "perf(moe): skip inactive block-fp8
@@ -85,6 +91,8 @@ typedef enum ftmoe_out_dtype {
  * NVFP4: q      uint8 [E][n][k/2]
  *        scales uint8 (e4m3) [E][n][k/16]
  *        global_scale float [E]
+ * MXFP8: q      uint8 [E][n][k]
+ *        scales uint8 (E8M0) [E][n][k/32]; the grouped GEMM needs k % 512 == 0
  * Gate/up banks hold the gate rows [0, I) then the up rows [I, 2I) of each expert. */
 typedef struct ftmoe_expert_bank {
   int32_t format;      /* ftmoe_format */
@@ -93,12 +101,13 @@ typedef struct ftmoe_expert_bank {
   int64_t k;
   const uint8_t* q;
   const void* scales;
-  const float* global_scale; /* NVFP4 only; NULL for FP8 */
+  const float* global_scale; /* NVFP4 only; NULL for FP8 and MXFP8 */
 } ftmoe_expert_bank;
 
 /* Quantized activation rows [rows, k] in the same formats (FP8: scales float
  * [rows][ceil(k/128)]; NVFP4: q [rows][k/2], scales e4m3 [rows][k/16], global_scale
- * float[1]). Rows are dense (row stride k, resp. k/2 bytes). */
+ * float[1]; MXFP8: q [rows][k], scales E8M0 [rows][k/32]). Rows are dense (row stride k,
+ * resp. k/2 bytes). */
 typedef struct ftmoe_act {
   int32_t format;
   int32_t reserved;
@@ -161,14 +170,17 @@ ftmoe_status ftmoe_pick_tile(int64_t routes, int32_t num_experts, ftmoe_tile* ou
  *   global_scale must be NULL.
  * NVFP4 (requires k % 32 == 0): g = amax_tensor / 2688 is written to global_scale[0];
  *   per 16 elements sb = e4m3(amax_block / (6 g)), q = e2m1_rne(x / (sb g)).
- *   q uint8 [rows][k/2]; scales uint8 [rows][k/16]. */
+ *   q uint8 [rows][k/2]; scales uint8 [rows][k/16].
+ * MXFP8 (requires k % 32 == 0; global_scale must be NULL): per 32 elements the E8M0 byte and
+ *   codes of FTMOE_FMT_MXFP8. q uint8 [rows][k]; scales uint8 [rows][k/32]. */
 ftmoe_status ftmoe_quantize_act(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
                                 int32_t format, uint8_t* q, void* scales, float* global_scale,
                                 void* stream);
 
 /* Weight-bank quantization of float32 w [E][n][k] (dense) into the layout of
  * ftmoe_expert_bank: FP8 with one scale per 128x128 block (amax / 448, padded grid),
- * or NVFP4 with one global scale per expert matrix (requires k % 32 == 0). */
+ * NVFP4 with one global scale per expert matrix (requires k % 32 == 0), or MXFP8 with one
+ * E8M0 byte per 32 elements of a row (requires k % 32 == 0; global_scale NULL). */
 ftmoe_status ftmoe_quantize_weights(const float* w, int32_t num_experts, int64_t n, int64_t k,
                                     int32_t format, uint8_t* q, void* scales, float* global_scale,
                                     void* stream);
@@ -201,9 +213,23 @@ ftmoe_status ftmoe_gather_rows_scales(const uint8_t* src, const void* src_scales
                                       const int32_t* n_dst_dev, uint8_t* dst, void* dst_scales,
                                       void* stream);
 
+/* Gather of a bf16 activation with quantization of the gathered rows (SGLang gather page,
+ * Modifications: the mxfp8 branch gathers a bf16 activation through its own kernel): for
+ * every destination row d < n_dst (or < *n_dst_dev when given), the bf16 row x[dst2src[d]]
+ * (row stride ld_x elements, n_src rows) is quantized into q [n_dst][k] and scales
+ * [n_dst][...] in `format`'s layout. Only FTMOE_FMT_MXFP8 (k % 32 == 0); other formats
+ * return FTMOE_UNSUPPORTED. Quantization is per row, so the result equals quantizing the
+ * source rows and gathering the codes. A map entry outside [0, n_src) is skipped (its row
+ * is left untouched) and raises FTMOE_ERR_MAP_RANGE. n_dst == 0 launches nothing. */
+ftmoe_status ftmoe_gather_quantize_act(const uint16_t* x, int64_t n_src, int64_t k, int64_t ld_x,
+                                       const int32_t* dst2src, int64_t n_dst, const int32_t* n_dst_dev,
+                                       int32_t format, uint8_t* q, void* scales, void* stream);
+
 /* Grouped gate/up GEMM: out[row, c] = sum over 128-wide K blocks kb of
  *   act_scale[row, kb] * w_scale[e, c/128, kb] * sum_{k in kb} a[row, k] * w[e, c, k]
- * for c in [0, w->n) (= 2I), with e the expert of the row (see ftmoe_routes).
+ * for c in [0, w->n) (= 2I), with e the expert of the row (see ftmoe_routes). NVFP4 and
+ * MXFP8 banks apply their own scales (code * block scale [* tensor scales]) inside the
+ * block-scaled MMA; both take FTMOE_ROUTES_GROUPED only (k % 256 == 0, resp. k % 512 == 0).
  * a->k must equal w->k (= hidden). out float32, row stride ld_out >= w->n.
  * FTMOE_ROUTES_SLOTS: an inactive route's row is written as zeros before anything of
  * that route is read (FreeToken page, first section). tile may be NULL. */
@@ -234,7 +260,8 @@ ftmoe_status ftmoe_grouped_gemm_gateup_silu(const ftmoe_act* a, const ftmoe_rout
  * g = gu[row, 0:inter], u = gu[row, inter:2*inter], silu(g) = g / (1 + exp(-g)) in fp32;
  * then a is quantized like ftmoe_quantize_act (FP8: q [rows][inter], scales float
  * [rows][ceil(inter/128)]; NVFP4: q [rows][inter/2], scales [rows][inter/16],
- * global_scale float[1] taken over all valid rows). rows_dev: optional device int32
+ * global_scale float[1] taken over all valid rows; MXFP8: q [rows][inter], scales E8M0
+ * [rows][inter/32], global_scale NULL). rows_dev: optional device int32
  * count of valid rows (<= rows); rows beyond it are not touched. An all-zero input
  * row gives scale 0 and zero codes. */
 ftmoe_status ftmoe_silu_mul(const float* gu, int64_t rows, int64_t inter, int64_t ld_gu,
@@ -286,6 +313,10 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * the separate kernel. Paths 2 and 3 give bit-identical outputs; path 4 adds the partial
  * sums of a gate/up element in another order, so it agrees with them within the fp32
  * rounding of that sum.
+ * NVFP4 and MXFP8 take the grouped path with the separate SiLU-and-mul kernel only (paths 0
+ * and 2; 1, 3 and 4 return FTMOE_UNSUPPORTED). MXFP8 segments the routes first, then
+ * gathers the bf16 token rows and quantizes the gathered rows (ftmoe_gather_quantize_act);
+ * its GEMMs need H % 512 == 0 and I % 512 == 0.
  * ------------------------------------------------------------------------------------ */
 typedef struct ftmoe_moe_shape {
   int64_t tokens;     /* T */

@@ -228,6 +228,72 @@ def nvfp4_requant_flip_bound(res, expert_ids, weights, bank_gu, bank_dn):
     return extra
 
 
+def mxfp8_sum_rel(k):
+    """Bound on the MXFP8 block-scaled MMA's error over K as a share of the sum of the product
+    magnitudes: one fp32 ulp (2^-23, truncation) of the running sum per K = 32 instruction.
+    The accumulation grows with K, unlike the FP8 path's per-128 promotion on CUDA cores; the
+    GEMM test measures it at K = 512 .. 7168 against this bound."""
+    return (k / 32) * 2.0 ** -23
+
+
+def mxfp8_route_move(a, ea):
+    """Per intermediate element of one route, how far the kernels' MXFP8 re-quantization may
+    move its dequantized value from the oracle's: a (float64 silu(g)*u of the route), ea (the
+    kernels' fp32 error bound on it). Per 32 elements the shared exponent floor(log2(amax)) - 8
+    and each e4m3 code are decisions taken from fp32 values. Where the oracle's block maximum
+    lies within their error of a power of two, the block's scale may be a binade finer or
+    coarser: under either an element's code is within an E4M3 step (1/8 of its value) or the
+    clamp at 448 (under 1/8 of 512) of it, or below the smallest step, so a quarter of |a| plus
+    two of the smallest steps covers it. Where a scaled value lies within their error of a code
+    midpoint it may move by one code step."""
+    from oracle import formats as F
+    pos = F.E4M3_VALUES[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2
+    inter = a.shape[0]
+    a32 = a.astype(np.float32).astype(np.float64)
+    move = np.zeros(inter)
+    for b in range(-(-inter // 32)):
+        sl = slice(b * 32, min(inter, (b + 1) * 32))
+        blk = np.abs(a32[sl])
+        amax = float(np.max(blk))
+        if amax == 0:
+            continue
+        sh = M.mx_shared_exp(amax)
+        X = 2.0 ** sh
+        err_max = float(ea[sl][np.argmax(blk)])
+        lo, hi = 2.0 ** (sh + 8), 2.0 ** (sh + 9)  # amax's binade when not clamped
+        if amax - err_max < lo or amax + err_max >= hi:
+            move[sl] = np.maximum(move[sl], 0.25 * blk + 2.0 ** -8 * X)
+        v = blk / X
+        ev = ea[sl] / X
+        k = np.clip(np.searchsorted(mids, v), 1, len(mids) - 1)
+        d = np.minimum(np.abs(v - mids[k - 1]), np.abs(v - mids[np.minimum(k, len(mids) - 1)]))
+        step = np.abs(np.diff(pos))[np.clip(np.searchsorted(pos, v) - 1, 0, len(pos) - 2)] * X
+        move[sl] = np.maximum(move[sl], np.where(d <= ev, step, 0.0))
+    return move
+
+
+def mxfp8_requant_flip_bound(res, expert_ids, weights, bank_gu, bank_dn):
+    """requant_flip_bound for the MXFP8 intermediate (see mxfp8_route_move): each element's
+    possible move reaches token t's output through |w_tj| |W_down[h, i]|. Computed from the
+    oracle's values only."""
+    ids = np.asarray(expert_ids)
+    w = np.asarray(weights, np.float64)
+    T = ids.shape[0]
+    H = res["out"].shape[1]
+    extra = np.zeros((T, H))
+    for (t, j), a in res["a"].items():
+        e = int(ids[t, j])
+        gu = res["gu"][(t, j)]
+        absum = np.abs(bank_gu.dequant(e)) @ np.abs(res["xdeq"][t])
+        ea = _silu_mul_error(gu, absum, mxfp8_sum_rel(res["xdeq"].shape[1])) + 2.0 ** -21 * np.abs(a)
+        move = mxfp8_route_move(a, ea)
+        nz = np.nonzero(move)[0]
+        if nz.size:
+            extra[t] += abs(w[t, j]) * (np.abs(bank_dn.dequant(e)[:, nz]) @ move[nz])
+    return extra
+
+
 class Problem:
     """A seeded MoE FFN problem: activations, routes, weights, GPU bank, oracle bank."""
 
@@ -237,7 +303,7 @@ class Problem:
         import block_quantized_moe_gb300 as ft
         self.T, self.H, self.I, self.E, self.topk, self.seed, self.dev = T, H, I, E, topk, seed, device
         self.fmt = fmt
-        self.ft_fmt = ft.FMT_FP8 if fmt == "fp8" else ft.FMT_NVFP4
+        self.ft_fmt = {"fp8": ft.FMT_FP8, "nvfp4": ft.FMT_NVFP4, "mxfp8": ft.FMT_MXFP8}[fmt]
         self.x = synth.activations_bf16(T, H, seed, device)
         if ids is None:
             ids = synth.routes(T, topk, E, seed, active_per_token=active, device=device)
@@ -257,6 +323,23 @@ class Problem:
             obg = M.LazyBank(lambda e: self.raw_gateup(e).cpu().numpy(), 2 * I, "nvfp4")
             obd = M.LazyBank(lambda e: self.raw_down(e).cpu().numpy(), H, "nvfp4")
             Problem._bank_cache[key] = (parts[0], parts[1], obg, obd)
+        if key not in Problem._bank_cache and fmt == "mxfp8":
+            parts = []
+            for n, k, raw in ((2 * I, H, self.raw_gateup), (H, I, self.raw_down)):
+                q = torch.empty(E, n, k, dtype=torch.uint8, device=device)
+                sf = torch.empty(E, n, k // 32, dtype=torch.uint8, device=device)
+                for e in range(E):
+                    ft.ftmoe_quantize_weights(raw(e)[None], q[e:e + 1], sf[e:e + 1], fmt=ft.FMT_MXFP8)
+                parts.append((q, sf))
+            obg = M.LazyBank(lambda e: self.raw_gateup(e).cpu().numpy(), 2 * I, "mxfp8")
+            obd = M.LazyBank(lambda e: self.raw_down(e).cpu().numpy(), H, "mxfp8")
+            Problem._bank_cache[key] = (parts[0], parts[1], obg, obd)
+        if fmt == "mxfp8":
+            (gq, gs), (dq, ds), self.obank_gu, self.obank_dn = Problem._bank_cache[key]
+            self.bank_gu = ft.make_bank(gq, gs, fmt=ft.FMT_MXFP8)
+            self.bank_dn = ft.make_bank(dq, ds, fmt=ft.FMT_MXFP8)
+            self._keep = (gq, gs, dq, ds)
+            return
         if fmt == "nvfp4":
             (gq, gs, gg), (dq, ds, dg), self.obank_gu, self.obank_dn = Problem._bank_cache[key]
             self.bank_gu = ft.make_bank(gq, gs, gg, fmt=ft.FMT_NVFP4)
@@ -299,7 +382,8 @@ class Problem:
         res = self.oracle(ids=ids, weights=weights, x=x, tokens_subset=tokens_subset)
         ref = res["out"]
         wv = torch.where(ids >= 0, weights, torch.zeros_like(weights)).cpu().numpy()
-        bound = requant_flip_bound if self.fmt == "fp8" else nvfp4_requant_flip_bound
+        bound = {"fp8": requant_flip_bound, "nvfp4": nvfp4_requant_flip_bound,
+                 "mxfp8": mxfp8_requant_flip_bound}[self.fmt]
         extra = bound(res, ids.cpu().numpy(), wv, self.obank_gu, self.obank_dn)
         got = out.float().cpu().numpy()
         rows = list(range(self.T)) if tokens_subset is None else list(tokens_subset)

@@ -30,6 +30,8 @@ def _quantize_weight(w, fmt):
             return C.quantize_weight_fp8(w)
         except (OSError, RuntimeError):
             return M.quantize_weight_fp8_fast(w)
+    if fmt == "mxfp8":
+        return M.quantize_mxfp8_fast(w)
     return M.quantize_nvfp4(w)
 
 
@@ -41,6 +43,8 @@ def _weights(e, which):
     n, k = (2 * I, H) if which == "gateup" else (H, I)
     w = synth.expert_weight_fp32(n, k, seed, e, which, "cpu").numpy()
     parts = _quantize_weight(w, fmt)
+    if fmt == "mxfp8":
+        return M.dequant_mxfp8(*parts)
     return M.dequant_weight_fp8(*parts) if fmt == "fp8" else M.dequant_nvfp4(*parts)
 
 
@@ -50,26 +54,28 @@ def _x_rows(c, tokens):
     call = _CTX["calls"][c]
     if _CTX["fmt"] == "fp8":
         return M.dequant_act_fp8(call["xq"][tokens], call["xs"][tokens])
+    if _CTX["fmt"] == "mxfp8":
+        return M.dequant_mxfp8(call["xq"][tokens], call["xs"][tokens])
     return M.dequant_nvfp4(call["xq"][tokens], call["xs"][tokens], call["xg"])
 
 
 def _gateup(c, tokens, wg):
     """Gate/up rows of call c's tokens, silu(g)*u, and the kernels' fp32 error bound on it."""
-    from common import FP32_SUM_REL, NVFP4_SUM_REL, _silu_mul_error
+    from common import FP32_SUM_REL, NVFP4_SUM_REL, _silu_mul_error, mxfp8_sum_rel
     from oracle import moe as M
     x = _x_rows(c, np.asarray(tokens))
     gu = M.gemm_rows(x, wg)
     a = M.silu_mul(gu)
     absum = np.abs(x) @ np.abs(wg).T
-    rel = FP32_SUM_REL if _CTX["fmt"] == "fp8" else NVFP4_SUM_REL
+    rel = {"fp8": FP32_SUM_REL, "nvfp4": NVFP4_SUM_REL, "mxfp8": mxfp8_sum_rel(_CTX["H"])}[_CTX["fmt"]]
     ea = np.stack([_silu_mul_error(gu[i], absum[i], rel) for i in range(len(tokens))]) + 2.0 ** -21 * np.abs(a)
     return a, ea
 
 
 def expert_fp8(task):
-    """FP8, one pass: for every call, the down-GEMM output rows of expert e's checked routes
-    and their re-quantization allowance, (y [m, H], extra [m, H]) per call, tokens in the
-    task's order."""
+    """FP8 and MXFP8 (row-wise scales only), one pass: for every call, the down-GEMM output
+    rows of expert e's checked routes and their re-quantization allowance, (y [m, H],
+    extra [m, H]) per call, tokens in the task's order."""
     from oracle import formats as F
     from oracle import moe as M
     e, per_call = task
@@ -83,9 +89,13 @@ def expert_fp8(task):
             out.append(None)
             continue
         a, ea = _gateup(c, tokens, wg)
-        adeq, _ = M.quantize_acts(a.astype(np.float32), "fp8")
+        adeq, _ = M.quantize_acts(a.astype(np.float32), _CTX["fmt"])
         y = M.gemm_rows(adeq, wd)
-        extra = np.stack([_fp8_extra(a[i], ea[i], awd, F) for i in range(len(tokens))])
+        if _CTX["fmt"] == "mxfp8":
+            from common import mxfp8_route_move
+            extra = np.stack([awd @ mxfp8_route_move(a[i], ea[i]) for i in range(len(tokens))])
+        else:
+            extra = np.stack([_fp8_extra(a[i], ea[i], awd, F) for i in range(len(tokens))])
         out.append((y, extra))
     return out
 
@@ -224,6 +234,9 @@ def forward_calls(calls, H, I, E, seed, fmt, workers):
         if fmt == "fp8":
             xq, xs = M.quantize_act_fp8_fast(c["x32"])
             ctx_calls.append(dict(xq=xq, xs=xs))
+        elif fmt == "mxfp8":
+            xq, xs = M.quantize_mxfp8_fast(c["x32"])
+            ctx_calls.append(dict(xq=xq, xs=xs))
         else:
             xq, xs, xg = M.quantize_nvfp4(c["x32"])
             ctx_calls.append(dict(xq=xq, xs=xs, xg=xg))
@@ -253,7 +266,7 @@ def forward_calls(calls, H, I, E, seed, fmt, workers):
     saved = {v: os.environ.get(v) for v in _BLAS_VARS}
     os.environ.update({v: "1" for v in _BLAS_VARS})
     try:
-        if fmt == "fp8":
+        if fmt in ("fp8", "mxfp8"):
             tasks = [(e, [[t for t, _ in rc[e]] for rc in routes_chk]) for e in range(E)]
             with pool_ctx.Pool(workers, initializer=_init, initargs=(ctx,)) as pool:
                 res = pool.map(expert_fp8, tasks, chunksize=1)

@@ -7,12 +7,12 @@ import numpy as np
 import pytest
 
 import synth
-from common import nvfp4_requant_flip_bound, requant_flip_bound
+from common import mxfp8_requant_flip_bound, nvfp4_requant_flip_bound, requant_flip_bound
 from fullsize_oracle import forward_calls, forward_subsample
 from oracle import moe as M
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "mxfp8"])
 def test_driver_equals_the_oracle_forward(fmt):
     T, H, I, E, k, seed = 12, 256, 128, 6, 3, 77
     x = synth.activations_bf16(T, H, seed, "cpu").float().numpy()
@@ -28,7 +28,7 @@ def test_driver_equals_the_oracle_forward(fmt):
     assert np.allclose(got[sub], ref[sub], rtol=1e-12, atol=1e-15 * scale)
     assert not np.any(got[[t for t in range(T) if t not in sub]])
     wv = np.where(ids >= 0, w, 0.0)
-    bound = requant_flip_bound if fmt == "fp8" else nvfp4_requant_flip_bound
+    bound = {"fp8": requant_flip_bound, "nvfp4": nvfp4_requant_flip_bound, "mxfp8": mxfp8_requant_flip_bound}[fmt]
     ref_extra = bound(res, ids, wv, bg, bd)
     assert np.allclose(extra[sub], ref_extra[sub], rtol=1e-6, atol=1e-12 * scale)
 
@@ -43,7 +43,7 @@ def test_driver_calls_sharing_one_bank_equal_separate_runs():
         ids = synth.routes(T, k, E, seed + s, device="cpu").numpy()
         w = synth.routing_weights(T, k, seed + s, "cpu").numpy()
         calls.append(dict(x32=x, ids=ids, weights=w, checked=list(range(0, T, 2))))
-    for fmt in ("fp8", "nvfp4"):
+    for fmt in ("fp8", "nvfp4", "mxfp8"):
         both = forward_calls(calls, H, I, E, seed, fmt, workers=2)
         for c, (out, extra) in zip(calls, both):
             one, one_extra = forward_subsample(c["x32"], c["ids"], c["weights"], c["checked"], H, I, E, seed, fmt,

@@ -1,5 +1,5 @@
 """The prefill workloads at full size against the oracle: 256 experts, top-6, hidden 7168,
-intermediate 2048, FP8 with 128x128 block scales and NVFP4.
+intermediate 2048, FP8 with 128x128 block scales, NVFP4 and MXFP8.
 
 Every token is compared at 1,536 routes (256 tokens) and 6,144 routes (1,024 tokens); the
 24,576-route calls (4,096 tokens) are compared on a seeded random 1,024-token subsample.
@@ -41,11 +41,15 @@ def _bank(ft, n, k, tag, fmt):
         q = torch.empty(E, n, k, dtype=torch.uint8, device=DEV)
         s = torch.empty(E, -(-n // 128), -(-k // 128), dtype=torch.float32, device=DEV)
         g = None
+    elif fmt == "mxfp8":
+        q = torch.empty(E, n, k, dtype=torch.uint8, device=DEV)
+        s = torch.empty(E, n, k // 32, dtype=torch.uint8, device=DEV)
+        g = None
     else:
         q = torch.empty(E, n, k // 2, dtype=torch.uint8, device=DEV)
         s = torch.empty(E, n, k // 16, dtype=torch.uint8, device=DEV)
         g = torch.empty(E, dtype=torch.float32, device=DEV)
-    f = ft.FMT_FP8 if fmt == "fp8" else ft.FMT_NVFP4
+    f = {"fp8": ft.FMT_FP8, "nvfp4": ft.FMT_NVFP4, "mxfp8": ft.FMT_MXFP8}[fmt]
     draw = lambda e: synth.expert_weight_fp32(n, k, WEIGHT_SEED, e, tag, "cpu")  # noqa: E731
     threads = max(2, min(16, os.cpu_count() or 4))
     with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
@@ -69,7 +73,7 @@ def _call(routes):
 
 def _gpu_forward(ft, banks, x, ids, w, fmt, path=0):
     T = x.shape[0]
-    f = ft.FMT_FP8 if fmt == "fp8" else ft.FMT_NVFP4
+    f = {"fp8": ft.FMT_FP8, "nvfp4": ft.FMT_NVFP4, "mxfp8": ft.FMT_MXFP8}[fmt]
     shape = ft.moe_shape(T, H, I, TOPK, E, fmt=f, path=path)
     ws = torch.empty(ft.ftmoe_forward_workspace_bytes(shape), dtype=torch.uint8, device=DEV)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
@@ -79,7 +83,8 @@ def _gpu_forward(ft, banks, x, ids, w, fmt, path=0):
     return out
 
 
-@pytest.mark.parametrize("fmt,sizes", [("fp8", (1536, 6144, 24576)), ("nvfp4", (6144, 24576))])
+@pytest.mark.parametrize("fmt,sizes", [("fp8", (1536, 6144, 24576)), ("nvfp4", (6144, 24576)),
+                                       ("mxfp8", (6144, 24576))])
 def test_prefill_full_sizes_against_the_oracle(ft, fmt, sizes):
     keep_gu, bank_gu = _bank(ft, 2 * I, H, "gateup", fmt)
     keep_dn, bank_dn = _bank(ft, H, I, "down", fmt)
