@@ -12,7 +12,8 @@
 // epilogue only applies g_a * g_w once.
 //
 // Work layout as in the FP8 kernel: MMA M = 128 weight rows, MMA N = the token tile; one
-// persistent CTA per SM over a contiguous range of (expert, token tile, weight block) units.
+// persistent CTA per SM; CTA c takes units c, c + G, ... of the (expert, token tile, weight
+// block) list.
 // Roles: warp 0 TMA producer (code tiles with the 128-byte swizzle, scale tiles plain);
 // warp 1 MMA issuer and TMEM owner; warps 2-5 move each stage's scale factors from shared
 // memory into TMEM, warps 6-13 epilogue. Every wait is bounded.
@@ -179,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t tmem_base = s_tmem;
   const int total_units = cum[E];
-  const int u_begin = (int)(((int64_t)blockIdx.x * total_units) / gridDim.x);
-  const int u_end = (int)(((int64_t)(blockIdx.x + 1) * total_units) / gridDim.x);
+  // units c, c + G, ...: the CTAs sweep the (expert, token tile, weight block) list together,
+  // so a token tile is read by several CTAs at about the same time and stays in L2
+  const int u_begin = (int)blockIdx.x, u_end = total_units, u_step = (int)gridDim.x;
 
   auto decode = [&](int u, int& e, int& nb, int& row0, int& rows) {
     int lo = 0, hi = E - 1;
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto advance = [&]() {
         if (++sp == SP) {
           sp = 0;
-          if (++u < u_end) decode(u, e, nb, row0, rows);
+          if ((u += u_step) < u_end) decode(u, e, nb, row0, rows);
         }
       };
       // one box per operand and stage: K blocks [sp * KBS, sp * KBS + KBS)
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_nvf4(TT);
       const int SP = (KB + KBS - 1) / KBS;
       bool ok = true;
-      for (int u = u_begin; u < u_end && ok && !s_abort; ++u, ++uc) {
+      for (int u = u_begin; u < u_end && ok && !s_abort; u += u_step, ++uc) {
         const uint32_t acc = uc % kAcc;
         if (!mbar_wait(smem_u32(&tempty[acc]), ((uc / kAcc) & 1) ^ 1, &s_abort)) { ok = false; break; }
         fence_after();
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int SP = (KB + KBS - 1) / KBS;
     uint32_t it = 0, kc = 0;
-    for (int u = u_begin; u < u_end; ++u) {
+    for (int u = u_begin; u < u_end; u += u_step) {
       bool ok = true;
       for (int sp = 0; sp < SP && ok; ++sp, ++it) {
         const int st = it % S;
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     constexpr int HC = TT / 2;
     uint32_t uc = 0;
-    for (int u = u_begin; u < u_end; ++u, ++uc) {
+    for (int u = u_begin; u < u_end; u += u_step, ++uc) {
       int e, nb, row0, rows;
       decode(u, e, nb, row0, rows);
       const float f = __ldg(p.g_a) * __ldg(p.g_w + e);
