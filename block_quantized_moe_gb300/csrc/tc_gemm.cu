@@ -139,9 +139,9 @@ __host__ __device__ constexpr int kbs_for(int tt, int mode) {
 template <int TT, int MODE>
 struct Warps {
   static constexpr bool kSplitRegs = TT >= 64 && wb_of(MODE) == 2;
-  static constexpr int kCtl = kSplitRegs ? 4 : 2;
+  static constexpr int kCtl = 4;  // TMA, MMA, scale-product tables, one idle warp
   static constexpr int kThreads = 32 * (kCtl + kEpiWarps);
-  static constexpr int kCtlRegs = 56, kEpiRegs = 104;
+  static constexpr int kCtlRegs = 64, kEpiRegs = 104;
   static constexpr int kRegsNeeded = kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps;
 };
 
@@ -159,14 +159,10 @@ struct Smem {
   static __device__ __forceinline__ uint32_t w_off(int b, int h) {
     return (uint32_t)((MODE == kPair ? h * kWB + b : b * KBS + h) * kSubW);
   }
-  // epilogue tables (bytes): activation scales [kGroups][2][kSaChunk][TT / kGroups], their
-  // products with the weight-block scales [kGroups][2][kSaChunk][kWB][TT / kGroups], SiLU
-  // group maxima per lane quarter and group scales [kGroups][5][TT / kGroups], then the
-  // weight-block scales of the unit
-  // [kGroups][kWB][K blocks] (sw_bytes: sized by the launch's K)
-  static constexpr int kSaBytes = 2 * kSaChunk * TT * 4;
+  // epilogue tables (bytes): the products act_scale x weight_scale
+  // [kGroups][2][kSaChunk][kWB][TT / kGroups] (two chunk buffers), SiLU group maxima per lane
+  // quarter and group scales [kGroups][5][TT / kGroups]
   static constexpr int kProdBytes = 2 * kSaChunk * kWB * TT * 4;
-  static __host__ __device__ int sw_bytes(int kb_count) { return ((kGroups * kWB * kb_count + 3) & ~3) * 4; }
   static constexpr int kRedBytes = MODE == kGateUpSilu ? 5 * TT * 4 : 0;
 };
 
@@ -182,11 +178,9 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
   uint8_t* tiles = smem;
-  float* sa = reinterpret_cast<float*>(smem + (size_t)S * SM::kStage);
-  float* prod = sa + SM::kSaBytes / 4;
+  float* prod = reinterpret_cast<float*>(smem + (size_t)S * SM::kStage);
   float* red = prod + SM::kProdBytes / 4;
-  float* swt = red + SM::kRedBytes / 4;
-  int* cum = reinterpret_cast<int*>(swt + SM::sw_bytes(p.kb_count) / 4);  // [E+2] unit prefix
+  int* cum = reinterpret_cast<int*>(red + SM::kRedBytes / 4);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
   int* seg_hi = seg_lo + p.E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
@@ -196,6 +190,8 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   constexpr int kTmemCols = kAcc * WB * TT < 32 ? 32 : kAcc * WB * TT;
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + kAcc;
+  uint64_t* pfull = tempty + kAcc;   // [2] a chunk's scale products are in place
+  uint64_t* pempty = pfull + 2;      // [2] every epilogue warp is done with a chunk buffer
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -216,6 +212,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
       mbar_init(smem_u32(&tempty[i]), kCP ? 2 * kEpiWarps : kEpiWarps);  // one arrival per epilogue warp
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&pfull[i]), 32);         // every lane of the table warp
+      mbar_init(smem_u32(&pempty[i]), kEpiWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -450,6 +450,75 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         }
       }
     }
+  } else if (warp == 2) {
+    // ------------------------ scale-product tables ------------------------
+    // For every (unit, chunk of kSaChunk K blocks) of this CTA, in the epilogue's order, the
+    // products s_a[row0 + col][kb] * s_w[e, weight block, kb]: the same for all 128 weight
+    // rows, so formed once per token column instead of per element. Two buffers alternate;
+    // each lane loads all its scales of a chunk before it waits for the buffer, so the loads
+    // of the next chunk are in flight while the epilogue still reads the current one.
+    constexpr int NJ = (TT + 31) / 32;  // token columns per lane
+    const int nchunks = (KB + kSaChunk - 1) / kSaChunk;
+    uint32_t gch = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok; u += u_step) {
+      int e, nb, tt, row0, rows;
+      decode(u, e, nb, tt, row0, rows);
+      for (int ch = 0; ch < nchunks; ++ch, ++gch) {
+        // (kernels that split registers keep 64 for this warpgroup: there the weight scales
+        // are loaded per block inside the store loop and the columns go in batches)
+        constexpr bool kLean = W::kSplitRegs;
+        constexpr int JB = kLean ? 1 : NJ;
+        auto w_scale = [&](int b, int kbl) {
+          const int kb = ch * kSaChunk + kbl;
+          return kb < KB ? __ldg(p.w_s + ((int64_t)e * NB + wblock(nb, b)) * KB + kb) : 0.0f;
+        };
+        float sw[kLean ? 1 : WB][kSaChunk];
+        if constexpr (!kLean) {
+#pragma unroll
+          for (int b = 0; b < WB; ++b)
+#pragma unroll
+            for (int kbl = 0; kbl < kSaChunk; ++kbl) sw[b][kbl] = w_scale(b, kbl);
+        }
+        const int buf = (int)(gch & 1);
+#pragma unroll
+        for (int j0 = 0; j0 < NJ; j0 += JB) {
+          float sa[JB][kSaChunk];
+#pragma unroll
+          for (int jj = 0; jj < JB; ++jj) {
+            const int col = lane + 32 * (j0 + jj);
+#pragma unroll
+            for (int kbl = 0; kbl < kSaChunk; ++kbl) {
+              const int kb = ch * kSaChunk + kbl;
+              sa[jj][kbl] =
+                  (col < TT && col < rows && kb < KB) ? __ldg(p.a_s + (int64_t)(row0 + col) * KB + kb) : 0.0f;
+            }
+          }
+          if (j0 == 0 && !mbar_wait(smem_u32(&pempty[buf]), ((gch >> 1) & 1) ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int b = 0; b < WB; ++b) {
+            float swb[kSaChunk];
+#pragma unroll
+            for (int kbl = 0; kbl < kSaChunk; ++kbl) swb[kbl] = kLean ? w_scale(b, kbl) : sw[kLean ? 0 : b][kbl];
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj) {
+              const int col = lane + 32 * (j0 + jj);
+              if (col < TT) {
+                const int g = col / (TT / kGroups), c = col - g * (TT / kGroups);
+                float* dst = prod + g * 2 * kSaChunk * WB * (TT / kGroups) + buf * kSaChunk * WB * (TT / kGroups);
+#pragma unroll
+                for (int kbl = 0; kbl < kSaChunk; ++kbl) dst[(kbl * WB + b) * (TT / kGroups) + c] = sa[jj][kbl] * swb[kbl];
+              }
+            }
+          }
+        }
+        if (!ok) break;
+        mbar_arrive(smem_u32(&pfull[buf]));  // each lane releases its own products
+      }
+    }
   }
   } else {
     // --------------------------------- epilogue ---------------------------------
@@ -464,102 +533,49 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     const int grp = ew >> 2;                  // column group
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int tid_g = (ew & 3) * 32 + lane;   // 0..127 within the group
-    float* my_sw = swt + grp * WB * KB;       // [WB][KB]
-    float* my_sa = sa + grp * 2 * kSaChunk * HC;  // [2][kSaChunk][HC]
     float* my_prod = prod + grp * 2 * kSaChunk * WB * HC;  // [2][kSaChunk][WB][HC]
     float* my_red = red + grp * 5 * HC;       // [4][HC] maxima, [HC] scales (kGateUpSilu)
     uint32_t kc = 0;
-    float sw_next[WB];
-    bool have_next = false;
     float acc[WB][HC];
-    const int nchunks = (KB + kSaChunk - 1) / kSaChunk;
-    // Activation scales travel in chunks of kSaChunk K blocks, copied global -> shared by
-    // cp.async (no registers held) into two buffers that alternate along the whole sequence
-    // of (unit, chunk) pairs of this CTA: entry (kbl, c) of a chunk is
-    // s_a[row0 + grp * HC + c][ch * kSaChunk + kbl], 0 for columns past the tile's rows.
-    // While a chunk is in use the next one is in flight, the next unit's first chunk included.
-    auto sa_issue = [&](int r0, int nrows, int ch, int buf) {
-      for (int i = tid_g; i < kSaChunk * HC; i += 128) {
-        const int kbl = i / HC, c = i - kbl * HC;
-        const int kb = ch * kSaChunk + kbl, r = grp * HC + c;
-        const bool valid = kb < KB && r < nrows;
-        cp_async_4(smem_u32(my_sa + buf * kSaChunk * HC + i), valid ? p.a_s + (int64_t)(r0 + r) * KB + kb : p.a_s,
-                   valid);
-      }
-      cp_async_commit();
-    };
-    // products s_a * s_w of the chunk in buffer buf, one per (K block, weight block,
-    // column): the same for all 128 rows, so formed once here instead of per element
-    auto prod_fill = [&](int ch, int buf) {
-      const float* src = my_sa + buf * kSaChunk * HC;
-      float* dst = my_prod + buf * kSaChunk * WB * HC;
-      for (int i = tid_g; i < kSaChunk * WB * HC; i += 128) {
-        const int kbl = i / (WB * HC), rem = i - kbl * (WB * HC);
-        const int b = rem / HC, c = rem - b * HC;
-        const int kb = ch * kSaChunk + kbl;
-        dst[i] = kb < KB ? src[kbl * HC + c] * my_sw[b * KB + kb] : 0.0f;
-      }
-    };
-    uint32_t gch = 0;  // chunks begun so far; chunk gch uses buffer gch & 1
-    if (u_begin < u_end) {
-      int e0, nb0, tt0, r00, rows0;
-      decode(u_begin, e0, nb0, tt0, r00, rows0);
-      sa_issue(r00, rows0, 0, 0);
-    }
+    uint32_t gch = 0;  // chunks begun so far; chunk gch uses product buffer gch & 1
     for (int u = u_begin; u < u_end; u += u_step) {
       int e, nb, tt, row0, rows;
       decode(u, e, nb, tt, row0, rows);
-      // all warps of the group leave together on an abort; the barrier also orders the
-      // previous unit's reads of the weight-scale table before it is rewritten
+      // all warps of the group leave together on an abort
       if (named_bar_or(1 + grp, 128, s_abort)) break;
-      // weight-block scales of this unit (prefetched during the previous unit)
-      if (tid_g < KB) {
-#pragma unroll
-        for (int b = 0; b < WB; ++b)
-          my_sw[b * KB + tid_g] =
-              have_next ? sw_next[b] : __ldg(p.w_s + ((int64_t)e * NB + wblock(nb, b)) * KB + tid_g);
-      }
-      have_next = false;
-      if (u + u_step < u_end && tid_g < KB) {
-        int e2, nb2, tt2, r02, rows2;
-        decode(u + u_step, e2, nb2, tt2, r02, rows2);
-#pragma unroll
-        for (int b = 0; b < WB; ++b) sw_next[b] = __ldg(p.w_s + ((int64_t)e2 * NB + wblock(nb2, b)) * KB + tid_g);
-        have_next = true;
-      }
 #pragma unroll
       for (int b = 0; b < WB; ++b)
 #pragma unroll
         for (int c = 0; c < HC; ++c) acc[b][c] = 0.0f;
       bool ok = true;
+      // a group whose token columns all lie past the tile's rows has nothing to promote:
+      // it hands each accumulator straight back
+      const bool live = grp * HC < rows;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
-        const int ch = kb / kSaChunk, kbl = kb - ch * kSaChunk;
-        if (kbl == 0) {
-          // Chunk gch has landed once this thread's copies are done; the first barrier
-          // publishes it and shows that the products of chunk gch - 2 (same buffer) and the
-          // scales of chunk gch - 1 are no longer read, and that this unit's weight scales are
-          // in place; the second publishes the products. Then chunk gch + 1 goes in flight.
-          cp_async_wait<0>();
-          named_bar(1 + grp, 128);
-          prod_fill(ch, gch & 1);
-          named_bar(1 + grp, 128);
-          if (ch + 1 < nchunks) {
-            sa_issue(row0, rows, ch + 1, (gch + 1) & 1);
-          } else if (u + u_step < u_end) {
-            int e2, nb2, tt2, r02, rows2;
-            decode(u + u_step, e2, nb2, tt2, r02, rows2);
-            sa_issue(r02, rows2, 0, (gch + 1) & 1);
-          }
-          ++gch;
+        const int kbl = kb % kSaChunk;
+        const int buf = (int)(gch & 1);
+        if (kbl == 0 && ok) {
+          // the table warp's products of this chunk
+          const int got = mbar_wait(smem_u32(&pfull[buf]), (gch >> 1) & 1, &s_abort) ? 1 : 0;
+          ok = __all_sync(0xffffffffu, got) != 0;
         }
-        const int buf = (gch - 1) & 1;
         const uint32_t ab = kc % kAcc;
         if (ok) {
           const int got = mbar_wait(smem_u32(&tfull[ab]), (kc / kAcc) & 1, &s_abort) ? 1 : 0;
           ok = __all_sync(0xffffffffu, got) != 0;
         }
-        if (!ok) continue;
+        if (ok) {
         fence_after();
+        if (!live) {
+          fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kCP)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[ab]), 0));
+            else
+              mbar_arrive(smem_u32(&tempty[ab]));
+          }
+        } else {
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + ab * (WB * TT) + grp * HC;
         const float* pp = my_prod + (buf * kSaChunk + kbl) * WB * HC;
 #pragma unroll
@@ -591,6 +607,15 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
               acc[b][c0 + 4 * c4 + 3] = fmaf(d[b][4 * c4 + 3], s4.w, acc[b][c0 + 4 * c4 + 3]);
             }
           }
+        }
+        }  // live
+        }  // ok
+        if (kbl == kSaChunk - 1 || kb == KB - 1) {
+          // this warp reads nothing more of the chunk's products (on every path: the table
+          // warp must not wait on a warp that gave up)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&pempty[buf]));
+          ++gch;
         }
       }
       const int m = 32 * quarter + lane;  // row of this lane inside a 128-row weight block
@@ -659,7 +684,6 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         }
       }
     }
-    cp_async_wait<0>();  // a copy left in flight by an abort lands before the CTA exits
   }
 
   fence_before();
@@ -745,8 +769,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     *unsupported = 1;
     return cudaSuccess;
   }
-  const size_t fixed = 1024 /*align*/ + SM::kSaBytes + SM::kProdBytes + SM::kRedBytes + SM::sw_bytes(KB) +
-                       (size_t)(3 * a.E + 2) * 4 + 8;
+  const size_t fixed = 1024 /*align*/ + SM::kProdBytes + SM::kRedBytes + (size_t)(3 * a.E + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
   int dev = 0;
@@ -779,8 +802,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   }
   constexpr int kAcc = tc::acc_count(SM::kWB * TT);
   int stages = tc::kMaxStages;
-  while (stages > 2 && fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc) * 8 > max_smem) --stages;
-  const size_t smem = fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc) * 8;
+  while (stages > 2 && fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc + 4) * 8 > max_smem) --stages;
+  const size_t smem = fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc + 4) * 8;
   if (smem > max_smem) {
     *unsupported = 1;
     return cudaSuccess;
