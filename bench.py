@@ -499,7 +499,11 @@ class MoeWorkload:
         off = self.ws[lay["offsets"]:lay["offsets"] + (self.E + 1) * 4].view(torch.int32)
         tile = ft.ftmoe_pick_tile(R, self.E)
         if f == "fp8":
-            act, kname = ft.make_act(rq, rs), f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)"
+            # (a CTA pair per unit at token tile 128 where the matrix is whole 256-row block pairs)
+            pair = tile == 128 and (2 * self.I) % 256 == 0 and H % 128 == 0
+            act = ft.make_act(rq, rs)
+            kname = (f"tc_gemm_kernel<{tile}, CTA pair> (gate/up, grouped, tcgen05 cta_group::2)" if pair else
+                     f"tc_gemm_kernel<{tile}> (gate/up, grouped, tcgen05)")
         elif f == "mxfp8":
             act = ft.make_act(rq, rs, fmt=ft.FMT_MXFP8)
             kname = f"mxfp8_gemm_kernel<{tile}> (gate/up, grouped, tcgen05 block-scaled)"
