@@ -9,7 +9,8 @@
 
 namespace ftmoe {
 
-// One warp per (row, 128 outputs); lane owns 4 consecutive outputs.
+// One half-warp per (row, 128 outputs); a lane owns 8 consecutive outputs, so a warp keeps
+// two groups' gate and up loads (four 16-byte loads a lane) in flight before any arithmetic.
 template <bool kVec>
 __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
     const float* __restrict__ gu, int64_t rows, int64_t inter, int64_t ld,
@@ -25,43 +26,61 @@ __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
     const int64_t d = *rows_dev;
     limit = d < limit ? d : limit;
   }
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const int64_t units = limit * ng;  // (row, group) pairs
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < limit * ng;
-       w += nwarps) {
-    const int64_t row = w / ng, g = w - row * ng;
-    const int64_t c0 = g * kGroup + lane * 4;
+  // the loop bound is uniform over the warp, so every shuffle sees all 32 lanes
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); 2 * w < units; w += nwarps) {
+    const int64_t unit = 2 * w + (lane >> 4);
+    const bool live = unit < units;
+    const int64_t row = live ? unit / ng : 0, g = live ? unit - row * ng : 0;
+    const int64_t c0 = g * kGroup + hl * 8;
     const float* gr = gu + row * ld;
-    float a[4];
-    const bool full = c0 + 4 <= inter;
+    float a[8];
+    const bool full = live && c0 + 8 <= inter;
     if (kVec && full) {
-      const float4 gv = *reinterpret_cast<const float4*>(gr + c0);
-      const float4 uv = *reinterpret_cast<const float4*>(gr + inter + c0);
-      a[0] = silu_mul_1(gv.x, uv.x);
-      a[1] = silu_mul_1(gv.y, uv.y);
-      a[2] = silu_mul_1(gv.z, uv.z);
-      a[3] = silu_mul_1(gv.w, uv.w);
+      const float4 g0 = *reinterpret_cast<const float4*>(gr + c0);
+      const float4 g1 = *reinterpret_cast<const float4*>(gr + c0 + 4);
+      const float4 u0 = *reinterpret_cast<const float4*>(gr + inter + c0);
+      const float4 u1 = *reinterpret_cast<const float4*>(gr + inter + c0 + 4);
+      a[0] = silu_mul_1(g0.x, u0.x);
+      a[1] = silu_mul_1(g0.y, u0.y);
+      a[2] = silu_mul_1(g0.z, u0.z);
+      a[3] = silu_mul_1(g0.w, u0.w);
+      a[4] = silu_mul_1(g1.x, u1.x);
+      a[5] = silu_mul_1(g1.y, u1.y);
+      a[6] = silu_mul_1(g1.z, u1.z);
+      a[7] = silu_mul_1(g1.w, u1.w);
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = (c0 + i < inter) ? silu_mul_1(gr[c0 + i], gr[inter + c0 + i]) : 0.0f;
+      for (int i = 0; i < 8; ++i)
+        a[i] = (live && c0 + i < inter) ? silu_mul_1(gr[c0 + i], gr[inter + c0 + i]) : 0.0f;
     }
-    float amax = fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3])));
-    amax = warp_max(amax);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float sc = div_rn(amax, kE4M3Max);
-    uint32_t codes = 0;
+    uint32_t codes[2] = {0u, 0u};
     if (amax > 0.0f) {
-      codes = (uint32_t)f2_to_e4m3x2(div_rn(a[0], sc), div_rn(a[1], sc)) |
-              ((uint32_t)f2_to_e4m3x2(div_rn(a[2], sc), div_rn(a[3], sc)) << 16);
-    }
-    uint8_t* qr = q + row * inter;
-    if (kVec && full) {
-      *reinterpret_cast<uint32_t*>(qr + c0) = codes;
-    } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + i < inter) qr[c0 + i] = (uint8_t)(codes >> (8 * i));
+      for (int h = 0; h < 2; ++h)
+        codes[h] = (uint32_t)f2_to_e4m3x2(div_rn(a[4 * h], sc), div_rn(a[4 * h + 1], sc)) |
+                   ((uint32_t)f2_to_e4m3x2(div_rn(a[4 * h + 2], sc), div_rn(a[4 * h + 3], sc)) << 16);
     }
-    if (lane == 0) s[row * ng + g] = sc;
+    if (live) {
+      uint8_t* qr = q + row * inter;
+      if (kVec && full) {
+        *reinterpret_cast<uint32_t*>(qr + c0) = codes[0];
+        *reinterpret_cast<uint32_t*>(qr + c0 + 4) = codes[1];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c0 + i < inter) qr[c0 + i] = (uint8_t)(codes[i >> 2] >> (8 * (i & 3)));
+      }
+      if (hl == 0) s[row * ng + g] = sc;
+    }
   }
 }
 
@@ -77,7 +96,7 @@ cudaError_t launch_silu_mul_fp8(const float* gu, int64_t rows, int64_t inter, in
   const int64_t ng = cdiv(inter, kGroup);
   const bool vec = (ld_gu % 4 == 0) && (inter % 4 == 0) && ((uintptr_t)gu % 16 == 0) &&
                    ((uintptr_t)q % 4 == 0);
-  const int grid = grid_cap(cdiv(rows * ng, 8));
+  const int grid = grid_cap(cdiv(rows * ng, 16));
   return launch_kernel(vec ? silu_mul_fp8_kernel<true> : silu_mul_fp8_kernel<false>, dim3(grid), dim3(256), 0, st,
                        true, gu, rows, inter, ld_gu, rows_dev, q, scales, ng);
 }

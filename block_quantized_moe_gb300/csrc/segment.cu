@@ -1,10 +1,12 @@
 // Expert segmenter: per-expert row counts and offsets, the dst2src map the gather walks
 // ("m * topk entries", SGLang gather page, Motivation) and route2dst for the combine.
 //
-// One CTA per expert e. The routes are walked in chunks of the block size, one id per
-// thread, so route order inside an expert (stability) follows from an exclusive scan of
-// the matches in each chunk. The CTA also counts the active routes of lower experts for
-// its own offset. No atomics: every output is a deterministic function of expert_ids.
+// One CTA per expert e. Each warp of the CTA owns a contiguous range of routes and walks it
+// 32 ids at a time (coalesced); a ballot and a population count give each matching route
+// its place inside the warp's range, and one scan of the warps' totals gives each range its
+// first row, so rows follow route order (stability). The CTA also counts the active routes
+// of lower experts for its own offset. No atomics: every output is a deterministic function
+// of expert_ids.
 #include "common.cuh"
 #include "internal.h"
 #include "rowquant.cuh"
@@ -13,72 +15,63 @@ namespace ftmoe {
 
 constexpr int kSegThreads = 512;
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sh /*[32]*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) sh[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
-    }
-    sh[lane] = wi - w;  // exclusive prefix of warp totals
-    if (lane == 31) sh[32] = wi;
-  }
-  __syncthreads();
-  const int res = sh[warp] + inc - v;
-  *total = sh[32];
-  __syncthreads();
-  return res;
-}
-
-// Segments of expert e, by one CTA of kSegThreads threads. Pass 1 counts the active
-// routes of lower experts (this expert's offset) and of this expert; pass 2 walks the
-// routes in chunks of blockDim.x, one coalesced id per thread, and gives each matching
-// route its row by an exclusive scan of the chunk, so rows follow route order.
+// Segments of expert e, by one CTA of kSegThreads threads (sh: 2 * kSegThreads / 32 ints).
+// Pass 1: every warp counts, over its own range, the active routes of lower experts and
+// the routes of expert e. The warps' counts are combined once. Pass 2: every warp walks its
+// range again and writes its matches from its first row on.
 __device__ __forceinline__ void segment_expert(const int32_t* __restrict__ ids, int64_t routes, int32_t topk,
                                                int32_t E, int32_t* __restrict__ counts,
                                                int32_t* __restrict__ offsets, int32_t* __restrict__ dst2src,
                                                int32_t* __restrict__ route2dst, int e, int* sh) {
+  constexpr int kWarps = kSegThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the warp's range [r0, r1), a whole number of 32-id steps
+  const int64_t span = ((routes + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int64_t r0 = span * warp;
+  const int64_t r1 = r0 + span < routes ? r0 + span : routes;
   int below = 0, mine = 0;
-  for (int64_t r = threadIdx.x; r < routes; r += blockDim.x) {
+  for (int64_t r = r0 + lane; r < r1; r += 32) {
     const int id = ids[r];
     below += (id >= 0 && id < e);
     mine += (id == e);
     if (e == 0 && id >= E) raise_error(FTMOE_ERR_EXPERT_ID_RANGE);
   }
-  int below_total, mine_total;
-  (void)block_exclusive_scan(below, &below_total, sh);
-  (void)block_exclusive_scan(mine, &mine_total, sh);
-  const int off = below_total;
-  if (threadIdx.x == 0) {
-    counts[e] = mine_total;
-    offsets[e] = off;
-    if (e == E - 1) offsets[E] = off + mine_total;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    below += __shfl_xor_sync(0xffffffffu, below, o);
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
   }
-  int base = off;
-  for (int64_t c0 = 0; c0 < routes; c0 += blockDim.x) {
-    const int64_t r = c0 + threadIdx.x;
-    const int id = r < routes ? ids[r] : -1;
-    int chunk_total;
-    const int pos = block_exclusive_scan(id == e ? 1 : 0, &chunk_total, sh);
+  if (lane == 0) {
+    sh[warp] = mine;
+    sh[kWarps + warp] = below;
+  }
+  __syncthreads();
+  int first = 0, off = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    first += w < warp ? sh[w] : 0;
+    total += sh[w];
+    off += sh[kWarps + w];
+  }
+  if (threadIdx.x == 0) {
+    counts[e] = total;
+    offsets[e] = off;
+    if (e == E - 1) offsets[E] = off + total;
+  }
+  int base = off + first;
+  const uint32_t lower = (1u << lane) - 1u;
+  for (int64_t c0 = r0; c0 < r1; c0 += 32) {
+    const int64_t r = c0 + lane;
+    const int id = r < r1 ? ids[r] : -1;
+    const uint32_t m = __ballot_sync(0xffffffffu, id == e);
     if (id == e) {
-      const int d = base + pos;
+      const int d = base + __popc(m & lower);
       dst2src[d] = (int32_t)(r / topk);
       route2dst[r] = d;
-    } else if (e == 0 && r < routes && (id < 0 || id >= E)) {
+    } else if (e == 0 && r < r1 && (id < 0 || id >= E)) {
       route2dst[r] = -1;  // inactive (or out-of-range, reported above) routes
     }
-    base += chunk_total;
+    base += __popc(m);
   }
 }
 
@@ -88,7 +81,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(
     int32_t* __restrict__ route2dst) {
   pdl_wait();  // the predecessor's outputs are complete from here on
   pdl_trigger();
-  __shared__ int sh[33];
+  __shared__ int sh[2 * (kSegThreads / 32)];
   segment_expert(ids, routes, topk, E, counts, offsets, dst2src, route2dst, blockIdx.x, sh);
 }
 
@@ -104,7 +97,7 @@ __global__ void __launch_bounds__(kSegThreads) prep_fp8_kernel(
     int32_t* __restrict__ route2dst) {
   pdl_wait();  // the predecessor's outputs are complete from here on
   pdl_trigger();
-  __shared__ int sh[33];
+  __shared__ int sh[2 * (kSegThreads / 32)];
   if ((int)blockIdx.x < E) {
     segment_expert(ids, routes, topk, E, counts, offsets, dst2src, route2dst, (int)blockIdx.x, sh);
   } else {

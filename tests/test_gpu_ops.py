@@ -72,7 +72,8 @@ def test_quantize_weights_fp8_bitexact(ft, E, n, k):
 # -- segmenter -----------------------------------------------------------------------
 
 @pytest.mark.parametrize("T,k,E,inactive", [(1, 8, 8, 6), (8, 8, 64, 4), (256, 6, 256, 0),
-                                            (4096, 6, 256, 0), (33, 4, 5, 1), (16, 8, 64, 8)])
+                                            (4096, 6, 256, 0), (33, 4, 5, 1), (16, 8, 64, 8),
+                                            (1000, 7, 9, 2), (8192, 8, 12, 0)])
 def test_segment_bitexact(ft, T, k, E, inactive):
     if T * k > 2048:
         ids = synth.routes_fast(T, k, E, 5 + T, DEV)
@@ -152,7 +153,7 @@ def _e4m3_step(mag):
     return 2.0 ** (e - 3)
 
 
-@pytest.mark.parametrize("rows,inter", [(64, 1024), (7, 200), (8, 768)])
+@pytest.mark.parametrize("rows,inter", [(64, 1024), (7, 200), (8, 768), (5, 132), (3, 384)])
 def test_silu_mul_fp8(ft, rows, inter):
     g = torch.randn(rows, 2 * inter, generator=torch.Generator().manual_seed(rows + inter)) * 3
     g[0] = 0  # an inactive route's zero row
