@@ -68,6 +68,7 @@ WORKLOADS = {
     "prefill-fp8-h7168-i2048-e256-r1536-sep": (256, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r6144-sep": (1024, 7168, 2048, 256, 6, 6, 2),
     "prefill-fp8-h7168-i2048-e256-r24576-sep": (4096, 7168, 2048, 256, 6, 6, 2),
+    "prefill-fp8-h7168-i2048-e256-r24576-comb": (4096, 7168, 2048, 256, 6, 6, 5),
     # a 32-expert bank with the same rows per expert (96) as the 24,576-route case: small
     # enough (1.4 GB of weights) for multi-pass profiler captures
     "prefill-fp8-h7168-i2048-e32-r3072": (512, 7168, 2048, 32, 6, 6, 0),
@@ -403,6 +404,8 @@ class MoeWorkload:
         self.decode = lay["partials_bytes"] > 0  # the fused decode kernel (path 4)
         self.grouped = path != 1 and not self.decode
         self.fused = self.grouped and lay["gateup_bytes"] == 0
+        # the combine inside the down GEMM (arrival counters in the workspace, no combine launch)
+        self.comb = self.grouped and lay["counters_bytes"] > 0
         self.ws = torch.empty(ft.ftmoe_forward_workspace_bytes(self.shape), dtype=torch.uint8, device=device)
         self.x_in = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.ids_in = torch.empty(T, k, dtype=torch.int32, device=device)
@@ -412,7 +415,7 @@ class MoeWorkload:
         # FP8 on the grouped path quantizes and segments in one launch, and the fused path has
         # no SiLU-and-mul launch; each NVFP4 quantizer adds an amax pass and the tensor-scale
         # conversion; MXFP8 quantizes inside the gather (no quantizing launch)
-        self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) -
+        self.launches_per_step = ((5 if path == 1 else 7) - (1 if self.fused else 0) - (1 if self.comb else 0) -
                                   (1 if self.grouped and self.fmt in ("fp8", "mxfp8") else 0) +
                                   (4 if self.fmt == "nvfp4" else 0))
         if self.decode:
@@ -448,10 +451,15 @@ class MoeWorkload:
         else:
             gateup = uniq * w_gu + (ra if self.grouped else T) * row(H) + out_rows * 2 * I * 4
             silu = out_rows * 2 * I * 4 + out_rows * row(I)
-        down = uniq * w_dn + out_rows * row(I) + out_rows * H * 4
-        total = (gateup + silu
-                 + down
-                 + ra * H * 4 + T * k * 8 + T * H * 2)             # combine
+        if self.comb:
+            # the combine inside the down GEMM: the fp32 rows need not leave L2 (each is
+            # written once and read once, within the same block-pair span of the GEMM)
+            down = uniq * w_dn + out_rows * row(I)
+            comb = T * k * 8 + T * H * 2
+        else:
+            down = uniq * w_dn + out_rows * row(I) + out_rows * H * 4
+            comb = ra * H * 4 + T * k * 8 + T * H * 2
+        total = gateup + silu + down + comb
         if f == "nvfp4":
             total += T * H * 2 + out_rows * 2 * I * 4              # amax passes of the tensor scales
         if f == "mxfp8":
@@ -718,8 +726,9 @@ def run_gpu(args, rank, world, local):
                    "topk": wl.k, "active_routes_per_token": wl.active, "route_sets_rotated": wl.NSETS,
                    "forward_path": ("fused decode kernel (one launch after quantization)" if wl.decode else
                                     "route slots (streaming kernel)" if not wl.grouped else
-                                    "grouped, SiLU-and-mul fused into the gate/up GEMM" if wl.fused else
-                                    "grouped, separate SiLU-and-mul kernel"),
+                                    ("grouped, SiLU-and-mul fused into the gate/up GEMM" if wl.fused else
+                                     "grouped, separate SiLU-and-mul kernel") +
+                                    (", combine inside the down GEMM" if wl.comb else "")),
                    "l2": L2Flush.DESC, "parallelism": f"replicas x{world}",
                    "graph": ("direct launches (--eager)" if args.eager else
                              "one CUDA graph replayed; inputs copied in place between steps")},

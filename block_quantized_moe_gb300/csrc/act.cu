@@ -195,28 +195,7 @@ cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, 
 }
 
 // ---- combine: out[t, h] = round( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
-// Output element types: bf16 and fp16 (one round to nearest even of the fp32 sum) or fp32.
-struct OutBf16 {
-  using T = uint16_t;
-  static __device__ __forceinline__ uint16_t cvt(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
-};
-struct OutF16 {
-  using T = uint16_t;
-  static __device__ __forceinline__ uint16_t cvt(float v) { return __half_as_ushort(__float2half_rn(v)); }
-};
-struct OutF32 {
-  using T = float;
-  static __device__ __forceinline__ float cvt(float v) { return v; }
-};
-
-// four outputs of one row, one vector store when aligned
-__device__ __forceinline__ void store4(uint16_t* o, const uint16_t* b) {
-  *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
-}
-__device__ __forceinline__ void store4(float* o, const float* b) {
-  *reinterpret_cast<float4*>(o) = make_float4(b[0], b[1], b[2], b[3]);
-}
-
+// (output conversions OutBf16 / OutF16 / OutF32 and store4: common.cuh)
 // The slot ids, weights and rows of a token are loaded eight slots at a time with
 // independent loads, then accumulated in ascending slot order.
 template <bool kVec, typename Out>

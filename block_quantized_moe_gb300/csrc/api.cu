@@ -258,10 +258,49 @@ ftmoe_status gateup_silu(const ftmoe_act* a, const ftmoe_routes* routes, const f
   return from_cuda(e);
 }
 
+// The forward's down GEMM with the combine inside (tok_tile 64 or 128, CTA pairs): y keeps
+// the rows only until each token's last route has been added; out receives the combined rows
+// of every token with an active route (the prep launch wrote the others and zeroed cnt).
+ftmoe_status down_comb(const ftmoe_act* a, const int32_t* offsets, const ftmoe_expert_bank* w, float* y,
+                       int32_t tok_tile, const int32_t* dst2src, const int32_t* route2dst, const float* rw,
+                       int32_t topk, uint32_t* cnt, void* out, int64_t ld_out, int32_t out_dtype, void* stream) {
+  if (a->rows == 0) return FTMOE_OK;
+  TcGemmArgs t;
+  memset(&t, 0, sizeof(t));
+  t.a_q = a->q;
+  t.a_s = static_cast<const float*>(a->scales);
+  t.a_rows = a->rows;
+  t.w_q = w->q;
+  t.w_s = static_cast<const float*>(w->scales);
+  t.out = y;
+  t.ld_out = w->n;
+  t.n = w->n;
+  t.k = w->k;
+  t.E = w->num_experts;
+  t.offsets = offsets;
+  t.tok_tile = tok_tile;
+  t.wblocks = 1;
+  t.ctas = 2;
+  t.comb = 1;
+  t.dst2src = dst2src;
+  t.route2dst = route2dst;
+  t.rw = rw;
+  t.cnt = cnt;
+  t.out_c = out;
+  t.ld_c = ld_out;
+  t.topk = topk;
+  t.out_dtype = out_dtype;
+  int unsupported = 0;
+  cudaError_t e = launch_tc_gemm(t, as_stream(stream), &unsupported);
+  if (unsupported) return FTMOE_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 struct Layout {
   ftmoe_workspace_layout l;
   bool grouped;
   bool fused;   // SiLU-and-mul inside the gate/up GEMM: no fp32 gate/up buffer
+  bool comb;    // the combine inside the down GEMM (CTA pairs), when the output rows allow
   bool decode;  // the fused decode path (prep launch + one persistent kernel)
   DecodePlan plan;
 };
@@ -270,7 +309,7 @@ ftmoe_status check_shape(const ftmoe_moe_shape* s) {
   if (!s) return FTMOE_INVALID_ARG;
   if (s->tokens < 0 || s->hidden <= 0 || s->inter <= 0 || s->topk <= 0 || s->num_experts <= 0)
     return FTMOE_INVALID_ARG;
-  if (!valid_format(s->format) || s->path < 0 || s->path > 4 || !valid_out_dtype(s->out_dtype))
+  if (!valid_format(s->format) || s->path < 0 || s->path > 5 || !valid_out_dtype(s->out_dtype))
     return FTMOE_INVALID_ARG;
   if (s->tok_tile != 0 && s->tok_tile != 16 && s->tok_tile != 32 && s->tok_tile != 64 && s->tok_tile != 128)
     return FTMOE_INVALID_ARG;
@@ -317,6 +356,21 @@ bool use_fused(const ftmoe_moe_shape* s) {
   return experts * (s->inter / 128) >= kFusedMinUnits;
 }
 
+// When the down GEMM adds up each token's rows itself: path 5 only. Measured on GB300 at
+// 24,576 routes (4,096 tokens, 7168/2048, 256 experts), the forward took 6217 us with the
+// combine inside against 2615 us with the combine kernel. The combine warps' work per unit is
+// a chain of round trips to memory (the arrival counters' atomics, then each completed
+// token's rows), and with the weight stream holding HBM near its bandwidth each round trip
+// waits microseconds: without the atomics the forward took 3457 us, without the row loads
+// 3852 us, and without any combine work (no output) 2564 us -- so at most about 2% was to
+// be won. The automatic path keeps the combine kernel.
+bool use_comb(const ftmoe_moe_shape* s) {
+  if (s->path != 5 || s->format != FTMOE_FMT_FP8 || s->num_experts > kTcGemmMaxExperts) return false;
+  if (!tc_gemm_pairs_ok(s->hidden, s->inter)) return false;
+  const int tile = s->tok_tile ? s->tok_tile : pick_tile_value(s->tokens * s->topk, s->num_experts);
+  return tile == 64 || tile == 128;
+}
+
 Layout make_layout(const ftmoe_moe_shape* s) {
   Layout L;
   memset(&L, 0, sizeof(L));
@@ -350,6 +404,7 @@ Layout make_layout(const ftmoe_moe_shape* s) {
   }
   L.grouped = use_grouped(s);
   L.fused = L.grouped && use_fused(s);
+  L.comb = L.grouped && use_comb(s);
   // (MXFP8 quantizes the gathered rows: no quantized token rows)
   L.l.x_q = take(f == FTMOE_FMT_MXFP8 ? 0 : T * code_row_bytes(f, H));
   L.l.x_scales = take(f == FTMOE_FMT_MXFP8 ? 0 : T * scale_row_bytes(f, H));
@@ -373,6 +428,11 @@ Layout make_layout(const ftmoe_moe_shape* s) {
   L.l.act_gscale = take(16);
   L.l.down_bytes = (size_t)R * H * 4;
   L.l.down = take(L.l.down_bytes);
+  if (L.comb) {
+    // arrival counters of the fused combine, one per (token, 128-column block of H)
+    L.l.counters_bytes = (size_t)T * (H / 128) * 4;
+    L.l.counters = take(L.l.counters_bytes);
+  }
   L.l.total = off;
   return L;
 }
@@ -587,6 +647,20 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   // FP8 on the grouped path: quantization and the segmenter share the first launch
   const bool prep = L.grouped && f == FTMOE_FMT_FP8;
   if (prep && R > 0x7fffffff) return FTMOE_UNSUPPORTED;
+  // the combine inside the down GEMM where the layout has it and the output rows allow
+  const bool comb = L.comb && tc_gemm_comb_ok(tile.tok_tile, H, I, y, H, args->out, args->ld_out);
+  if (s->path == 5 && !comb) return FTMOE_UNSUPPORTED;
+  uint32_t* comb_cnt = comb ? reinterpret_cast<uint32_t*>(ws + L.l.counters) : nullptr;
+  PrepCombine pc;
+  memset(&pc, 0, sizeof(pc));
+  if (comb) {
+    pc.zero_words = comb_cnt;
+    pc.n_zero_words = T * (H / 128);
+    pc.out_rows = args->out;
+    pc.ld_out = args->ld_out;
+    pc.out_bytes = s->out_dtype == FTMOE_OUT_FP32 ? 4 : 2;
+    pc.hidden = H;
+  }
 
   OverlapScope overlap;
   if (L.decode) {
@@ -629,7 +703,7 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   const bool mx = f == FTMOE_FMT_MXFP8;
   if (prep)
     st = from_cuda(launch_prep_fp8(args->x, T, H, args->ld_x, xq, static_cast<float*>(xs), args->expert_ids, R,
-                                   s->topk, (int32_t)E, counts, offsets, dst2src, route2dst, strm));
+                                   s->topk, (int32_t)E, counts, offsets, dst2src, route2dst, pc, strm));
   else if (mx)
     st = ftmoe_segment_routes(args->expert_ids, T, s->topk, (int32_t)E, counts, offsets, dst2src, route2dst,
                               stream);
@@ -682,6 +756,9 @@ ftmoe_status ftmoe_moe_forward(const ftmoe_moe_args* args, void* workspace, size
   }
   if (st != FTMOE_OK) return st;
   ftmoe_act a2 = {f, 0, R, I, aq, as, ag};
+  if (comb)
+    return down_comb(&a2, offsets, &wd, y, tile.tok_tile, dst2src, route2dst, args->route_weights, s->topk, comb_cnt,
+                     args->out, args->ld_out, s->out_dtype, stream);
   st = ftmoe_grouped_gemm_down(&a2, &rt, &wd, y, H, &tile, stream);
   if (st != FTMOE_OK) return st;
   return ftmoe_combine(y, H, route2dst, args->expert_ids, args->route_weights, T, s->topk, H, s->out_dtype,

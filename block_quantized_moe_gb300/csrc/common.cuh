@@ -97,6 +97,29 @@ __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, 
 // separate kernel and the gate/up GEMM epilogue give bit-identical results).
 __device__ __forceinline__ float silu_mul_1(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Output element types of the combine: bf16 and fp16 (one round to nearest even of the fp32
+// sum) or fp32. The separate combine kernel and the down GEMM's fused combine both use these.
+struct OutBf16 {
+  using T = uint16_t;
+  static __device__ __forceinline__ uint16_t cvt(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+};
+struct OutF16 {
+  using T = uint16_t;
+  static __device__ __forceinline__ uint16_t cvt(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
+struct OutF32 {
+  using T = float;
+  static __device__ __forceinline__ float cvt(float v) { return v; }
+};
+
+// four outputs of one row, one vector store (8-byte aligned for 16-bit outputs, 16-byte for fp32)
+__device__ __forceinline__ void store4(uint16_t* o, const uint16_t* b) {
+  *reinterpret_cast<uint2*>(o) = make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+}
+__device__ __forceinline__ void store4(float* o, const float* b) {
+  *reinterpret_cast<float4*>(o) = make_float4(b[0], b[1], b[2], b[3]);
+}
+
 // Positive floats order like their bit patterns, so a max over |x| can use atomicMax on
 // the bits of a zero-initialised word.
 __device__ __forceinline__ void atomic_max_pos(float* addr, float v) {

@@ -114,10 +114,23 @@ uint32_t read_err_quant();
 cudaError_t launch_segment(const int32_t* ids, int64_t routes, int32_t topk, int32_t E,
                            int32_t* counts, int32_t* offsets, int32_t* dst2src,
                            int32_t* route2dst, cudaStream_t s);
-// the fused forward's first kernel: FP8 quantization of x and the segmenter in one grid
+// the fused forward's first kernel: FP8 quantization of x and the segmenter in one grid.
+// For the down GEMM's fused combine it also
+// zeroes the arrival counters (zero_words words, may be NULL) and writes a zero output row
+// for every token without an active route (out_rows: [rows][ld_out] elements of out_bytes
+// bytes, hidden of them per row; NULL when the combine runs as its own kernel).
+struct PrepCombine {
+  uint32_t* zero_words;
+  int64_t n_zero_words;
+  void* out_rows;
+  int64_t ld_out;
+  int32_t out_bytes;
+  int64_t hidden;
+};
 cudaError_t launch_prep_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* q, float* scales,
                             const int32_t* ids, int64_t routes, int32_t topk, int32_t E, int32_t* counts,
-                            int32_t* offsets, int32_t* dst2src, int32_t* route2dst, cudaStream_t s);
+                            int32_t* offsets, int32_t* dst2src, int32_t* route2dst, const PrepCombine& pc,
+                            cudaStream_t s);
 uint32_t read_err_segment();
 
 // gather.cu
@@ -168,9 +181,23 @@ struct TcGemmArgs {
   int32_t silu;            // 1: gate block j + up block j per unit, SiLU-and-mul + FP8 requant
   uint8_t* q_out;          // silu: codes [a_rows][n/2]
   float* s_out;            // silu: scales [a_rows][n/256]
+  // comb (CTA pair only): the routing-weighted combine of the rows into out_c inside the
+  // GEMM; out keeps the rows only until they are combined (their L2 lines are dropped)
+  int32_t comb;
+  const int32_t* dst2src;    // grouped row -> token
+  const int32_t* route2dst;  // route -> grouped row or -1
+  const float* rw;           // routing weights [tokens][topk]
+  uint32_t* cnt;             // [tokens][ceil(n/128)] zero-initialised arrival counters
+  void* out_c;               // [tokens][ld_c] of out_dtype
+  int64_t ld_c;
+  int32_t topk, out_dtype;
 };
 // whether an n x k weight matrix can run two weight blocks per unit (n % 256, k % 128)
 bool tc_gemm_pairs_ok(int64_t n, int64_t k);
+// whether the down GEMM with these buffers can run with the combine inside (CTA pair at
+// token tile 64 or 128, whole block pairs, 128-byte aligned rows of y, 16-byte aligned output rows)
+bool tc_gemm_comb_ok(int tok_tile, int64_t n, int64_t k, const void* y, int64_t ld_y, const void* out_c,
+                     int64_t ld_c);
 // largest expert count the tensor-core GEMM's unit table holds (tc::kMaxExperts in
 // tc_gemm.cu, which refuses larger banks as unsupported)
 constexpr int32_t kTcGemmMaxExperts = 1024;

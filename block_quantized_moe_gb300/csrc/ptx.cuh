@@ -136,6 +136,25 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// ---- global memory between CTAs of the grid (the down GEMM's fused combine) ----
+
+// A gpu-scope fence: with a relaxed atomic after it, it publishes everything this thread has
+// written or observed (through a CTA-scope barrier) to the threads that acquire the atomic's
+// value; after an atomic that read another CTA's value, it makes that CTA's published writes
+// visible to this thread's later loads.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// fp32 store with an L2 eviction-priority hint
+__device__ __forceinline__ void st_global_hint(float* p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+
+// The 128-byte L2 line at p (128-byte aligned) is dropped without being written back: its
+// data is dead (read once, by the caller, before this).
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
                                                  uint64_t policy) {
   asm volatile(

@@ -88,13 +88,15 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(
 // The fused forward's first launch: FP8 quantization of the token rows and the expert
 // segmenter are independent steps, so one grid runs both -- blocks [0, E) segment one
 // expert each (first, as they take longest), blocks [E, E + qblocks) quantize (one warp
-// per 1x128 group).
+// per 1x128 group). With the down GEMM's fused combine the quantizing blocks also zero its
+// arrival counters and write the zero output rows of tokens that have no active route (the
+// combine inside the GEMM only reaches tokens with at least one).
 template <bool kVec>
 __global__ void __launch_bounds__(kSegThreads) prep_fp8_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* __restrict__ q,
     float* __restrict__ s, int64_t ng, int qblocks, const int32_t* __restrict__ ids, int64_t routes, int32_t topk,
     int32_t E, int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ dst2src,
-    int32_t* __restrict__ route2dst) {
+    int32_t* __restrict__ route2dst, PrepCombine pc) {
   pdl_wait();  // the predecessor's outputs are complete from here on
   pdl_trigger();
   __shared__ int sh[2 * (kSegThreads / 32)];
@@ -104,9 +106,28 @@ __global__ void __launch_bounds__(kSegThreads) prep_fp8_kernel(
     const int qb = (int)blockIdx.x - E;
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)qblocks * (blockDim.x >> 5);
-    for (int64_t w = (int64_t)qb * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows * ng; w += nwarps) {
+    const int64_t gwarp = (int64_t)qb * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int64_t w = gwarp; w < rows * ng; w += nwarps) {
       const int64_t row = w / ng, g = w - row * ng;
       quantize_fp8_group<kVec>(x, k, ld_x, q, s, ng, row, g, lane);
+    }
+    if (pc.zero_words != nullptr) {
+      for (int64_t i = gwarp * 32 + lane; i < pc.n_zero_words; i += nwarps * 32) pc.zero_words[i] = 0u;
+    }
+    if (pc.out_rows != nullptr) {
+      // (rows of hidden * out_bytes bytes, a multiple of 16, at 16-byte aligned starts)
+      const int64_t row_bytes = pc.hidden * pc.out_bytes, ld_bytes = pc.ld_out * pc.out_bytes;
+      for (int64_t t = gwarp; t < rows; t += nwarps) {
+        bool any = false;
+        for (int64_t j = lane; j < topk; j += 32) {
+          const int id = ids[t * topk + j];
+          any = any || (id >= 0 && id < E);
+        }
+        if (__any_sync(0xffffffffu, any)) continue;
+        uint8_t* o = static_cast<uint8_t*>(pc.out_rows) + t * ld_bytes;
+        for (int64_t b = (int64_t)lane * 16; b < row_bytes; b += 32 * 16)
+          *reinterpret_cast<uint4*>(o + b) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 }
@@ -120,7 +141,8 @@ cudaError_t launch_segment(const int32_t* ids, int64_t routes, int32_t topk, int
 
 cudaError_t launch_prep_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* q, float* scales,
                             const int32_t* ids, int64_t routes, int32_t topk, int32_t E, int32_t* counts,
-                            int32_t* offsets, int32_t* dst2src, int32_t* route2dst, cudaStream_t st) {
+                            int32_t* offsets, int32_t* dst2src, int32_t* route2dst, const PrepCombine& pc,
+                            cudaStream_t st) {
   const int64_t ng = cdiv(k, kGroup);
   const int64_t warps = rows * ng;
   int64_t qb = cdiv(warps, kSegThreads / 32);
@@ -129,7 +151,7 @@ cudaError_t launch_prep_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t 
   const bool vec = quantize_fp8_vec_ok(x, ld_x, q, k);
   return launch_kernel(vec ? prep_fp8_kernel<true> : prep_fp8_kernel<false>, dim3((unsigned)qb + E),
                        dim3(kSegThreads), 0, st, true, x, rows, k, ld_x, q, scales, ng, (int)qb, ids, routes, topk, E,
-                       counts, offsets, dst2src, route2dst);
+                       counts, offsets, dst2src, route2dst, pc);
 }
 
 FTMOE_DEFINE_ERR_READER(read_err_segment)

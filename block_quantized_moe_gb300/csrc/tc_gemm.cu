@@ -60,12 +60,17 @@ constexpr int kMaxExperts = 1024;
 //               first CTA issues tcgen05.mma.cta_group::2 with M = 256, which reads the
 //               weights and the token halves of both CTAs and leaves each CTA the fp32
 //               accumulator of its own block over all TT token columns
+//   kCtaPairComb  kCtaPair for the down GEMM of the forward, with the routing-weighted
+//               combine inside: four more warps publish each unit's fp32 rows, count the
+//               arrivals per (token, weight block) and, for a token whose last route arrived,
+//               add its rows in ascending slot order into the output (see "Fused combine")
 // Two weight blocks per token tile halve the token bytes each stage carries for every
 // weight byte, so more weight bytes fit in flight in the same shared memory. kPair does it
 // on one SM (twice the epilogue work per K block); kCtaPair across two, with the epilogue
 // work of one block per SM.
-enum Mode { kSingle = 0, kPair = 1, kGateUpSilu = 2, kCtaPair = 3 };
+enum Mode { kSingle = 0, kPair = 1, kGateUpSilu = 2, kCtaPair = 3, kCtaPairComb = 4 };
 __host__ __device__ constexpr int wb_of(int mode) { return mode == kPair || mode == kGateUpSilu ? 2 : 1; }
+__host__ __device__ constexpr bool is_cp(int mode) { return mode == kCtaPair || mode == kCtaPairComb; }
 
 // TMEM accumulators in rotation: as many (weight blocks x TT)-column accumulators as 512
 // columns hold, at most 16, so the MMA can run that many K blocks ahead of the promotion
@@ -107,6 +112,14 @@ struct Params {
   float* s_out;       // kGateUpSilu: group scales [a_rows][n / 256]
   int64_t a_rows;
   int n, k, E, kb_count, nb_count, stages;
+  // kCtaPairComb: the combine out_c[t, :] = round(sum_j rw[t*topk + j] * out[route2dst[t*topk + j], :])
+  const int32_t* dst2src;    // grouped row -> token
+  const int32_t* route2dst;  // route -> grouped row, -1 for a route without one
+  const float* rw;           // routing weights [tokens][topk]
+  uint32_t* cnt;             // [tokens][nb_count] arrival counters, zero at launch
+  void* out_c;               // [tokens][ld_c] elements of out_dtype
+  int64_t ld_c;
+  int topk, out_dtype;
 };
 
 constexpr int kEpiWarps = 16;                    // 4 column groups x 4 TMEM lane quarters
@@ -114,6 +127,8 @@ constexpr int kGroups = kEpiWarps / 4;
 constexpr int kMaxKB = 128;                      // K <= 16384
 constexpr int kMaxStages = 12;
 constexpr int kSaChunk = 8;                      // K blocks of activation scales staged at once
+constexpr int kYRing = 4;                        // fused combine: units in flight between the roles
+constexpr int kCombK = 8;                        // fused combine: slots a token's last arrival stages
 
 // K blocks per pipeline stage (KBS). One TMA box brings all of them: the tensor maps carry
 // the K-block index as a dimension of its own, and each K block lands as its own canonical
@@ -126,7 +141,7 @@ constexpr int kSaChunk = 8;                      // K blocks of activation scale
 // multiple of 128 keeps one K block per stage and the per-row maps, whose x extent is K
 // itself, so the partial last block is zero-filled rather than read past the row.
 __host__ __device__ constexpr int kbs_for(int tt, int mode) {
-  return mode == kSingle ? (tt <= 64 ? 4 : 2) : (mode == kCtaPair ? 4 : (tt <= 32 ? 2 : 1));
+  return mode == kSingle ? (tt <= 64 ? 4 : 2) : (is_cp(mode) ? 4 : (tt <= 32 ? 2 : 1));
 }
 
 // Warp roles. Warp 0 issues TMA, warp 1 issues MMAs, the last kEpiWarps warps promote.
@@ -134,22 +149,27 @@ __host__ __device__ constexpr int kbs_for(int tt, int mode) {
 // or 64) per epilogue thread. Those kernels add two idle warps, so that warps 0-3 form a
 // warpgroup that gives registers back (setmaxnreg.dec to kCtlRegs) to the four epilogue
 // warpgroups (setmaxnreg.inc to kEpiRegs). The launch pool is threads x the kernel's
-// register count; the host checks kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps against it
+// register count; the host checks the warpgroups' shares (W::kRegsNeeded) against it
 // before launching, since an increase the pool cannot cover would never complete.
+// The fused-combine kernel (kCtaPairComb) has a second control warpgroup, the four combine
+// warps, and splits registers the same way: 768 threads launch with 80 registers each; both
+// control warpgroups keep 64, the epilogue takes 88 (its 32 accumulators and 16 TMEM
+// columns in flight fit without spilling).
 template <int TT, int MODE>
 struct Warps {
-  static constexpr bool kSplitRegs = TT >= 64 && wb_of(MODE) == 2;
-  static constexpr int kCtl = 4;  // TMA, MMA, scale-product tables, one idle warp
+  static constexpr bool kComb = MODE == kCtaPairComb;
+  static constexpr bool kSplitRegs = (TT >= 64 && wb_of(MODE) == 2) || kComb;
+  static constexpr int kCtl = kComb ? 8 : 4;  // TMA, MMA, scale-product tables, one idle warp (+ 4 combine)
   static constexpr int kThreads = 32 * (kCtl + kEpiWarps);
-  static constexpr int kCtlRegs = 64, kEpiRegs = 104;
-  static constexpr int kRegsNeeded = kCtlRegs * 128 + kEpiRegs * 32 * kEpiWarps;
+  static constexpr int kCtlRegs = 64, kEpiRegs = kComb ? 88 : 104, kCombRegs = 64;
+  static constexpr int kRegsNeeded = kCtlRegs * 128 + (kComb ? kCombRegs * 128 : 0) + kEpiRegs * 32 * kEpiWarps;
 };
 
 template <int TT, int KBS, int MODE>
 struct Smem {
   static constexpr int kWB = wb_of(MODE);
   static constexpr int kSubW = kBM * kBK;     // 16 KiB: one K block of one weight block
-  static constexpr int kSubA = (MODE == kCtaPair ? TT / 2 : TT) * kBK;  // one K block of this CTA's tokens
+  static constexpr int kSubA = (is_cp(MODE) ? TT / 2 : TT) * kBK;  // one K block of this CTA's tokens
   static constexpr int kTileW = kSubW * KBS * kWB;
   static constexpr int kTileA = kSubA * KBS;
   static constexpr int kStage = kTileW + kTileA;
@@ -164,6 +184,9 @@ struct Smem {
   // quarter and group scales [kGroups][5][TT / kGroups]
   static constexpr int kProdBytes = 2 * kSaChunk * kWB * TT * 4;
   static constexpr int kRedBytes = MODE == kGateUpSilu ? 5 * TT * 4 : 0;
+  // fused combine: per combine warp and lane, the rows and weights of the token whose last
+  // route it counted [4][32][kCombK] each
+  static constexpr int kCombBytes = MODE == kCtaPairComb ? 4 * 32 * kCombK * 8 : 0;
 };
 
 // Dynamic shared memory: [stages][W tile | A tile] (1024-aligned), then the epilogue tables,
@@ -180,7 +203,9 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   uint8_t* tiles = smem;
   float* prod = reinterpret_cast<float*>(smem + (size_t)S * SM::kStage);
   float* red = prod + SM::kProdBytes / 4;
-  int* cum = reinterpret_cast<int*>(red + SM::kRedBytes / 4);  // [E+2] unit prefix
+  int* crow = reinterpret_cast<int*>(red + SM::kRedBytes / 4);  // (fused combine) [4][32][kCombK]
+  float* cwt = reinterpret_cast<float*>(crow + SM::kCombBytes / 8);  // [4][32][kCombK]
+  int* cum = reinterpret_cast<int*>(cwt + SM::kCombBytes / 8);  // [E+2] unit prefix
   int* seg_lo = cum + p.E + 2;                                   // [E] rows of expert e: [seg_lo, seg_hi)
   int* seg_hi = seg_lo + p.E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(((reinterpret_cast<uintptr_t>(seg_hi + p.E)) + 7) & ~(uintptr_t)7);
@@ -192,6 +217,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   uint64_t* tempty = bars + 2 * S + kAcc;
   uint64_t* pfull = tempty + kAcc;   // [2] a chunk's scale products are in place
   uint64_t* pempty = pfull + 2;      // [2] every epilogue warp is done with a chunk buffer
+  // (kCtaPairComb) a ring of kYRing unit slots: ydone[i] every epilogue warp has stored its
+  // rows of a unit; yfree[i] every combine warp has taken them over
+  uint64_t* ydone = pempty + 2;
+  uint64_t* yfree = ydone + kYRing;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -200,7 +229,8 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   const int NBU = MODE == kSingle ? NB : NB / 2;  // units per token tile
   // CTA pair: rank 0 issues the MMAs and owns the barriers that both CTAs' loads and
   // epilogues report to; rank 1 works on weight block 2p + 1 and token rows TT/2 ..
-  constexpr bool kCP = MODE == kCtaPair;
+  constexpr bool kCP = is_cp(MODE);
+  constexpr bool kComb = MODE == kCtaPairComb;
   const uint32_t crank = kCP ? cluster_rank() : 0u;
 
   if (threadIdx.x == 0) {
@@ -216,6 +246,12 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&pfull[i]), 32);         // every lane of the table warp
       mbar_init(smem_u32(&pempty[i]), kEpiWarps);
+    }
+    if constexpr (kComb) {
+      for (int i = 0; i < kYRing; ++i) {
+        mbar_init(smem_u32(&ydone[i]), kEpiWarps);  // this CTA's epilogue warps
+        mbar_init(smem_u32(&yfree[i]), 4);          // its combine warps
+      }
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -282,18 +318,28 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
   const int u_end = total_units;
   const int u_step = kCP ? (int)cluster_count_x() : (int)gridDim.x;
 
-  // unit -> (expert, weight block or block pair, token tile, first row, rows in tile)
+  // unit -> (expert, weight block or block pair, token tile, first row, rows in tile).
+  // The fused combine orders the list (block pair, expert, token tile), block pairs
+  // outermost: the CTAs then finish every route's rows of one block pair within a short
+  // span, while those rows are still in L2 for the token's last arrival to add up. (Measured
+  // on GB300 for the plain down GEMM at 24,576 routes, either order takes the same time.)
   auto decode = [&](int u, int& e, int& nb, int& tt, int& row0, int& rows) {
+    int key = u, nb_outer = 0;
+    if constexpr (kComb) {
+      const int tiles = total_units / NBU;  // every expert has NBU units per token tile
+      nb_outer = u / tiles;
+      key = (u - nb_outer * tiles) * NBU;
+    }
     int lo = 0, hi = E - 1;
-    while (lo < hi) {  // last e with cum[e] <= u
+    while (lo < hi) {  // last e with cum[e] <= key
       const int mid = (lo + hi + 1) >> 1;
-      if (cum[mid] <= u) lo = mid; else hi = mid - 1;
+      if (cum[mid] <= key) lo = mid; else hi = mid - 1;
     }
     e = lo;
     const int s0 = seg_lo[e], s1 = seg_hi[e];
-    const int local = u - cum[e];
+    const int local = key - cum[e];
     tt = local / NBU;
-    nb = local - tt * NBU;
+    nb = kComb ? nb_outer : local - tt * NBU;
     row0 = s0 + tt * TT;
     rows = min(TT, s1 - row0);
   };
@@ -304,7 +350,14 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
 
   if (warp < W::kCtl) {
     // control warpgroup (register split: the whole warpgroup lowers its limit here)
-    if constexpr (W::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(W::kCtlRegs));
+    if constexpr (W::kComb) {
+      if (warp >= 4)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(W::kCombRegs));
+      else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(W::kCtlRegs));
+    } else if constexpr (W::kSplitRegs) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(W::kCtlRegs));
+    }
   if (warp == 0) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
@@ -481,7 +534,8 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
             for (int kbl = 0; kbl < kSaChunk; ++kbl) sw[b][kbl] = w_scale(b, kbl);
         }
         const int buf = (int)(gch & 1);
-#pragma unroll
+        // (lean: one column batch at a time, not unrolled, to stay within the registers)
+#pragma unroll(kLean ? 1 : NJ)
         for (int j0 = 0; j0 < NJ; j0 += JB) {
           float sa[JB][kSaChunk];
 #pragma unroll
@@ -519,6 +573,161 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
         mbar_arrive(smem_u32(&pfull[buf]));  // each lane releases its own products
       }
     }
+  } else if (kComb && warp >= 4) {
+    // ------------------------------ fused combine -------------------------------
+    // Combine warp q (0..3) takes the token columns 32q .. 32q + 31 of this CTA's units.
+    // Once every epilogue warp has stored a unit's rows (the ring barrier, release and
+    // acquire at CTA scope), a gpu-scope fence publishes them -- the fence is cumulative over
+    // what this warp observed through the barrier -- and a relaxed atomic counts one arrival
+    // per (token, weight block). The arrival that completes a token's active routes acquires
+    // the other arrivals' rows (a second fence) and adds the token's rows of this weight block
+    // in ascending slot order, with the separate combine kernel's expression and rounding;
+    // each row segment is read once, so its L2 lines are dropped, not written back.
+    if constexpr (kComb) {
+      const int q = warp - 4;
+      // out_c[t, 128 nblk + 4 lane ..] from the rows of token t's active routes
+      auto combine_token = [&](int t, int nblk) {
+        const int col = nblk * kBM + 4 * lane;
+        const int64_t rbase = (int64_t)t * p.topk;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // slots in batches of kB, the batch's loads issued before its additions
+        constexpr int kB = 4;
+        for (int j0 = 0; j0 < p.topk; j0 += kB) {
+          int row[kB];
+          float wt[kB];
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            row[i] = -1;
+            wt[i] = 0.0f;
+            if (j0 + i < p.topk) {
+              const int d = __ldg(p.route2dst + rbase + j0 + i);
+              if (d >= 0) {  // a route without a row is skipped unread, as in the combine kernel
+                row[i] = d;
+                wt[i] = __ldg(p.rw + rbase + j0 + i);
+              }
+            }
+          }
+          float4 v[kB];
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            v[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (row[i] >= 0) v[i] = __ldcg(reinterpret_cast<const float4*>(p.out + (int64_t)row[i] * p.ld_out + col));
+          }
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            if (row[i] >= 0) {
+              acc[0] = fmaf(wt[i], v[i].x, acc[0]);
+              acc[1] = fmaf(wt[i], v[i].y, acc[1]);
+              acc[2] = fmaf(wt[i], v[i].z, acc[2]);
+              acc[3] = fmaf(wt[i], v[i].w, acc[3]);
+              // the line's eight lanes have all read it (one load instruction of the warp)
+              if ((lane & 7) == 0) discard_l2_line(p.out + (int64_t)row[i] * p.ld_out + col);
+            }
+          }
+        }
+        const int64_t o = (int64_t)t * p.ld_c + col;
+        if (p.out_dtype == FTMOE_OUT_FP32) {
+          store4(static_cast<float*>(p.out_c) + o, acc);
+        } else {
+          uint16_t b[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) b[i] = p.out_dtype == FTMOE_OUT_FP16 ? OutF16::cvt(acc[i]) : OutBf16::cvt(acc[i]);
+          store4(static_cast<uint16_t*>(p.out_c) + o, b);
+        }
+      };
+      // topk <= kCombK: each lane's slots are loaded together, and a token whose last route
+      // this lane counted has its rows and weights staged in shared memory, so that the warp
+      // then issues all of that token's row loads at once
+      const bool staged = p.topk <= kCombK;
+      int* my_rows = crow + q * 32 * kCombK;
+      float* my_wts = cwt + q * 32 * kCombK;
+      uint32_t j = 0;
+      for (int u = u_begin; u < u_end; u += u_step, ++j) {
+        int e, nb, tt, row0, rows;
+        decode(u, e, nb, tt, row0, rows);
+        const uint32_t slot = j % kYRing;
+        if (!mbar_wait(smem_u32(&ydone[slot]), (j / kYRing) & 1, &s_abort)) break;
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&yfree[slot]));
+        const int nblk = 2 * nb + (int)crank;
+        const int c = 32 * q + lane;
+        int t = -1;
+        bool last = false;
+        if (c < rows) {
+          t = __ldg(p.dst2src + row0 + c);
+          const int64_t rbase = (int64_t)t * p.topk;
+          int active = 0;
+          if (staged) {
+            int sr[kCombK];
+#pragma unroll
+            for (int i = 0; i < kCombK; ++i) sr[i] = i < p.topk ? __ldg(p.route2dst + rbase + i) : -1;
+#pragma unroll
+            for (int i = 0; i < kCombK; ++i) active += sr[i] >= 0 ? 1 : 0;
+            const uint32_t before = atomicAdd(p.cnt + (int64_t)t * NB + nblk, 1u);
+            last = (int)before + 1 == active;
+            if (last) {
+#pragma unroll
+              for (int i = 0; i < kCombK; ++i) {
+                my_rows[lane * kCombK + i] = sr[i];
+                my_wts[lane * kCombK + i] = sr[i] >= 0 ? __ldg(p.rw + rbase + i) : 0.0f;
+              }
+            }
+          } else {
+            for (int i = 0; i < p.topk; ++i) active += __ldg(p.route2dst + rbase + i) >= 0 ? 1 : 0;
+            const uint32_t before = atomicAdd(p.cnt + (int64_t)t * NB + nblk, 1u);
+            last = (int)before + 1 == active;
+          }
+        }
+        uint32_t m = __ballot_sync(0xffffffffu, last);
+        __syncwarp();  // (the lanes' staged rows are visible to the whole warp)
+        if (m != 0) fence_acq_rel_gpu();
+        while (m != 0) {
+          const int i = __ffs((int)m) - 1;
+          m &= m - 1;
+          const int ti = __shfl_sync(0xffffffffu, t, i);
+          if (!staged) {
+            combine_token(ti, nblk);
+            continue;
+          }
+          // the token's rows of this weight block, all loads in flight together
+          const int col = nblk * kBM + 4 * lane;
+          const int* rr = my_rows + i * kCombK;
+          const float* ww = my_wts + i * kCombK;
+          float4 v[kCombK];
+#pragma unroll
+          for (int k = 0; k < kCombK; ++k) {
+            const int r = rr[k];
+            v[k] = r >= 0 ? __ldcg(reinterpret_cast<const float4*>(p.out + (int64_t)r * p.ld_out + col))
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          }
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int k = 0; k < kCombK; ++k) {
+            const int r = rr[k];
+            if (r >= 0) {  // a route without a row is skipped unread, as in the combine kernel
+              const float wk = ww[k];
+              acc[0] = fmaf(wk, v[k].x, acc[0]);
+              acc[1] = fmaf(wk, v[k].y, acc[1]);
+              acc[2] = fmaf(wk, v[k].z, acc[2]);
+              acc[3] = fmaf(wk, v[k].w, acc[3]);
+              // the line's eight lanes have all read it (one load instruction of the warp)
+              if ((lane & 7) == 0) discard_l2_line(p.out + (int64_t)r * p.ld_out + col);
+            }
+          }
+          const int64_t o = (int64_t)ti * p.ld_c + col;
+          if (p.out_dtype == FTMOE_OUT_FP32) {
+            store4(static_cast<float*>(p.out_c) + o, acc);
+          } else {
+            uint16_t b16[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) b16[k] = p.out_dtype == FTMOE_OUT_FP16 ? OutF16::cvt(acc[k]) : OutBf16::cvt(acc[k]);
+            store4(static_cast<uint16_t*>(p.out_c) + o, b16);
+          }
+        }
+        __syncwarp();  // the staged rows of this unit are read before the next unit overwrites them
+      }
+    }
   }
   } else {
     // --------------------------------- epilogue ---------------------------------
@@ -528,7 +737,7 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     // of the unit, and the group leaves together at the next unit boundary.
     constexpr int HC = TT / kGroups;          // token columns of this warp's group
     // TMEM columns read per tcgen05.ld round trip and block (keeps the registers in bounds)
-    constexpr int CH = WB * HC <= 16 ? HC : (W::kSplitRegs ? (TT == 128 ? 4 : 8) : 16 / WB);
+    constexpr int CH = kCP ? 16 : (WB * HC <= 16 ? HC : (W::kSplitRegs ? (TT == 128 ? 4 : 8) : 16 / WB));
     const int ew = warp - W::kCtl;            // 0 .. kEpiWarps-1
     const int grp = ew >> 2;                  // column group
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
@@ -538,7 +747,10 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
     uint32_t kc = 0;
     float acc[WB][HC];
     uint32_t gch = 0;  // chunks begun so far; chunk gch uses product buffer gch & 1
-    for (int u = u_begin; u < u_end; u += u_step) {
+    // (fused combine) the rows stay in L2 until the token's last route has arrived
+    const uint64_t pol_y = kComb ? l2_policy_evict_last() : 0ull;
+    uint32_t ucount = 0;  // units of this CTA so far
+    for (int u = u_begin; u < u_end; u += u_step, ++ucount) {
       int e, nb, tt, row0, rows;
       decode(u, e, nb, tt, row0, rows);
       // all warps of the group leave together on an abort
@@ -678,9 +890,22 @@ __global__ void __launch_bounds__(Warps<TT, MODE>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < HC; ++c) {
               const int r = grp * HC + c;
-              if (r < rows) p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[b][c];
+              if (r < rows) {
+                if constexpr (kComb)
+                  st_global_hint(p.out + (int64_t)(row0 + r) * p.ld_out + n, acc[b][c], pol_y);
+                else
+                  p.out[(int64_t)(row0 + r) * p.ld_out + n] = acc[b][c];
+              }
             }
           }
+        }
+        if constexpr (kComb) {
+          // hand the unit's rows to the combine warps (the slot's previous unit, kYRing
+          // units back, has been taken over by then)
+          const uint32_t slot = ucount % kYRing;
+          (void)mbar_wait(smem_u32(&yfree[slot]), ((ucount / kYRing) & 1) ^ 1, &s_abort);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ydone[slot]));
         }
       }
     }
@@ -769,7 +994,8 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     *unsupported = 1;
     return cudaSuccess;
   }
-  const size_t fixed = 1024 /*align*/ + SM::kProdBytes + SM::kRedBytes + (size_t)(3 * a.E + 2) * 4 + 8;
+  const size_t fixed =
+      1024 /*align*/ + SM::kProdBytes + SM::kRedBytes + SM::kCombBytes + (size_t)(3 * a.E + 2) * 4 + 8;
   // dynamic shared memory budget: the device's opt-in maximum per block minus the
   // kernel's static shared memory
   int dev = 0;
@@ -801,9 +1027,10 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     }
   }
   constexpr int kAcc = tc::acc_count(SM::kWB * TT);
+  constexpr int kBars = 2 * kAcc + 4 + (MODE == tc::kCtaPairComb ? 2 * tc::kYRing : 0);
   int stages = tc::kMaxStages;
-  while (stages > 2 && fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc + 4) * 8 > max_smem) --stages;
-  const size_t smem = fixed + (size_t)stages * SM::kStage + (2 * stages + 2 * kAcc + 4) * 8;
+  while (stages > 2 && fixed + (size_t)stages * SM::kStage + (2 * stages + kBars) * 8 > max_smem) --stages;
+  const size_t smem = fixed + (size_t)stages * SM::kStage + (2 * stages + kBars) * 8;
   if (smem > max_smem) {
     *unsupported = 1;
     return cudaSuccess;
@@ -820,7 +1047,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     const uint64_t ws[4] = {(uint64_t)a.k, 128, 128 * (uint64_t)a.k, half * (uint64_t)a.k};
     const uint32_t wb[5] = {128, 128, (uint32_t)KBS, 1, 2};
     if (!encode_u8_tmap(&mw, a.w_q, 5, wd, ws, wb)) return cudaErrorInvalidValue;
-  } else if constexpr (MODE == tc::kPair || MODE == tc::kCtaPair || KBS > 1) {
+  } else if constexpr (MODE == tc::kPair || tc::is_cp(MODE) || KBS > 1) {
     // (the CTA pair's loads are always 4-D: this map at every KBS)
     const uint64_t wd[4] = {128, (uint64_t)a.n, (uint64_t)KB, (uint64_t)a.E};
     const uint64_t ws[3] = {(uint64_t)a.k, 128, (uint64_t)a.k * (uint64_t)a.n};
@@ -836,7 +1063,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
     // (a CTA pair loads half of the token tile in each CTA)
     const uint64_t ad[3] = {128, (uint64_t)a.a_rows, (uint64_t)KB};
     const uint64_t as[2] = {(uint64_t)a.k, 128};
-    const uint32_t ab[3] = {128, (uint32_t)(MODE == tc::kCtaPair ? TT / 2 : TT), (uint32_t)KBS};
+    const uint32_t ab[3] = {128, (uint32_t)(tc::is_cp(MODE) ? TT / 2 : TT), (uint32_t)KBS};
     if (!encode_u8_tmap(&ma, a.a_q, 3, ad, as, ab)) return cudaErrorInvalidValue;
   } else {
     const uint64_t ad[2] = {(uint64_t)a.k, (uint64_t)a.a_rows};
@@ -859,6 +1086,14 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
   p.kb_count = KB;
   p.nb_count = NB;
   p.stages = stages;
+  p.dst2src = a.dst2src;
+  p.route2dst = a.route2dst;
+  p.rw = a.rw;
+  p.cnt = a.cnt;
+  p.out_c = a.out_c;
+  p.ld_c = a.ld_c;
+  p.topk = a.topk;
+  p.out_dtype = a.out_dtype;
   // raise the kernel's dynamic shared memory limit only when a launch needs more than
   // any earlier one on this device (the attribute is per function and device)
   static size_t granted[64] = {};
@@ -872,7 +1107,7 @@ static cudaError_t launch_tt(const TcGemmArgs& a, cudaStream_t st, int* unsuppor
         cudaFuncSetAttribute(tc::tc_gemm_kernel<TT, KBS, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  if constexpr (MODE == tc::kCtaPair) {
+  if constexpr (tc::is_cp(MODE)) {
     // as many CTA pairs as can be resident at once (one CTA per SM; a pair needs two SMs
     // of one cluster-capable group, so this may be a little under half the SMs)
     static int pairs[64] = {};
@@ -906,6 +1141,12 @@ static cudaError_t launch_mode(const TcGemmArgs& a, cudaStream_t st, int* unsupp
 
 bool tc_gemm_pairs_ok(int64_t n, int64_t k) { return n % 256 == 0 && k % 128 == 0; }
 
+bool tc_gemm_comb_ok(int tok_tile, int64_t n, int64_t k, const void* y, int64_t ld_y, const void* out_c,
+                     int64_t ld_c) {
+  return (tok_tile == 64 || tok_tile == 128) && tc_gemm_pairs_ok(n, k) && (uintptr_t)y % 128 == 0 && ld_y % 32 == 0 &&
+         (uintptr_t)out_c % 16 == 0 && ld_c % 4 == 0;
+}
+
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupported) {
   *unsupported = 0;
   // TMA needs 16-byte aligned bases and row strides; the kernel indexes rows and
@@ -916,6 +1157,16 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int* unsupporte
     return cudaSuccess;
   }
   // a CTA pair: one weight block per CTA, token tile 64 or 128, whole block pairs and K blocks
+  if (a.comb) {
+    if (a.ctas != 2 || a.silu || a.wblocks == 2 || a.topk <= 0 ||
+        !tc_gemm_comb_ok(a.tok_tile, a.n, a.k, a.out, a.ld_out, a.out_c, a.ld_c)) {
+      *unsupported = 1;
+      return cudaSuccess;
+    }
+    return a.tok_tile == 64
+               ? launch_tt<64, tc::kbs_for(64, tc::kCtaPairComb), tc::kCtaPairComb>(a, st, unsupported)
+               : launch_tt<128, tc::kbs_for(128, tc::kCtaPairComb), tc::kCtaPairComb>(a, st, unsupported);
+  }
   if (a.ctas == 2) {
     if (a.silu || a.wblocks == 2 || !tc_gemm_pairs_ok(a.n, a.k) || (a.tok_tile != 64 && a.tok_tile != 128)) {
       *unsupported = 1;

@@ -12,7 +12,8 @@
  *      (FreeToken "perf(moe): skip inactive block-fp8 decode routes", first section);
  *   5. SiLU-and-mul, re-quantized per 1x128 for the down GEMM;
  *   6. grouped down GEMM;
- *   7. routing-weighted top-k combine into bf16.
+ *   7. routing-weighted top-k combine into bf16 (a kernel of its own, or inside the down
+ *      GEMM on its CTA-pair kernel: ftmoe_moe_forward, path 5).
  * A negative expert slot is an inactive route: its gate/up and down output tiles are
  * written as exact zeros and nothing else of it is read (FreeToken page, first section).
  *
@@ -306,13 +307,22 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * with FP8 re-quantization, down and the combine run in one persistent tensor-core kernel
  * whose weight stream is split evenly over the SMs (FP8; T <= 8, T*topk <= 64, E <= 1024,
  * H and I multiples of 128, H <= 8192, I <= 2048; a token that lists one expert twice
- * computes that expert once and weights it per listing).
+ * computes that expert once and weights it per listing),
+ * 5 = grouped path with the combine inside the down GEMM (FP8; token tile 64 or 128,
+ * H % 256 == 0, I % 128 == 0; out 16-byte aligned with ld_out % 4 == 0): the down GEMM runs
+ * on CTA pairs, counts the arrivals of each token's routes per 128 columns and, at the last,
+ * adds the token's rows in ascending slot order with the combine's expression and rounding
+ * (decode page, first section: the reduction after the down GEMM), so no fp32 row has to
+ * travel back from HBM. The down buffer's contents are undefined after such a call (its rows
+ * are dropped from L2 once added), and the arrival counters live in the workspace's
+ * counters region (zeroed by the call itself).
  * Automatic: the fused decode path where its limits hold; else the grouped path, fused where
  * the token tile is at most 64, the bank has at most 1024 experts and the routes can reach at
  * least 2048 (expert, gate/up block pair) units (min(T*topk, E) * I/128 >= 2048), else with
- * the separate kernel. Paths 2 and 3 give bit-identical outputs; path 4 adds the partial
- * sums of a gate/up element in another order, so it agrees with them within the fp32
- * rounding of that sum.
+ * the separate kernel, and the combine kernel (path 5 measured slower on GB300: 6.2 ms
+ * against 2.6 ms for 24,576 routes of 7168/2048, its per-token round trips to memory waiting
+ * behind the weight stream). Paths 2, 3 and 5 give bit-identical outputs; path 4 adds the partial sums of a gate/up
+ * element in another order, so it agrees with them within the fp32 rounding of that sum.
  * NVFP4 and MXFP8 take the grouped path with the separate SiLU-and-mul kernel only (paths 0
  * and 2; 1, 3 and 4 return FTMOE_UNSUPPORTED). MXFP8 segments the routes first, then
  * gathers the bf16 token rows and quantizes the gathered rows (ftmoe_gather_quantize_act);
@@ -352,7 +362,8 @@ typedef struct ftmoe_workspace_layout {
   size_t act_q, act_q_bytes, act_scales, act_scales_bytes, act_gscale;
   size_t down, down_bytes;                   /* float down output [R][H] */
   size_t partials, partials_bytes;           /* fused decode path: gate/up partial sums */
-  size_t counters, counters_bytes;           /* fused decode path: arrival counters */
+  size_t counters, counters_bytes;           /* arrival counters: fused decode path, and the
+                                                combine inside the down GEMM ([T][H/128]) */
   size_t total;
 } ftmoe_workspace_layout;
 

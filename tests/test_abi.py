@@ -166,8 +166,18 @@ def test_automatic_forward_path_choice(ft):
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=2))["gateup_bytes"] > 0
     assert lay(ft.moe_shape(2048, 7168, 2048, 6, 2048))["gateup_bytes"] > 0  # beyond the GEMM's 1024 experts
     assert lay(ft.moe_shape(1, 2048, 768, 8, 8, path=3))["gateup_bytes"] == 0
+    # the combine inside the down GEMM (arrival counters, one word per token and 128 columns):
+    # path 5 only (FP8, token tile 64 or 128); the automatic path keeps the combine kernel
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256))["counters_bytes"] == 0
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, path=5))["counters_bytes"] == 4096 * 56 * 4
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, path=3))["counters_bytes"] == 0
+    assert lay(ft.moe_shape(1024, 7168, 2048, 6, 256, path=5))["counters_bytes"] == 0         # tile 32
+    assert lay(ft.moe_shape(1024, 7168, 2048, 6, 256, tok_tile=64, path=5))["counters_bytes"] == 1024 * 56 * 4
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, fmt=ft.FMT_NVFP4, path=5))["counters_bytes"] == 0
+    assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, fmt=ft.FMT_MXFP8, path=5))["counters_bytes"] == 0
+    assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=5))["counters_bytes"] == 0             # tile 16
     with pytest.raises(ft.FtmoeError):
-        lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=5))
+        lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=6))
 
 
 def test_fused_decode_workspace(ft):

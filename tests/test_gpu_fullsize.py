@@ -100,6 +100,11 @@ def test_prefill_full_sizes_against_the_oracle(ft, fmt, sizes):
             assert ft.ftmoe_forward_workspace_layout(ft.moe_shape(x.shape[0], H, I, TOPK, E))["gateup_bytes"] == 0
             sep = _gpu_forward(ft, (bank_gu, bank_dn), x, ids, w, fmt, path=2)
             assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
+        if fmt == "fp8" and r == 24576:
+            # at 24,576 routes (token tile 128, CTA pairs) the forward that adds up each token's
+            # rows inside the down GEMM (path 5) gives the automatic forward's bits
+            comb = _gpu_forward(ft, (bank_gu, bank_dn), x, ids, w, fmt, path=5)
+            assert torch.equal(out.view(torch.int16), comb.view(torch.int16))
         outs.append((got, sub))
         calls.append(dict(x32=x.float().numpy(), ids=ids.numpy(), weights=w.numpy(), checked=sub))
     del keep_gu, keep_dn, bank_gu, bank_dn
