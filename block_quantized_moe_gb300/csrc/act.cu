@@ -196,7 +196,7 @@ cudaError_t launch_silu_mul_nvfp4(const float* gu, int64_t rows, int64_t inter, 
 
 // ---- combine: out[t, h] = round( sum_j w[t,j] * y[row(t,j), h] ), active j ascending ----
 // (output conversions OutBf16 / OutF16 / OutF32 and store4: common.cuh)
-// The slot ids, weights and rows of a token are loaded eight slots at a time with
+// The slot ids, weights and rows of a token are loaded six slots at a time with
 // independent loads, then accumulated in ascending slot order.
 template <bool kVec, typename Out>
 __global__ void __launch_bounds__(128) combine_kernel(
@@ -206,62 +206,82 @@ __global__ void __launch_bounds__(128) combine_kernel(
   pdl_wait();  // the predecessor's outputs are complete from here on
   pdl_trigger();
   const int64_t t = blockIdx.y;
-  const int64_t h0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  // eight outputs per thread, two runs of four: every slot's two row loads are in flight
+  // together, and a slot's row index is loaded beside its id (the id only decides whether
+  // the weight and the row are read)
+  const int64_t h0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (h0 >= hidden) return;
-  const bool full = kVec && h0 + 4 <= hidden;
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int j0 = 0; j0 < topk; j0 += 8) {
-    int64_t row[8];
-    float wt[8];
+  float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+  for (int j0 = 0; j0 < topk; j0 += 6) {
+    constexpr int kS = 6;  // slots per batch
+    int idv[kS];
+    int64_t dst[kS];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kS; ++u) {
+      const int j = j0 + u;
+      const int64_t r = t * topk + j;
+      idv[u] = j < topk ? ids[r] : -1;
+      dst[u] = (j < topk && route2dst != nullptr) ? (int64_t)route2dst[r] : r;
+    }
+    int64_t row[kS];
+    float wt[kS];
+#pragma unroll
+    for (int u = 0; u < kS; ++u) {
       row[u] = -1;
       wt[u] = 0.0f;
-      const int j = j0 + u;
-      if (j < topk) {
-        const int64_t r = t * topk + j;
-        if (ids[r] >= 0) {  // inactive: neither the weight nor the row is read
-          wt[u] = w[r];
-          row[u] = route2dst != nullptr ? (int64_t)route2dst[r] : r;
+      if (idv[u] >= 0) {  // inactive: neither the weight nor the row is read
+        wt[u] = w[t * topk + j0 + u];
+        row[u] = dst[u];
+      }
+    }
+    float4 v[kS][2];
+#pragma unroll
+    for (int u = 0; u < kS; ++u) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        v[u][h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const int64_t c = h0 + 4 * h;
+        if (row[u] >= 0 && c < hidden) {
+          const float* yr = y + row[u] * ld_y + c;
+          if (kVec && c + 4 <= hidden) {
+            v[u][h] = *reinterpret_cast<const float4*>(yr);
+          } else {
+            v[u][h].x = yr[0];
+            if (c + 1 < hidden) v[u][h].y = yr[1];
+            if (c + 2 < hidden) v[u][h].z = yr[2];
+            if (c + 3 < hidden) v[u][h].w = yr[3];
+          }
         }
       }
     }
-    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int u = 0; u < kS; ++u) {
       if (row[u] >= 0) {
-        const float* yr = y + row[u] * ld_y + h0;
-        if (full) {
-          v[u] = *reinterpret_cast<const float4*>(yr);
-        } else {
-          v[u].x = yr[0];
-          if (h0 + 1 < hidden) v[u].y = yr[1];
-          if (h0 + 2 < hidden) v[u].z = yr[2];
-          if (h0 + 3 < hidden) v[u].w = yr[3];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          acc[h][0] = fmaf(wt[u], v[u][h].x, acc[h][0]);
+          acc[h][1] = fmaf(wt[u], v[u][h].y, acc[h][1]);
+          acc[h][2] = fmaf(wt[u], v[u][h].z, acc[h][2]);
+          acc[h][3] = fmaf(wt[u], v[u][h].w, acc[h][3]);
         }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (row[u] >= 0) {
-        acc[0] = fmaf(wt[u], v[u].x, acc[0]);
-        acc[1] = fmaf(wt[u], v[u].y, acc[1]);
-        acc[2] = fmaf(wt[u], v[u].z, acc[2]);
-        acc[3] = fmaf(wt[u], v[u].w, acc[3]);
       }
     }
   }
-  typename Out::T b[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) b[i] = Out::cvt(acc[i]);
-  typename Out::T* o = out + t * ld_out + h0;
-  if (full) {
-    store4(o, b);
-  } else {
+  for (int h = 0; h < 2; ++h) {
+    const int64_t c = h0 + 4 * h;
+    if (c >= hidden) break;
+    typename Out::T b[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (h0 + i < hidden) o[i] = b[i];
+    for (int i = 0; i < 4; ++i) b[i] = Out::cvt(acc[h][i]);
+    typename Out::T* o = out + t * ld_out + c;
+    if (kVec && c + 4 <= hidden) {
+      store4(o, b);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c + i < hidden) o[i] = b[i];
+    }
   }
 }
 
@@ -283,7 +303,7 @@ static cudaError_t launch_combine_t(const float* y, int64_t ld_y, const int32_t*
   constexpr int kOutBytes = (int)sizeof(typename Out::T);
   const bool vec = (hidden % 4 == 0) && (ld_y % 4 == 0) && ((uintptr_t)y % 16 == 0) && (ld_out % 4 == 0) &&
                    ((uintptr_t)out % (4 * kOutBytes) == 0);
-  dim3 grid((unsigned)cdiv(hidden, 4 * 128), (unsigned)tokens);
+  dim3 grid((unsigned)cdiv(hidden, 8 * 128), (unsigned)tokens);
   return launch_kernel(vec ? combine_kernel<true, Out> : combine_kernel<false, Out>, grid, dim3(128), 0, st, true, y,
                        ld_y, route2dst, ids, w, tokens, topk, hidden, out, ld_out);
 }

@@ -14,6 +14,7 @@
 namespace ftmoe {
 
 constexpr int kSegThreads = 512;
+constexpr int kSegBatch = 8;  // 32-id steps whose loads a warp issues together
 
 // Segments of expert e, by one CTA of kSegThreads threads (sh: 2 * kSegThreads / 32 ints).
 // Pass 1: every warp counts, over its own range, the active routes of lower experts and
@@ -29,12 +30,22 @@ __device__ __forceinline__ void segment_expert(const int32_t* __restrict__ ids, 
   const int64_t span = ((routes + kWarps - 1) / kWarps + 31) / 32 * 32;
   const int64_t r0 = span * warp;
   const int64_t r1 = r0 + span < routes ? r0 + span : routes;
+  // (the ids of a chunk of kSegBatch steps are loaded together: the walk is a chain of L2
+  // round trips otherwise)
   int below = 0, mine = 0;
-  for (int64_t r = r0 + lane; r < r1; r += 32) {
-    const int id = ids[r];
-    below += (id >= 0 && id < e);
-    mine += (id == e);
-    if (e == 0 && id >= E) raise_error(FTMOE_ERR_EXPERT_ID_RANGE);
+  for (int64_t c0 = r0; c0 < r1; c0 += 32 * kSegBatch) {
+    int v[kSegBatch];
+#pragma unroll
+    for (int u = 0; u < kSegBatch; ++u) {
+      const int64_t r = c0 + 32 * u + lane;
+      v[u] = r < r1 ? ids[r] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kSegBatch; ++u) {
+      below += (v[u] >= 0 && v[u] < e);
+      mine += (v[u] == e);
+      if (e == 0 && v[u] >= E) raise_error(FTMOE_ERR_EXPERT_ID_RANGE);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -60,18 +71,27 @@ __device__ __forceinline__ void segment_expert(const int32_t* __restrict__ ids, 
   }
   int base = off + first;
   const uint32_t lower = (1u << lane) - 1u;
-  for (int64_t c0 = r0; c0 < r1; c0 += 32) {
-    const int64_t r = c0 + lane;
-    const int id = r < r1 ? ids[r] : -1;
-    const uint32_t m = __ballot_sync(0xffffffffu, id == e);
-    if (id == e) {
-      const int d = base + __popc(m & lower);
-      dst2src[d] = (int32_t)(r / topk);
-      route2dst[r] = d;
-    } else if (e == 0 && r < r1 && (id < 0 || id >= E)) {
-      route2dst[r] = -1;  // inactive (or out-of-range, reported above) routes
+  for (int64_t c0 = r0; c0 < r1; c0 += 32 * kSegBatch) {
+    int v[kSegBatch];
+#pragma unroll
+    for (int u = 0; u < kSegBatch; ++u) {
+      const int64_t r = c0 + 32 * u + lane;
+      v[u] = r < r1 ? ids[r] : -1;
     }
-    base += __popc(m);
+#pragma unroll
+    for (int u = 0; u < kSegBatch; ++u) {
+      const int64_t r = c0 + 32 * u + lane;
+      const int id = v[u];
+      const uint32_t m = __ballot_sync(0xffffffffu, id == e);
+      if (id == e) {
+        const int d = base + __popc(m & lower);
+        dst2src[d] = (int32_t)(r / topk);
+        route2dst[r] = d;
+      } else if (e == 0 && r < r1 && (id < 0 || id >= E)) {
+        route2dst[r] = -1;  // inactive (or out-of-range, reported above) routes
+      }
+      base += __popc(m);
+    }
   }
 }
 

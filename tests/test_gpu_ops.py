@@ -199,6 +199,31 @@ def test_combine(ft):
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
 
 
+@pytest.mark.parametrize("H,ld_pad", [(4096, 0), (1000, 0), (1002, 0), (520, 3)])
+@pytest.mark.parametrize("k", [6, 8, 13])
+def test_combine_ragged_hidden_and_slot_counts(ft, H, ld_pad, k):
+    # hidden not a multiple of 8 (or of 4), padded row strides, slot counts below, at and past
+    # one batch of loads; route-major y, and y rows reached through route2dst
+    T = 10
+    ids = synth.routes(T, k, 32, 11 + k, active_per_token=[k, 3, 0, 1, k - 1] * 2, device=DEV)
+    w = synth.routing_weights(T, k, 11 + k, DEV)
+    w[ids < 0] = float("nan")  # never read
+    y = torch.randn(T * k, H + ld_pad, device=DEV)
+    perm = torch.randperm(T * k, generator=torch.Generator().manual_seed(k)).to(torch.int32).to(DEV)
+    y_perm = torch.empty_like(y)
+    y_perm[perm.long()] = y
+    out = torch.zeros(T, H + ld_pad, dtype=torch.bfloat16, device=DEV)
+    out2 = torch.zeros(T, H + ld_pad, dtype=torch.bfloat16, device=DEV)
+    ft.ftmoe_combine(y[:, :H], ids, w, out[:, :H])
+    ft.ftmoe_combine(y_perm[:, :H], ids, w, out2[:, :H], route2dst=perm)
+    torch.cuda.synchronize()
+    ref = M.combine(y[:, :H].cpu().numpy(), np.arange(T * k), ids.cpu().numpy(), w.cpu().numpy())
+    got = out[:, :H].float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))  # the padding stays zero too
+    assert torch.all(out[:, H:] == 0)
+
+
 def test_combine_single_route_weight_one_is_the_row(ft):
     T, k, H = 3, 4, 520
     ids = torch.full((T, k), -1, dtype=torch.int32, device=DEV)
