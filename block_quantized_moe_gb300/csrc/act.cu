@@ -64,10 +64,11 @@ __global__ void __launch_bounds__(256) silu_mul_fp8_kernel(
     const float sc = div_rn(amax, kE4M3Max);
     uint32_t codes[2] = {0u, 0u};
     if (amax > 0.0f) {
+      const SharedDivisor ds(sc);  // a / sc as IEEE division rounds it
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        codes[h] = (uint32_t)f2_to_e4m3x2(div_rn(a[4 * h], sc), div_rn(a[4 * h + 1], sc)) |
-                   ((uint32_t)f2_to_e4m3x2(div_rn(a[4 * h + 2], sc), div_rn(a[4 * h + 3], sc)) << 16);
+        codes[h] = (uint32_t)f2_to_e4m3x2(ds.div(a[4 * h]), ds.div(a[4 * h + 1])) |
+                   ((uint32_t)f2_to_e4m3x2(ds.div(a[4 * h + 2]), ds.div(a[4 * h + 3])) << 16);
     }
     if (live) {
       uint8_t* qr = q + row * inter;

@@ -93,6 +93,31 @@ __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
 // explicit intrinsic documents that the quantization decision depends on it).
 __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
 
+// Many dividends over one divisor d, each quotient rounded to nearest even exactly as IEEE
+// division rounds it. Markstein's theorem (P. W. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990): with
+// y = RN(1/d), q0 = RN(x*y) and the residual r = x - q0*d (exact with a fused multiply-add),
+// RN(q0 + r*y) is the correctly rounded x/d, as long as nothing leaves the normal range. The
+// reciprocal takes one IEEE division per divisor instead of one per element. A divisor far
+// from 1 (outside [2^-100, 2^100], or not finite) keeps the IEEE division per element, and an
+// exact q0 (r = 0) is kept as it is, so that a zero quotient keeps its sign. Quotients so small
+// that they are subnormal round to zero codes in every format here either way.
+struct SharedDivisor {
+  float d, y;
+  bool fast;
+  __device__ __forceinline__ explicit SharedDivisor(float d_) : d(d_) {
+    const float ad = fabsf(d_);
+    fast = ad >= 0x1p-100f && ad <= 0x1p100f;
+    y = fast ? __fdiv_rn(1.0f, d_) : 0.0f;
+  }
+  __device__ __forceinline__ float div(float x) const {
+    if (!fast) return __fdiv_rn(x, d);
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, d, x);
+    return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);
+  }
+};
+
 // silu(g) * u in fp32, the one expression every SiLU-and-mul of the library evaluates (the
 // separate kernel and the gate/up GEMM epilogue give bit-identical results).
 __device__ __forceinline__ float silu_mul_1(float g, float u) { return g / (1.0f + expf(-g)) * u; }

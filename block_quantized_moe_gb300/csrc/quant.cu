@@ -21,11 +21,8 @@ __global__ void __launch_bounds__(256) quantize_act_fp8_kernel(
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows * ng;
-       w += nwarps) {
-    const int64_t row = w / ng, g = w - row * ng;
-    quantize_fp8_group<kVec>(x, k, ld_x, q, s, ng, row, g, lane);
-  }
+  quantize_fp8_rows_hw<kVec>(x, k, ld_x, q, s, ng, rows * ng,
+                             (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), nwarps, lane);
 }
 
 static int grid_for(int64_t work_items, int per_block) {
@@ -38,8 +35,11 @@ static int grid_for(int64_t work_items, int per_block) {
 cudaError_t launch_quantize_act_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t ld_x,
                                     uint8_t* q, float* scales, cudaStream_t st) {
   const int64_t ng = cdiv(k, kGroup);
-  const bool vec = quantize_fp8_vec_ok(x, ld_x, q, k);
-  const int grid = grid_for(rows * ng, 8);
+  const bool vec = quantize_fp8_vec16_ok(x, ld_x, q, k);
+  // (at most four resident CTAs per SM: each warp then runs several batches, the next one's
+  // loads in flight while it finishes the current one)
+  int grid = grid_for(rows * ng, 16 * kHwBatch);
+  if (grid > 152 * 4) grid = 152 * 4;
   return launch_kernel(vec ? quantize_act_fp8_kernel<true> : quantize_act_fp8_kernel<false>, dim3(grid), dim3(256), 0,
                        st, true, x, rows, k, ld_x, q, scales, ng);
 }

@@ -26,9 +26,12 @@ __device__ __forceinline__ void segment_expert(const int32_t* __restrict__ ids, 
                                                int32_t* __restrict__ route2dst, int e, int* sh) {
   constexpr int kWarps = kSegThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // the warp's range [r0, r1), a whole number of 32-id steps
+  // the warp's range [r0, r1), a whole number of 32-id steps. Range ri goes to warp
+  // (ri - e) mod 16: every CTA reads all of the ids at the same time, and the rotation spreads
+  // their first reads over 16 places instead of one
+  const int ri = (warp + e) % kWarps;
   const int64_t span = ((routes + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int64_t r0 = span * warp;
+  const int64_t r0 = span * ri;
   const int64_t r1 = r0 + span < routes ? r0 + span : routes;
   // (the ids of a chunk of kSegBatch steps are loaded together: the walk is a chain of L2
   // round trips otherwise)
@@ -53,14 +56,14 @@ __device__ __forceinline__ void segment_expert(const int32_t* __restrict__ ids, 
     mine += __shfl_xor_sync(0xffffffffu, mine, o);
   }
   if (lane == 0) {
-    sh[warp] = mine;
-    sh[kWarps + warp] = below;
+    sh[ri] = mine;
+    sh[kWarps + ri] = below;
   }
   __syncthreads();
   int first = 0, off = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    first += w < warp ? sh[w] : 0;
+    first += w < ri ? sh[w] : 0;
     total += sh[w];
     off += sh[kWarps + w];
   }
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(
 
 // The fused forward's first launch: FP8 quantization of the token rows and the expert
 // segmenter are independent steps, so one grid runs both -- blocks [0, E) segment one
-// expert each (first, as they take longest), blocks [E, E + qblocks) quantize (one warp
+// expert each (first, as they take longest), blocks [E, E + qblocks) quantize (a half-warp
 // per 1x128 group). With the down GEMM's fused combine the quantizing blocks also zero its
 // arrival counters and write the zero output rows of tokens that have no active route (the
 // combine inside the GEMM only reaches tokens with at least one).
@@ -127,10 +130,7 @@ __global__ void __launch_bounds__(kSegThreads) prep_fp8_kernel(
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)qblocks * (blockDim.x >> 5);
     const int64_t gwarp = (int64_t)qb * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    for (int64_t w = gwarp; w < rows * ng; w += nwarps) {
-      const int64_t row = w / ng, g = w - row * ng;
-      quantize_fp8_group<kVec>(x, k, ld_x, q, s, ng, row, g, lane);
-    }
+    quantize_fp8_rows_hw<kVec>(x, k, ld_x, q, s, ng, rows * ng, gwarp, nwarps, lane);
     if (pc.zero_words != nullptr) {
       for (int64_t i = gwarp * 32 + lane; i < pc.n_zero_words; i += nwarps * 32) pc.zero_words[i] = 0u;
     }
@@ -164,11 +164,11 @@ cudaError_t launch_prep_fp8(const uint16_t* x, int64_t rows, int64_t k, int64_t 
                             int32_t* offsets, int32_t* dst2src, int32_t* route2dst, const PrepCombine& pc,
                             cudaStream_t st) {
   const int64_t ng = cdiv(k, kGroup);
-  const int64_t warps = rows * ng;
+  const int64_t warps = cdiv(rows * ng, 2 * kHwBatch);
   int64_t qb = cdiv(warps, kSegThreads / 32);
-  if (qb > 152 * 16) qb = 152 * 16;  // grid-stride beyond this
+  if (qb > 152 * 2) qb = 152 * 2;  // two resident CTAs per SM; the warps stride over the rest
   if (qb < 1) qb = 1;
-  const bool vec = quantize_fp8_vec_ok(x, ld_x, q, k);
+  const bool vec = quantize_fp8_vec16_ok(x, ld_x, q, k);
   return launch_kernel(vec ? prep_fp8_kernel<true> : prep_fp8_kernel<false>, dim3((unsigned)qb + E),
                        dim3(kSegThreads), 0, st, true, x, rows, k, ld_x, q, scales, ng, (int)qb, ids, routes, topk, E,
                        counts, offsets, dst2src, route2dst, pc);

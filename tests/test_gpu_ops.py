@@ -30,7 +30,7 @@ def _bits(t):
 # -- quantization ------------------------------------------------------------------
 
 @pytest.mark.parametrize("rows,k,ld_pad", [(1, 2048, 0), (8, 4096, 0), (37, 896, 0), (5, 200, 8),
-                                           (3, 7168, 0), (64, 130, 2), (0, 256, 0)])
+                                           (3, 7168, 0), (64, 130, 2), (0, 256, 0), (3, 384, 0), (7, 1000, 0)])
 def test_quantize_act_fp8_bitexact(ft, rows, k, ld_pad):
     xf = synth.activations_bf16(rows, k + ld_pad, 1000 + k, DEV)
     if rows:
@@ -44,6 +44,25 @@ def test_quantize_act_fp8_bitexact(ft, rows, k, ld_pad):
     rq, rs = M.quantize_act_fp8_fast(x.float().cpu().numpy())
     assert np.array_equal(q.cpu().numpy(), rq)
     assert np.array_equal(_bits(s), rs.view(np.uint32))
+
+
+def test_quantize_act_fp8_many_binades_bitexact(ft):
+    # 3.7 M elements whose magnitudes span 2^-30 .. 2^30 within a group, so that the quotients
+    # x / s cover every binade the e4m3 codes use and many far below: the kernels' division by
+    # the group scale must round exactly as IEEE division (the oracle's float32 x / s)
+    g = torch.Generator().manual_seed(0xD1)
+    rows, k = 512, 7168
+    mant = torch.rand(rows, k, generator=g) + 1.0
+    expo = torch.randint(-30, 31, (rows, k), generator=g).float()
+    sign = torch.where(torch.rand(rows, k, generator=g) < 0.5, -1.0, 1.0)
+    x = (sign * mant * torch.pow(2.0, expo)).to(torch.bfloat16).to(DEV)
+    q = torch.empty(rows, k, dtype=torch.uint8, device=DEV)
+    s = torch.empty(rows, k // 128, dtype=torch.float32, device=DEV)
+    ft.ftmoe_quantize_act(x, q, s)
+    torch.cuda.synchronize()
+    rq, rs = M.quantize_act_fp8_fast(x.float().cpu().numpy())
+    assert np.array_equal(_bits(s), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
 
 
 def test_quantize_act_fp8_special_values(ft):
