@@ -98,6 +98,7 @@ _SIGNATURES = [
     ("ftmoe_moe_forward", c_i32, [ctypes.POINTER(MoeArgs), c_ptr, c_size, c_ptr]),
     ("ftmoe_moe_forward_noalloc", c_i32, [ctypes.POINTER(MoeArgs), c_ptr]),
     ("ftmoe_selftest_wait_timeout", c_i32, [ctypes.c_uint64, c_ptr, c_ptr]),
+    ("ftmoe_selftest_shared_division", c_i32, [c_ptr, c_ptr]),
     ("ftmoe_expert_slots", c_i32, [c_ptr, c_i64, c_ptr, c_ptr, c_i32, c_ptr, c_i32, c_i64, c_i32, c_ptr, c_ptr,
                                    c_ptr]),
     ("ftmoe_read_error_flags", c_i32, [ctypes.POINTER(ctypes.c_uint32)]),
@@ -318,6 +319,12 @@ def ftmoe_selftest_wait_timeout(timeout_ns, elapsed_ns=None, stream=None):
     """One bounded pipeline wait that nothing completes, given up after timeout_ns."""
     _check("ftmoe_selftest_wait_timeout", lib().ftmoe_selftest_wait_timeout(
         int(timeout_ns), _p(elapsed_ns), _stream(stream)))
+
+
+def ftmoe_selftest_shared_division(counts, stream=None):
+    """The quantizers' division by a shared group scale against IEEE division on the device;
+    counts (int64 tensor [2]) receives {quotients checked, quotients that differ}."""
+    _check("ftmoe_selftest_shared_division", lib().ftmoe_selftest_shared_division(_p(counts), _stream(stream)))
 
 
 def ftmoe_read_error_flags():

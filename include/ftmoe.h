@@ -430,6 +430,16 @@ ftmoe_status ftmoe_expert_slots(int32_t* expert_ids, int64_t routes, int32_t* sl
  * gave up (0 if it completed, which cannot happen). */
 ftmoe_status ftmoe_selftest_wait_timeout(uint64_t timeout_ns, unsigned long long* elapsed_ns, void* stream);
 
+/* Self-test of the quantizers' division (step 1 of the path: x divided by the group scale
+ * s = amax/448, gather page, Motivation). The FP8 activation and SiLU-and-mul quantizers form
+ * one reciprocal per group and correct each quotient with one fused multiply-add (Markstein's
+ * method), which must give exactly the IEEE quotient. This call compares that division with
+ * the IEEE one (__fdiv_rn) on the device, bit for bit: every divisor mantissa at three
+ * exponents against 4096 dividends each, and 1024 divisors against every dividend mantissa
+ * (111.7 G quotients). counts: device uint64[2], set to {quotients checked, quotients that
+ * differ}; read them after the stream's work completes. NULL counts: FTMOE_INVALID_ARG. */
+ftmoe_status ftmoe_selftest_shared_division(unsigned long long* counts, void* stream);
+
 /* Reads and clears the device error word of the current device (FTMOE_ERR_* bits) into
  * *flags (host pointer). Synchronises the device; not for use inside graph capture. */
 ftmoe_status ftmoe_read_error_flags(uint32_t* flags);

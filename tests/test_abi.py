@@ -88,6 +88,7 @@ def test_invalid_arguments_rejected_on_host(ft):
     # the wait self-test takes a limit of 1 us .. 1 s
     assert L.ftmoe_selftest_wait_timeout(999, None, None) == ft.FTMOE_INVALID_ARG
     assert L.ftmoe_selftest_wait_timeout(2 * 10 ** 9, None, None) == ft.FTMOE_INVALID_ARG
+    assert L.ftmoe_selftest_shared_division(None, None) == ft.FTMOE_INVALID_ARG
 
 
 def test_forward_workspace_layout(ft):

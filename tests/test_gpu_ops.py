@@ -65,6 +65,18 @@ def test_quantize_act_fp8_many_binades_bitexact(ft):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+def test_quantizer_division_equals_ieee_division(ft):
+    # the quantizers divide by the group scale through one reciprocal per group and a
+    # Markstein correction; on the device, against __fdiv_rn: every divisor mantissa at three
+    # exponents x 4098 dividends, and 1024 divisors x every dividend mantissa
+    counts = torch.zeros(2, dtype=torch.int64, device=DEV)
+    ft.ftmoe_selftest_shared_division(counts)
+    torch.cuda.synchronize()
+    checked, differ = counts.tolist()
+    assert checked == (1 << 23) * (3 * 4098 + 1024)
+    assert differ == 0
+
+
 def test_quantize_act_fp8_special_values(ft):
     x = torch.zeros(2, 256, dtype=torch.float32)
     x[0, 0], x[0, 1], x[0, 2], x[0, 3] = 448.0, -1e-6, -0.0, 1e-30
