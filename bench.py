@@ -916,8 +916,6 @@ def _cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=0xF7E00002):
     import concurrent.futures
     from oracle import cpu as C
     C.lib()  # raises if the C++ oracle cannot be built or loaded
-    if fmt == "mxfp8":
-        raise RuntimeError("the C++ oracle has no MXFP8 path")
     remap = np.full(max(used) + 1 if used else 1, -1, np.int32)
     remap[used] = np.arange(len(used), dtype=np.int32)
     ids_c = np.where(ids >= 0, remap[np.maximum(ids, 0)], -1).astype(np.int32)
@@ -925,7 +923,9 @@ def _cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=0xF7E00002):
     def quantized(job):
         e, tag, n, k = job
         raw = synth.expert_weight_fp32(n, k, seed, e, tag, "cpu").numpy()
-        return C.quantize_weight_fp8(raw) if fmt == "fp8" else C.quantize_nvfp4(raw)
+        if fmt == "fp8":
+            return C.quantize_weight_fp8(raw)
+        return C.quantize_mxfp8(raw) if fmt == "mxfp8" else C.quantize_nvfp4(raw)
 
     jobs = [(e, tag, n, k) for e in used for tag, n, k in (("gateup", 2 * I, H), ("down", H, I))]
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, C.hardware_threads())) as ex:
@@ -936,6 +936,10 @@ def _cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=0xF7E00002):
         if fmt == "fp8":
             if not ps:
                 return np.zeros((0, n, k), np.uint8), np.zeros((0, -(-n // 128), -(-k // 128)), np.float32)
+            return np.stack([p[0] for p in ps]), np.stack([p[1] for p in ps])
+        if fmt == "mxfp8":
+            if not ps:
+                return np.zeros((0, n, k), np.uint8), np.zeros((0, n, -(-k // 32)), np.uint8)
             return np.stack([p[0] for p in ps]), np.stack([p[1] for p in ps])
         if not ps:
             return (np.zeros((0, n, k), np.uint8), np.zeros((0, n, -(-k // 16)), np.uint8),
@@ -952,9 +956,9 @@ def cpu_baseline(name, budget_s=20.0, min_s=10.0):
     """Time the oracle on the first (at most 8) tokens of a call, taken as a call of their
     own, in repeated calls until at least min_s (stopping at budget_s); scale the time per
     token to one full call. The C++ oracle runs on every host thread; where it cannot be
-    built or loaded, the numpy oracle runs on one thread, token by token. FP8 quantizes per
-    token, so the sample's rows equal the full call's; NVFP4's tensor scales span the
-    sample instead (the same work per token)."""
+    built or loaded, the numpy oracle runs on one thread, token by token. FP8 and MXFP8
+    quantize per token, so the sample's rows equal the full call's; NVFP4's tensor scales
+    span the sample instead (the same work per token)."""
     T_full = WORKLOADS[name][0]
     x, ids, w, T, fmt, used = _oracle_problem(name, max_tokens=min(T_full, 8))
     n = ids.shape[0]

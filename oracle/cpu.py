@@ -37,6 +37,9 @@ def lib():
         h.ftor_nvfp4_global_scale.restype = ctypes.c_float
         h.ftor_nvfp4_global_scale.argtypes = [ctypes.c_float]
         h.ftor_quantize_nvfp4.argtypes = [_P, _I64, _I64, ctypes.c_float, _P, _P, _P]
+        h.ftor_mx_shared_exp.restype = ctypes.c_int
+        h.ftor_mx_shared_exp.argtypes = [ctypes.c_float]
+        h.ftor_quantize_mxfp8.argtypes = [_P, _I64, _I64, _P, _P]
         h.ftor_segment.restype = ctypes.c_int
         h.ftor_segment.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P]
         h.ftor_gather.argtypes = [_P, _P, _I64, _I64, _P, _I64, _P, _P]
@@ -112,6 +115,19 @@ def quantize_nvfp4(x, global_amax=None):
     return q, sb, np.float32(g[0])
 
 
+def mx_shared_exp(amax):
+    return int(lib().ftor_mx_shared_exp(ctypes.c_float(float(amax))))
+
+
+def quantize_mxfp8(x):
+    x = _c(x, np.float32)
+    rows, k = x.shape
+    q = np.zeros((rows, k), np.uint8)
+    sb = np.zeros((rows, -(-k // 32)), np.uint8)
+    lib().ftor_quantize_mxfp8(_ptr(x), rows, k, _ptr(q), _ptr(sb))
+    return q, sb
+
+
 def segment_routes(expert_ids, num_experts):
     ids = _c(expert_ids, np.int32)
     tokens, topk = ids.shape
@@ -139,7 +155,8 @@ def gather_rows_scales(src, src_scales, dst2src):
 
 def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", tokens_subset=None, threads=1):
     """The whole FFN (see cpu_oracle.cpp). Banks: fp8 (q [E, n, k] uint8, s [E, nb, kb] float32);
-    nvfp4 (q [E, n, k] unpacked codes, sb [E, n, ceil(k/16)] uint8, g [E] float32).
+    nvfp4 (q [E, n, k] unpacked codes, sb [E, n, ceil(k/16)] uint8, g [E] float32); mxfp8
+    (q [E, n, k] uint8, sb [E, n, ceil(k/32)] E8M0 bytes).
     Returns float64 [T, H] (rows outside tokens_subset are zero)."""
     x = _c(x, np.float32)
     ids = _c(expert_ids, np.int32)
@@ -153,12 +170,15 @@ def moe_forward(x, expert_ids, weights, bank_gateup, bank_down, fmt="fp8", token
     if fmt == "fp8":
         gs, ds = _c(bank_gateup[1], np.float32), _c(bank_down[1], np.float32)
         gg = dg = None
+    elif fmt == "mxfp8":
+        gs, ds = _c(bank_gateup[1], np.uint8), _c(bank_down[1], np.uint8)
+        gg = dg = None
     else:
         gs, ds = _c(bank_gateup[1], np.uint8), _c(bank_down[1], np.uint8)
         gg, dg = _c(bank_gateup[2], np.float32), _c(bank_down[2], np.float32)
     sub = None if tokens_subset is None else _c(list(tokens_subset), np.int64)
     out = np.zeros((T, H), np.float64)
-    rc = lib().ftor_moe_forward(0 if fmt == "fp8" else 1, _ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(w), _ptr(gq),
+    rc = lib().ftor_moe_forward({"fp8": 0, "nvfp4": 1, "mxfp8": 2}[fmt], _ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(w), _ptr(gq),
                                 _ptr(gs), _ptr(gg), _ptr(dq), _ptr(ds), _ptr(dg), _ptr(sub),
                                 0 if sub is None else sub.shape[0], int(threads), _ptr(out))
     if rc != 0:

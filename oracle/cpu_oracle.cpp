@@ -17,6 +17,10 @@
 //   * NVFP4 (the format the dsfp4 density page names; two-level recipe): g = fl32(amax / 2688)
 //     per tensor, sb = e4m3(fl32(amax_16 / fl32(6 g))) per 16 elements, eff = fl32(sb * g),
 //     q = e2m1(fl32(x / eff)), zero codes where eff = 0.
+//   * MXFP8 (the SGLang gather page's mxfp8 branch: a ue8m0 scale per 32; OCP Microscaling
+//     recipe): per 32 elements of a row, shared = floor(log2(amax)) - 8 clamped to
+//     [-127, 127] (amax = 0 gives -127), scale byte = shared + 127, q = e4m3(x / 2^shared);
+//     value = e4m3(q) * 2^(byte - 127).
 //   * Segmentation: a stable grouping of the active routes by expert (counting sort).
 //   * Gather: byte copies of a row and its scale row by the map.
 //   * The FFN: dequantize (code x scale, exact in double), gate/up and down products in
@@ -38,6 +42,9 @@ namespace {
 
 constexpr int kGroup = 128;     // activation group width, weight block edge
 constexpr int kNvBlock = 16;    // elements per NVFP4 block scale
+constexpr int kMxBlock = 32;    // elements per MXFP8 scale byte
+constexpr int kE8M0Bias = 127;
+constexpr int kE4M3Emax = 8;    // exponent of E4M3's largest power of two (256)
 constexpr float kE4M3Max = 448.0f;
 constexpr float kE2M1Max = 6.0f;
 
@@ -182,6 +189,31 @@ void quantize_nvfp4(const float* x, int64_t rows, int64_t k, float global_amax, 
     }
 }
 
+// floor(log2(amax)) - 8 clamped to [-127, 127]; amax = 0 gives -127. frexp writes amax as
+// m * 2^e with m in [0.5, 1), so floor(log2(amax)) = e - 1 with no logarithm taken.
+int mx_shared_exp(float amax) {
+  const double a = (double)amax;
+  if (a == 0.0) return -kE8M0Bias;
+  int e = 0;
+  (void)std::frexp(a, &e);
+  return std::min(kE8M0Bias, std::max(-kE8M0Bias, (e - 1) - kE4M3Emax));
+}
+
+// Rows of x -> e4m3 codes and one E8M0 byte per 32 elements (a partial last block takes its
+// amax over its valid elements). Dividing by 2^shared is exact in double.
+void quantize_mxfp8(const float* x, int64_t rows, int64_t k, uint8_t* q, uint8_t* sb) {
+  const int64_t nblk = ceil_div(k, kMxBlock);
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nblk; ++b) {
+      const int64_t c0 = b * kMxBlock, w = std::min<int64_t>(kMxBlock, k - c0);
+      float amax = 0.0f;
+      for (int64_t i = 0; i < w; ++i) amax = std::fmax(amax, std::fabs(x[r * k + c0 + i]));
+      const int e = mx_shared_exp(amax);
+      sb[r * nblk + b] = (uint8_t)(e + kE8M0Bias);
+      for (int64_t i = 0; i < w; ++i) q[r * k + c0 + i] = encode_e4m3((double)x[r * k + c0 + i] * std::ldexp(1.0, -e));
+    }
+}
+
 // ---------------------------------------------------------------- dequantized views
 
 // Row r of an FP8 activation / weight matrix with 128-wide scale groups, in double.
@@ -202,6 +234,15 @@ struct Nvfp4Rows {
   double at(int64_t r, int64_t c) const {
     return tables().e2m1[q[r * k + c] & 0xF] * tables().e4m3[sb[r * ceil_div(k, kNvBlock) + c / kNvBlock]] *
            (double)g;
+  }
+};
+
+struct MxRows {
+  const uint8_t* q;   // e4m3 codes
+  const uint8_t* sb;  // E8M0 bytes, one per 32 elements
+  int64_t k;
+  double at(int64_t r, int64_t c) const {
+    return tables().e4m3[q[r * k + c]] * std::ldexp(1.0, (int)sb[r * ceil_div(k, kMxBlock) + c / kMxBlock] - kE8M0Bias);
   }
 };
 
@@ -232,6 +273,12 @@ float ftor_nvfp4_global_scale(float amax) { return nvfp4_global(amax); }
 void ftor_quantize_nvfp4(const float* x, int64_t rows, int64_t k, float global_amax, uint8_t* q, uint8_t* sb,
                          float* g) {
   quantize_nvfp4(x, rows, k, global_amax, q, sb, g);
+}
+
+int ftor_mx_shared_exp(float amax) { return mx_shared_exp(amax); }
+
+void ftor_quantize_mxfp8(const float* x, int64_t rows, int64_t k, uint8_t* q, uint8_t* sb) {
+  quantize_mxfp8(x, rows, k, q, sb);
 }
 
 // Stable grouping of the active routes by expert. Returns 0, or -1 if an id >= E.
@@ -267,11 +314,12 @@ void ftor_gather(const uint8_t* src, const uint8_t* src_scales, int64_t row_byte
   }
 }
 
-// The whole FFN. fmt 0 = FP8, 1 = NVFP4.
+// The whole FFN. fmt 0 = FP8, 1 = NVFP4, 2 = MXFP8.
 //   x [T][H] float (exact bf16 values); ids [T][topk] (negative = inactive); w [T][topk].
 //   FP8 banks: q uint8 [E][n][k], scales float [E][ceil(n/128)][ceil(k/128)], g unused.
 //   NVFP4 banks: q unpacked e2m1 codes [E][n][k], scales e4m3 codes [E][n][ceil(k/16)],
-//   g float [E]. Gate/up: n = 2I (gate rows first), k = H; down: n = H, k = I.
+//   g float [E]. MXFP8 banks: q uint8 [E][n][k], scales E8M0 bytes [E][n][ceil(k/32)], g unused.
+//   Gate/up: n = 2I (gate rows first), k = H; down: n = H, k = I.
 //   subset: token indices to evaluate (NULL = all); out [T][H] double (other rows zero).
 //   The NVFP4 tensor scales span the whole call (all tokens; all active routes for the
 //   intermediate) even when a subset is evaluated.
@@ -292,6 +340,9 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
   if (fmt == 0) {
     xs.resize((size_t)(T * ceil_div(H, kGroup)));
     quantize_act_fp8(x, T, H, xq.data(), xs.data());
+  } else if (fmt == 2) {
+    xsb.resize((size_t)(T * ceil_div(H, kMxBlock)));
+    quantize_mxfp8(x, T, H, xq.data(), xsb.data());
   } else {
     float amax = 0.0f;
     for (int64_t i = 0; i < T * H; ++i) amax = std::fmax(amax, std::fabs(x[i]));
@@ -300,6 +351,7 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
   }
   auto xval = [&](int64_t t, int64_t c) {
     if (fmt == 0) return Fp8Rows{xq.data(), xs.data(), H, ceil_div(H, kGroup), 1}.at(t, c);
+    if (fmt == 2) return MxRows{xq.data(), xsb.data(), H}.at(t, c);
     return Nvfp4Rows{xq.data(), xsb.data(), xg, H}.at(t, c);
   };
   // 2. routes: the evaluated tokens' active routes; NVFP4 needs every active route's
@@ -337,6 +389,9 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
           if (fmt == 0) {
             const float* s = static_cast<const float*>(gs) + (size_t)e * ceil_div(N2, kGroup) * ceil_div(H, kGroup);
             wv = Fp8Rows{q, s, H, ceil_div(H, kGroup), kGroup}.at(n, c);
+          } else if (fmt == 2) {
+            const uint8_t* sb = static_cast<const uint8_t*>(gs) + (size_t)e * N2 * ceil_div(H, kMxBlock);
+            wv = MxRows{q, sb, H}.at(n, c);
           } else {
             const uint8_t* sb = static_cast<const uint8_t*>(gs) + (size_t)e * N2 * ceil_div(H, kNvBlock);
             wv = Nvfp4Rows{q, sb, gg[e], H}.at(n, c);
@@ -361,6 +416,10 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
     as.assign((size_t)(T * topk * ceil_div(I, kGroup)), 0.0f);
     for (int64_t r = 0; r < T * topk; ++r)
       if (ids[r] >= 0) quantize_act_fp8(a.data() + r * I, 1, I, aq.data() + r * I, as.data() + r * ceil_div(I, kGroup));
+  } else if (fmt == 2) {
+    asb.assign((size_t)(T * topk * ceil_div(I, kMxBlock)), 0);
+    for (int64_t r = 0; r < T * topk; ++r)
+      if (ids[r] >= 0) quantize_mxfp8(a.data() + r * I, 1, I, aq.data() + r * I, asb.data() + r * ceil_div(I, kMxBlock));
   } else {
     float amax = 0.0f;
     for (int64_t r = 0; r < T * topk; ++r)
@@ -381,8 +440,9 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
       if (!wanted[(size_t)rt.t]) continue;
       const int64_t r = rt.t * topk + rt.j;
       for (int64_t c = 0; c < I; ++c)
-        arow[(size_t)c] = fmt == 0 ? Fp8Rows{aq.data(), as.data(), I, ceil_div(I, kGroup), 1}.at(r, c)
-                                   : Nvfp4Rows{aq.data(), asb.data(), ag, I}.at(r, c);
+        arow[(size_t)c] = fmt == 0   ? Fp8Rows{aq.data(), as.data(), I, ceil_div(I, kGroup), 1}.at(r, c)
+                          : fmt == 2 ? MxRows{aq.data(), asb.data(), I}.at(r, c)
+                                     : Nvfp4Rows{aq.data(), asb.data(), ag, I}.at(r, c);
       for (int64_t h = 0; h < H; ++h) {
         double acc = 0.0;
         for (int64_t c = 0; c < I; ++c) {
@@ -390,6 +450,9 @@ int ftor_moe_forward(int fmt, const float* x, int64_t T, int64_t H, int64_t I, i
           if (fmt == 0) {
             const float* s = static_cast<const float*>(ds) + (size_t)e * ceil_div(H, kGroup) * ceil_div(I, kGroup);
             wv = Fp8Rows{q, s, I, ceil_div(I, kGroup), kGroup}.at(h, c);
+          } else if (fmt == 2) {
+            const uint8_t* sb = static_cast<const uint8_t*>(ds) + (size_t)e * H * ceil_div(I, kMxBlock);
+            wv = MxRows{q, sb, I}.at(h, c);
           } else {
             const uint8_t* sb = static_cast<const uint8_t*>(ds) + (size_t)e * H * ceil_div(I, kNvBlock);
             wv = Nvfp4Rows{q, sb, dg[e], I}.at(h, c);

@@ -44,7 +44,7 @@ def test_vs_baseline_only_for_workloads_the_pages_time():
 
 def test_cpu_baseline_oracle_call_equals_the_numpy_oracle():
     # the bench's CPU-baseline call (C++ oracle over a bank compacted to the used experts)
-    # computes the numpy oracle's forward, in both formats and with no active route
+    # computes the numpy oracle's forward, in every format and with no active route
     import numpy as np
 
     import synth
@@ -54,7 +54,7 @@ def test_cpu_baseline_oracle_call_equals_the_numpy_oracle():
     ids = synth.routes(T, k, E, seed, active_per_token=[3, 2, 0, 3], device="cpu").numpy()
     w = synth.routing_weights(T, k, seed, "cpu").numpy()
     used = sorted(set(int(e) for e in ids.reshape(-1) if e >= 0))
-    for fmt in ("fp8", "nvfp4"):
+    for fmt in ("fp8", "nvfp4", "mxfp8"):
         bg = M.LazyBank(lambda e: synth.expert_weight_fp32(2 * I, H, seed, e, "gateup", "cpu").numpy(), 2 * I, fmt)
         bd = M.LazyBank(lambda e: synth.expert_weight_fp32(H, I, seed, e, "down", "cpu").numpy(), H, fmt)
         got = bench._cpp_oracle_call(x, ids, w, used, fmt, H, I, seed=seed)(4)

@@ -3,8 +3,8 @@
 It is a second, independently written oracle of the same definitions. Its pins:
 - the numpy oracle, itself pinned in test_oracle_formats.py and test_oracle_pipeline.py:
   codecs, encoders, quantizers, segmenter and gather bit for bit;
-- the per-element brute-force dense FFN loops of test_oracle_pipeline.py (no grouping, no
-  matmul) for the whole forward in both formats;
+- the per-element brute-force dense FFN loops of test_oracle_pipeline.py and
+  test_oracle_mxfp8.py (no grouping, no matmul) for the whole forward in all three formats;
 - the decode page's inactive-route invariants;
 - thread-count independence.
 """
@@ -14,6 +14,7 @@ import pytest
 from oracle import cpu as C
 from oracle import formats as F
 from oracle import moe as M
+from test_oracle_mxfp8 import _dense_ffn_brute_mx
 from test_oracle_pipeline import _dense_ffn_brute, _dense_ffn_brute_nvfp4, _tiny_problem
 
 
@@ -94,7 +95,38 @@ def test_segment_and_gather_match_the_numpy_oracle(T, k, E, frac):
 
 
 def _bank(b, fmt):
-    return (b.q, b.s) if fmt == "fp8" else (b.q, b.s, b.g)
+    return (b.q, b.s) if fmt in ("fp8", "mxfp8") else (b.q, b.s, b.g)
+
+
+def test_mxfp8_quantizer_matches_the_numpy_oracle():
+    rng = np.random.default_rng(34)
+    x = rng.standard_normal((6, 200)).astype(np.float32) * rng.uniform(1e-3, 1e3, (6, 1)).astype(np.float32)
+    x[1, 32:64] = 0.0                # a zero block: byte 0 (shared -127), zero codes
+    x[2, :7] = -1e-30                # negatives that round to zero keep their sign
+    x[3, 64] = 3.0e38                # the clamp at +127
+    x[4, 96:128] = 1.875 * 2.0 ** 5  # a block maximum that saturates to 448 under 2^(5-8)
+    x[5, 160:192] = 0.0
+    x[5, 160] = 1e-40                # a block whose maximum is subnormal: the clamp at -127
+    q, sb = C.quantize_mxfp8(x)
+    qr, sbr = M.quantize_mxfp8(x)
+    assert np.array_equal(q, qr) and np.array_equal(sb, sbr)
+    for a in (0.0, 1e-40, 1.0, 448.0, 255.9, 256.0, 3.0e38, 2.0 ** -126):
+        assert C.mx_shared_exp(a) == M.mx_shared_exp(a), a
+
+
+def test_mxfp8_forward_matches_per_element_brute_force():
+    rng = np.random.default_rng(35)
+    T, H, I, E, k = 3, 256, 128, 4, 2
+    x = F.bf16_bits_to_f32(F.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)))
+    bg = M.quantize_bank((rng.standard_normal((E, 2 * I, H)) * 0.02).astype(np.float32), "mxfp8")
+    bd = M.quantize_bank((rng.standard_normal((E, H, I)) * 0.02).astype(np.float32), "mxfp8")
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[2, 0] = -1
+    logits = rng.standard_normal((T, k))
+    wts = (np.exp(logits) / np.exp(logits).sum(1, keepdims=True)).astype(np.float32)
+    ref = _dense_ffn_brute_mx(x, ids, wts, bg, bd)
+    got = C.moe_forward(x, ids, wts, _bank(bg, "mxfp8"), _bank(bd, "mxfp8"), fmt="mxfp8")
+    assert np.allclose(got, ref, rtol=1e-9, atol=1e-12 * np.max(np.abs(ref)))
 
 
 def test_fp8_forward_matches_per_element_brute_force():
@@ -116,7 +148,7 @@ def test_nvfp4_forward_matches_per_element_brute_force():
     assert np.allclose(got, ref, rtol=1e-9, atol=1e-12 * np.max(np.abs(ref)))
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "mxfp8"])
 def test_forward_matches_the_numpy_oracle_and_does_not_depend_on_threads(fmt):
     x, ids, wts, _, _ = _tiny_problem(33, T=12, H=256, I=128, E=6, k=3)
     rng = np.random.default_rng(33)
