@@ -366,6 +366,8 @@ bool use_fused(const ftmoe_moe_shape* s) {
 // be won. The automatic path keeps the combine kernel.
 bool use_comb(const ftmoe_moe_shape* s) {
   if (s->path != 5 || s->format != FTMOE_FMT_FP8 || s->num_experts > kTcGemmMaxExperts) return false;
+  // the combine warps stage a token's slots in registers and shared memory: at most 8
+  if (s->topk > 8) return false;
   if (!tc_gemm_pairs_ok(s->hidden, s->inter)) return false;
   const int tile = s->tok_tile ? s->tok_tile : pick_tile_value(s->tokens * s->topk, s->num_experts);
   return tile == 64 || tile == 128;

@@ -309,7 +309,7 @@ ftmoe_status ftmoe_combine(const float* y, int64_t ld_y, const int32_t* route2ds
  * H and I multiples of 128, H <= 8192, I <= 2048; a token that lists one expert twice
  * computes that expert once and weights it per listing),
  * 5 = grouped path with the combine inside the down GEMM (FP8; token tile 64 or 128,
- * H % 256 == 0, I % 128 == 0; out 16-byte aligned with ld_out % 4 == 0): the down GEMM runs
+ * topk <= 8, H % 256 == 0, I % 128 == 0; out 16-byte aligned with ld_out % 4 == 0): the down GEMM runs
  * on CTA pairs, counts the arrivals of each token's routes per 128 columns and, at the last,
  * adds the token's rows in ascending slot order with the combine's expression and rounding
  * (decode page, first section: the reduction after the down GEMM), so no fp32 row has to

@@ -177,6 +177,7 @@ def test_automatic_forward_path_choice(ft):
     assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, fmt=ft.FMT_NVFP4, path=5))["counters_bytes"] == 0
     assert lay(ft.moe_shape(4096, 7168, 2048, 6, 256, fmt=ft.FMT_MXFP8, path=5))["counters_bytes"] == 0
     assert lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=5))["counters_bytes"] == 0             # tile 16
+    assert lay(ft.moe_shape(4096, 7168, 2048, 9, 256, path=5))["counters_bytes"] == 0         # topk > 8
     with pytest.raises(ft.FtmoeError):
         lay(ft.moe_shape(8, 4096, 1024, 8, 64, path=6))
 
