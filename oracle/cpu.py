@@ -22,33 +22,37 @@ def lib():
     """The loaded C++ oracle, built on first use if needed."""
     global _lib
     if _lib is None:
-        path = build_cpu_oracle.build()
-        h = ctypes.CDLL(path)
-        h.ftor_e4m3_decode.restype = ctypes.c_double
-        h.ftor_e4m3_decode.argtypes = [ctypes.c_uint8]
-        h.ftor_e2m1_decode.restype = ctypes.c_double
-        h.ftor_e2m1_decode.argtypes = [ctypes.c_uint8]
-        h.ftor_e4m3_encode.restype = ctypes.c_uint8
-        h.ftor_e4m3_encode.argtypes = [ctypes.c_double]
-        h.ftor_e2m1_encode.restype = ctypes.c_uint8
-        h.ftor_e2m1_encode.argtypes = [ctypes.c_double]
-        h.ftor_quantize_act_fp8.argtypes = [_P, _I64, _I64, _P, _P]
-        h.ftor_quantize_weight_fp8.argtypes = [_P, _I64, _I64, _P, _P]
-        h.ftor_nvfp4_global_scale.restype = ctypes.c_float
-        h.ftor_nvfp4_global_scale.argtypes = [ctypes.c_float]
-        h.ftor_quantize_nvfp4.argtypes = [_P, _I64, _I64, ctypes.c_float, _P, _P, _P]
-        h.ftor_mx_shared_exp.restype = ctypes.c_int
-        h.ftor_mx_shared_exp.argtypes = [ctypes.c_float]
-        h.ftor_quantize_mxfp8.argtypes = [_P, _I64, _I64, _P, _P]
-        h.ftor_segment.restype = ctypes.c_int
-        h.ftor_segment.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P]
-        h.ftor_gather.argtypes = [_P, _P, _I64, _I64, _P, _I64, _P, _P]
-        h.ftor_moe_forward.restype = ctypes.c_int
-        h.ftor_moe_forward.argtypes = [ctypes.c_int, _P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
-                                       _P, _P, _P, _I64, ctypes.c_int, _P]
-        h.ftor_hardware_threads.restype = ctypes.c_int
-        _lib = h
+        _lib = bind(ctypes.CDLL(build_cpu_oracle.build()))
     return _lib
+
+
+def bind(h):
+    """Sets the C signatures on a loaded oracle library (also used for copies of it that the
+    tests build with planted mistakes); returns it."""
+    h.ftor_e4m3_decode.restype = ctypes.c_double
+    h.ftor_e4m3_decode.argtypes = [ctypes.c_uint8]
+    h.ftor_e2m1_decode.restype = ctypes.c_double
+    h.ftor_e2m1_decode.argtypes = [ctypes.c_uint8]
+    h.ftor_e4m3_encode.restype = ctypes.c_uint8
+    h.ftor_e4m3_encode.argtypes = [ctypes.c_double]
+    h.ftor_e2m1_encode.restype = ctypes.c_uint8
+    h.ftor_e2m1_encode.argtypes = [ctypes.c_double]
+    h.ftor_quantize_act_fp8.argtypes = [_P, _I64, _I64, _P, _P]
+    h.ftor_quantize_weight_fp8.argtypes = [_P, _I64, _I64, _P, _P]
+    h.ftor_nvfp4_global_scale.restype = ctypes.c_float
+    h.ftor_nvfp4_global_scale.argtypes = [ctypes.c_float]
+    h.ftor_quantize_nvfp4.argtypes = [_P, _I64, _I64, ctypes.c_float, _P, _P, _P]
+    h.ftor_mx_shared_exp.restype = ctypes.c_int
+    h.ftor_mx_shared_exp.argtypes = [ctypes.c_float]
+    h.ftor_quantize_mxfp8.argtypes = [_P, _I64, _I64, _P, _P]
+    h.ftor_segment.restype = ctypes.c_int
+    h.ftor_segment.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P]
+    h.ftor_gather.argtypes = [_P, _P, _I64, _I64, _P, _I64, _P, _P]
+    h.ftor_moe_forward.restype = ctypes.c_int
+    h.ftor_moe_forward.argtypes = [ctypes.c_int, _P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                   _P, _P, _P, _I64, ctypes.c_int, _P]
+    h.ftor_hardware_threads.restype = ctypes.c_int
+    return h
 
 
 def _ptr(a):
