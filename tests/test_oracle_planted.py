@@ -137,3 +137,65 @@ def test_planted_constant_in_the_numpy_mxfp8_recipe_fails_a_pin(monkeypatch, con
         except Exception:  # noqa: BLE001 - a failed assertion or a shape the pin cannot use
             failures += 1
     assert failures > 0, f"{const} = {value} passed every MXFP8 pin"
+
+
+# numpy oracle (oracle/moe.py): each mistake is written into a copy of the module's source,
+# the copy is executed as a module of its own, and the pins of test_oracle_pipeline.py run
+# with it in place of the real module.
+NUMPY_MUTANTS = [
+    ("gate and up swapped", "g, u = gu[:, :inter], gu[:, inter:]", "u, g = gu[:, :inter], gu[:, inter:]"),
+    ("weight block scales transposed", "sc = np.repeat(np.repeat(np.asarray(s, np.float64), GROUP, axis=0)",
+     "sc = np.repeat(np.repeat(np.asarray(s, np.float64).T, GROUP, axis=0)"),
+    ("routing weight dropped", "out[t] += np.float64(weights[t, j]) * y_rows[(t, j)]", "out[t] += y_rows[(t, j)]"),
+    ("unstable segment order", 'order = active[np.argsort(flat[active], kind="stable")]',
+     'order = active[::-1][np.argsort(flat[active][::-1], kind="stable")]'),
+    ("route index in place of the token index", "dst2src = (order // topk).astype(np.int32)",
+     "dst2src = order.astype(np.int32)"),
+    ("multiply by 448 / amax instead of dividing by s", "v = (vals32 / s).astype(np.float32)",
+     "v = (vals32 * (np.float32(E4M3_MAX) / amax)).astype(np.float32)"),
+    ("intermediate not re-quantized", "adeq_all, _ = quantize_acts(A, fmt, gamax)",
+     "adeq_all = A.astype(np.float64)"),
+]
+
+
+def _numpy_mutant(text, repl):
+    import types
+    path = os.path.join(os.path.dirname(M.__file__), "moe.py")
+    src = open(path).read()
+    if text is not None:
+        assert src.count(text) == 1, text
+        src = src.replace(text, repl)
+    mod = types.ModuleType("oracle.moe_planted")
+    mod.__package__ = "oracle"
+    mod.__file__ = path
+    exec(compile(src, path, "exec"), mod.__dict__)
+    return mod
+
+
+def _pipeline_pins_failing(monkeypatch, mod):
+    import inspect
+
+    import test_oracle_pipeline as P
+    monkeypatch.setattr(P, "M", mod)
+    failing = []
+    for name, fn in sorted(vars(P).items()):
+        if not name.startswith("test_") or not callable(fn):
+            continue
+        params = inspect.signature(fn).parameters
+        calls = [()] if not params else [(8, 8, 64, 0.5), (37, 6, 16, 0.0)]
+        for args in calls:
+            try:
+                fn(*args)
+            except Exception:  # noqa: BLE001 - a failed assertion or an operand the pin cannot use
+                failing.append(name)
+                break
+    return failing
+
+
+def test_unmodified_numpy_copy_passes_the_pipeline_pins(monkeypatch):
+    assert _pipeline_pins_failing(monkeypatch, _numpy_mutant(None, None)) == []
+
+
+@pytest.mark.parametrize("name,text,repl", NUMPY_MUTANTS, ids=[m[0] for m in NUMPY_MUTANTS])
+def test_planted_mistake_in_the_numpy_oracle_fails_a_pin(monkeypatch, name, text, repl):
+    assert _pipeline_pins_failing(monkeypatch, _numpy_mutant(text, repl)), f"'{name}' passed every pin"
