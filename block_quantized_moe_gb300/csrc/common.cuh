@@ -47,12 +47,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // Two floats -> two e4m3 codes (round to nearest even, saturate to +-448), packed with
 // the first value in the low byte. Uses the cuda_fp8.h conversion.
 __device__ __forceinline__ uint16_t f2_to_e4m3x2(float a, float b) {
@@ -68,21 +62,10 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t c) {
   return __half2float(__half(h));
 }
 
-// Two e4m3 codes (low byte first) -> two floats.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c2) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
-  return __half22float2(__half2(h));
-}
-
 // Two floats -> two e2m1 codes in one byte (first value in the low nibble), round to
 // nearest even with saturation to +-6 (cuda_fp4.h conversion).
 __device__ __forceinline__ uint8_t f2_to_e2m1x2(float a, float b) {
   return (uint8_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
-}
-
-__device__ __forceinline__ float2 e2m1x2_to_f2(uint8_t c2) {
-  __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)c2, __NV_E2M1);
-  return __half22float2(__half2(h));
 }
 
 __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
